@@ -1,0 +1,358 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Pins used here (none re-types the oracle's formula):
+  * numpy's IEEE binary16 conversion (exhaustive / randomized),
+  * hand-written packing words and the byte layout the pages describe,
+  * exact rational arithmetic (fractions.Fraction) with an independent
+    round-to-nearest-even search over all binary16 values,
+  * closed forms (zero update, constant (q - z) per group),
+  * torch's binary64 matmul as an independent contraction,
+  * invariants (power-of-two scale invariance of the norm, split iterations).
+"""
+import bisect
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# ---------------------------------------------------------------------------
+# independent exact rounding to binary16 (bisection over all finite halves)
+# ---------------------------------------------------------------------------
+_POS_HALVES = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64).tolist()
+
+
+def rne_half_bits(v: Fraction) -> int:
+    """Round an exact rational to binary16 bits (RNE, overflow to inf)."""
+    sign = 0x8000 if v < 0 else 0
+    a = -v if v < 0 else v
+    if a >= Fraction(65520):
+        return sign | 0x7C00
+    i = bisect.bisect_right(_POS_HALVES, a) - 1  # _POS_HALVES[i] <= a
+    lo = Fraction(_POS_HALVES[i])
+    if lo == a:
+        return sign | i
+    hi = Fraction(_POS_HALVES[i + 1])
+    dlo, dhi = a - lo, hi - a
+    if dlo < dhi or (dlo == dhi and i % 2 == 0):
+        return sign | i
+    return sign | (i + 1)
+
+
+def half_frac(h) -> Fraction:
+    return Fraction(float(np.float16(h)))
+
+
+# ---------------------------------------------------------------------------
+# FP16 conversions
+# ---------------------------------------------------------------------------
+
+def test_half_to_double_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits.tolist()])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_double_to_half_against_numpy():
+    rng = np.random.default_rng(1)
+    xs = [0.0, -0.0, 65504.0, 65519.99, 65520.0, -65520.0, 1e9, -1e-30, 2.0 ** -25,
+          2.0 ** -24, 3 * 2.0 ** -26, 6.1e-5, float("inf"), -float("inf")]
+    # exact midpoints between neighbouring halves (ties) and their neighbours
+    h = np.arange(1, 0x7BFF, 37, dtype=np.uint16).view(np.float16).astype(np.float64)
+    h2 = (np.arange(1, 0x7BFF, 37, dtype=np.uint16) + 1).view(np.float16).astype(np.float64)
+    mids = (h + h2) / 2
+    xs += mids.tolist() + (-mids).tolist()
+    xs += np.nextafter(mids, np.inf).tolist() + np.nextafter(mids, -np.inf).tolist()
+    xs += (rng.standard_normal(20000) * 10.0 ** rng.uniform(-9, 5, 20000)).tolist()
+    for x in xs:
+        ref = int(np.array([x], dtype=np.float64).astype(np.float16).view(np.uint16)[0])
+        assert oracle.double_to_half(x) == ref, (x, hex(ref))
+
+
+# ---------------------------------------------------------------------------
+# Packing
+# ---------------------------------------------------------------------------
+
+def _golden_pack_vectors():
+    out = []
+    with open(os.path.join(GOLDEN, "pack_vectors.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            parts = line.split()
+            bits = int(parts[0])
+            codes = [int(t) for t in parts[1:-1]]
+            word = int(parts[-1], 16)
+            out.append((bits, codes, word))
+    return out
+
+
+def test_golden_pack_vectors():
+    vecs = _golden_pack_vectors()
+    assert len(vecs) >= 8
+    for bits, codes, word in vecs:
+        assert len(codes) == 32 // bits
+        got = oracle.pack(np.array([codes], dtype=np.uint8), bits)
+        assert got.shape == (1, 1)
+        assert int(got[0, 0]) == word, (bits, codes, hex(int(got[0, 0])), hex(word))
+        back = oracle.unpack(got, len(codes), bits)
+        assert back[0].tolist() == codes
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_pack_byte_layout(bits):
+    """K/2 (INT4) or K/4 (INT2) bytes per row; byte j holds codes
+    (8/bits)*j ... in increasing bit position."""
+    rng = np.random.default_rng(2)
+    N, K = 7, 256
+    codes = rng.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    W = oracle.pack(codes, bits)
+    assert W.dtype == np.uint32 and W.shape == (N, K * bits // 32)
+    raw = W.astype("<u4").view(np.uint8).reshape(N, K * bits // 8)
+    per = 8 // bits
+    expect = np.zeros((N, K // per), dtype=np.uint8)
+    for j in range(per):
+        expect |= (codes[:, j::per] << (bits * j)).astype(np.uint8)
+    assert np.array_equal(raw, expect)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_pack_roundtrip_and_mask(bits):
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 256, size=(5, 128), dtype=np.uint8)
+    W = oracle.pack(codes, bits)
+    back = oracle.unpack(W, 128, bits)
+    assert np.array_equal(back, codes & ((1 << bits) - 1))
+    W2 = oracle.pack(back, bits)
+    assert np.array_equal(W, W2)
+
+
+# ---------------------------------------------------------------------------
+# Dequantization
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits,group", [(4, 128), (2, 64), (4, 32), (2, 128)])
+def test_dequant_exact(bits, group):
+    """Every dequantized weight equals the exact rational (q - z) * s."""
+    rng = synth.rng_for(4)
+    N, K = 6, 256
+    codes, s, z = synth.quant_weights(rng, N, K, bits, group)
+    W = oracle.pack(codes, bits)
+    w = oracle.dequant(W, s, z, K, bits, group)
+    for n in range(N):
+        for k in range(K):
+            g = k // group
+            exact = (Fraction(int(codes[n, k])) - half_frac(z[n, g])) * half_frac(s[n, g])
+            assert Fraction(w[n, k]) == exact
+
+
+def test_dequant_special_cases():
+    # s = 1, z = 0: w = q (plain integer codes)
+    codes = np.arange(16, dtype=np.uint8).reshape(1, 16).repeat(2, 0)
+    W = oracle.pack(codes, 4)
+    one = np.ones((2, 1), np.float16)
+    zero = np.zeros((2, 1), np.float16)
+    w = oracle.dequant(W, one, zero, 16, 4, 16)
+    assert np.array_equal(w, codes.astype(np.float64))
+    # q == z (integer zero point): w = 0
+    z8 = np.full((2, 1), 8.0, np.float16)
+    W8 = oracle.pack(np.full((2, 16), 8, np.uint8), 4)
+    assert np.all(oracle.dequant(W8, one * 3, z8, 16, 4, 16) == 0.0)
+
+
+# ---------------------------------------------------------------------------
+# The GEMM
+# ---------------------------------------------------------------------------
+
+def _exact_gemm_bits(A, codes, s, z, group):
+    M, K = A.shape
+    N = codes.shape[0]
+    Af = [[half_frac(A[m, k]) for k in range(K)] for m in range(M)]
+    out = np.zeros((M, N), dtype=np.uint16)
+    for n in range(N):
+        wn = [(Fraction(int(codes[n, k])) - half_frac(z[n, k // group])) * half_frac(s[n, k // group])
+              for k in range(K)]
+        for m in range(M):
+            acc = sum((Af[m][k] * wn[k] for k in range(K)), Fraction(0))
+            out[m, n] = rne_half_bits(acc)
+    return out
+
+
+@pytest.mark.parametrize("bits,group,M,N,K", [(4, 128, 3, 5, 256), (2, 64, 2, 4, 192),
+                                              (4, 32, 4, 3, 96), (2, 128, 1, 6, 128)])
+def test_gemm_brute_force_exact(bits, group, M, N, K):
+    """quant_gemm == round-to-nearest-even of the exact rational sum."""
+    case = synth.gemm_case(M, N, K, bits, group, seed=5)
+    W = oracle.pack(case["codes"], bits)
+    C = oracle.quant_gemm(case["A"], W, case["scales"], case["zeros"], bits, group)
+    ref = _exact_gemm_bits(case["A"], case["codes"], case["scales"], case["zeros"], group)
+    assert np.array_equal(C.view(np.uint16), ref)
+
+
+def test_gemm_closed_form_zero():
+    """All codes 8 with integer zero point 8: every output is +0 exactly."""
+    M, N, K, g = 4, 9, 256, 128
+    rng = synth.rng_for(6)
+    A = synth.activations(rng, M, K)
+    W = oracle.pack(np.full((N, K), 8, np.uint8), 4)
+    s = rng.uniform(0.005, 0.02, (N, K // g)).astype(np.float16)
+    z = np.full((N, K // g), 8.0, np.float16)
+    C = oracle.quant_gemm(A, W, s, z, 4, g)
+    assert np.all(C.view(np.uint16) == 0)
+
+
+@pytest.mark.parametrize("bits,group", [(4, 128), (2, 64)])
+def test_gemm_closed_form_constant_offset(bits, group):
+    """q - z == 1/2 everywhere with one scale per row:
+    C[m, n] = RNE(s_n / 2 * sum_k A[m, k]) -- pins rows vs columns."""
+    M, N, K = 5, 7, 512
+    rng = synth.rng_for(7)
+    A = synth.activations(rng, M, K)
+    G = K // group
+    qg = rng.integers(1, 1 << bits, size=(N, G), dtype=np.uint8)
+    codes = np.repeat(qg, group, axis=1)
+    z = (qg.astype(np.float64) - 0.5).astype(np.float16)
+    srow = rng.uniform(0.01, 0.05, size=(N, 1)).astype(np.float16)
+    s = np.repeat(srow, G, axis=1)
+    C = oracle.quant_gemm(A, oracle.pack(codes, bits), s, z, bits, group)
+    for m in range(M):
+        rs = sum((half_frac(a) for a in A[m]), Fraction(0))
+        for n in range(N):
+            assert int(C.view(np.uint16)[m, n]) == rne_half_bits(half_frac(srow[n, 0]) / 2 * rs)
+
+
+def test_gemm_against_torch_float64():
+    torch = pytest.importorskip("torch")
+    case = synth.gemm_case(16, 96, 512, 4, 128, seed=8)
+    W = oracle.pack(case["codes"], 4)
+    w = oracle.dequant(W, case["scales"], case["zeros"], 512, 4, 128)
+    ref = (torch.from_numpy(case["A"].astype(np.float64)) @ torch.from_numpy(w).T).numpy()
+    C = oracle.quant_gemm(case["A"], W, case["scales"], case["zeros"], 4, 128)
+    ref16 = ref.astype(np.float16)
+    diff = np.abs(C.astype(np.float64) - ref16.astype(np.float64))
+    ulp = np.abs(np.spacing(ref16.astype(np.float16))).astype(np.float64)
+    assert np.all(diff <= ulp)
+    assert np.mean(C.view(np.uint16) == ref16.view(np.uint16)) > 0.999
+
+
+def test_gemm_points_match_full():
+    case = synth.gemm_case(9, 40, 256, 2, 64, seed=9)
+    W = oracle.pack(case["codes"], 2)
+    C = oracle.quant_gemm(case["A"], W, case["scales"], case["zeros"], 2, 64)
+    rng = np.random.default_rng(0)
+    pm = rng.integers(0, 9, 50)
+    pn = rng.integers(0, 40, 50)
+    pts = oracle.quant_gemm_points(case["A"], W, case["scales"], case["zeros"], 2, 64, pm, pn)
+    assert np.array_equal(pts.view(np.uint16), C.view(np.uint16)[pm, pn])
+
+
+# ---------------------------------------------------------------------------
+# RMS norm of the loop block
+# ---------------------------------------------------------------------------
+
+def test_rms_norm_closed_forms():
+    # eps = 0: a constant row normalizes to +-1 exactly; a one-hot row of
+    # length 4 to 2 exactly (sqrt(mean) = |a| / 2).
+    x = np.array([[3.5] * 8, [-0.25] * 8], np.float32)
+    h = oracle.rms_norm_half(x, eps=0.0)
+    assert np.array_equal(h.astype(np.float32), np.array([[1.0] * 8, [-1.0] * 8], np.float32))
+    x = np.array([[5.0, 0, 0, 0], [0, 0, -7.0, 0]], np.float32)
+    h = oracle.rms_norm_half(x, eps=0.0)
+    assert np.array_equal(h.astype(np.float32), np.array([[2, 0, 0, 0], [0, 0, -2, 0]], np.float32))
+
+
+def test_rms_norm_power_of_two_invariance():
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((6, 64)).astype(np.float32)
+    h = oracle.rms_norm_half(x, eps=0.0)
+    for j in (-6, 3, 11):
+        assert np.array_equal(oracle.rms_norm_half(x * np.float32(2.0 ** j), eps=0.0).view(np.uint16),
+                              h.view(np.uint16))
+    m2 = np.mean(h.astype(np.float64) ** 2, axis=1)
+    assert np.all(np.abs(m2 - 1.0) < 2e-3)
+
+
+# ---------------------------------------------------------------------------
+# Loop block
+# ---------------------------------------------------------------------------
+
+def _tiny_block(bits, seed, D=64, F=128, M=2):
+    case = synth.block_case(M, bits, group=32 if bits == 4 else 64, seed=seed, D=D, F=F)
+    blk = {k: (oracle.pack(c, bits), s, z) for k, (c, s, z) in case["proj"].items()}
+    return case, blk
+
+
+def _exact_block_once(x, case):
+    """One un-normalized block application with exact sums, independent rounding."""
+    g = case["group"]
+    x = x.astype(np.float32)
+    h = np.array([[rne_half_bits(Fraction(float(v))) for v in row] for row in x], np.uint16).view(np.float16)
+
+    def q(a, name):
+        codes, s, z = case["proj"][name]
+        return _exact_gemm_bits(a, codes, s, z, g).view(np.float16)
+
+    D = case["D"]
+    qkv = q(h, "qkv")
+    o = q(np.ascontiguousarray(qkv[:, :D]), "o")
+    u = q(o, "up")
+    u = np.where(u.astype(np.float64) > 0, u, np.float16(0)).astype(np.float16)
+    d = q(u, "down")
+    return (x + d.astype(np.float32)).astype(np.float32)  # numpy FP32 add, IEEE rounding
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_loop_block_brute_force(bits):
+    case, blk = _tiny_block(bits, seed=11)
+    x1 = oracle.loop_block(case["x0"], blk, bits, case["group"], L=1, normalize=False)
+    ref = _exact_block_once(case["x0"], case)
+    assert np.array_equal(x1.view(np.uint32), ref.view(np.uint32))
+    x2 = oracle.loop_block(case["x0"], blk, bits, case["group"], L=2, normalize=False)
+    ref2 = _exact_block_once(ref, case)
+    assert np.array_equal(x2.view(np.uint32), ref2.view(np.uint32))
+
+
+def test_loop_block_zero_update():
+    """A DOWN projection with q == z (integer) adds exactly zero: x is unchanged."""
+    case, blk = _tiny_block(4, seed=12)
+    W, s, z = blk["down"]
+    N, KW = W.shape
+    K = KW * 8
+    W0 = oracle.pack(np.full((N, K), 5, np.uint8), 4)
+    blk["down"] = (W0, s, np.full_like(z, 5.0))
+    for norm in (True, False):
+        x = oracle.loop_block(case["x0"], blk, 4, case["group"], L=3, normalize=norm)
+        assert np.array_equal(x.view(np.uint32), case["x0"].view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_loop_block_split_invariant(bits):
+    """Warm-start invariant: running L1 iterations and then L - L1 from the
+    saved residual equals running L iterations at once, bit for bit."""
+    case, blk = _tiny_block(bits, seed=13, D=64, F=128, M=3)
+    g = case["group"]
+    full = oracle.loop_block(case["x0"], blk, bits, g, L=5)
+    mid = oracle.loop_block(case["x0"], blk, bits, g, L=2)
+    rest = oracle.loop_block(mid, blk, bits, g, L=3)
+    assert np.array_equal(full.view(np.uint32), rest.view(np.uint32))
+    assert not np.array_equal(full.view(np.uint32), case["x0"].view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_loop_block_full_width_stays_finite(bits):
+    """With the pre-norm the D = 2048 block stays finite over 16 iterations."""
+    case = synth.block_case(1, bits, seed=0)
+    blk = {k: (oracle.pack(c, bits), s, z) for k, (c, s, z) in case["proj"].items()}
+    x = oracle.loop_block(case["x0"], blk, bits, case["group"], L=16, normalize=True)
+    assert np.all(np.isfinite(x))
+    assert np.max(np.abs(x)) > 10.0
