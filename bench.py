@@ -1,0 +1,526 @@
+#!/usr/bin/env python
+"""Benchmark of the weight-only quantized linear layer (quant_gemm) on GB300.
+
+Headline workload (one step): the INT4 decode pass over the four projections
+of the D = 2048 loop block -- QKV 2048->6144, O 2048->2048, UP 2048->8192,
+DOWN 8192->2048, group 128 -- at M = 1, 4 and 16 tokens (12 GEMMs per step).
+Metric: effective HBM bandwidth, algorithmic bytes / time, where one GEMM
+moves N*K*bits/8 (codes) + 4*N*K/group (FP16 scales + zeros) + 2*M*K (A) +
+2*M*N (C) bytes.  Weights, scales and zeros are rotated over enough copies
+(> 1.5x L2) that every GEMM reads them from HBM.
+
+The same JSON line also carries the INT2 decode pass, the tensor-core prefill
+GEMMs and the loop block (secondary workloads), the roofline of the dominant
+kernel, the clocks seen during the timed region, an end-to-end number through
+the C ABI with host buffers, and the CPU oracle timed on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tlq|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DECODE_MS = (1, 4, 16)
+PREFILL_MS = (128, 512, 2048)
+PROJ = synth.PROJ_ORDER
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def gemm_bytes(M, N, K, bits, group):
+    return N * K * bits // 8 + 4 * N * K // group + 2 * M * K + 2 * M * N
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the library arm
+# ---------------------------------------------------------------------------
+class Workload:
+    """Packed weights (rotated copies), activations and outputs on the GPU."""
+
+    def __init__(self, tlq, torch, bits, Ms, shapes, copies, seed=0, a_scale=1.0):
+        self.tlq, self.torch = tlq, torch
+        self.bits = bits
+        self.group = synth.DIST[bits]["group"]
+        self.Ms = Ms
+        self.shapes = shapes
+        rng = synth.rng_for(seed)
+        base = {}
+        for name, (N, K) in shapes.items():
+            codes, s, z = synth.quant_weights(rng, N, K, bits, self.group)
+            W = tlq.pack_weights(torch.from_numpy(codes).cuda(), bits)
+            base[name] = (W, torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda())
+        self.copies = [base] + [{k: tuple(t.clone() for t in v) for k, v in base.items()} for _ in range(copies - 1)]
+        self.A = {}
+        self.C = {}
+        for M in Ms:
+            for name, (N, K) in shapes.items():
+                self.A[M, name] = torch.from_numpy(synth.activations(rng, M, K, a_scale)).cuda()
+                self.C[M, name] = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        torch.cuda.synchronize()
+        self.step_bytes = sum(gemm_bytes(M, N, K, bits, self.group) for M in Ms for (N, K) in shapes.values())
+        self.step_flops = sum(2 * M * N * K for M in Ms for (N, K) in shapes.values())
+        self.launches = len(Ms) * len(shapes)
+        self.weight_set_bytes = sum(N * K * bits // 8 + 4 * N * K // self.group for (N, K) in shapes.values())
+
+    def run_step(self, i, stream=None):
+        ncopy = len(self.copies)
+        for j, M in enumerate(self.Ms):
+            cp = self.copies[(len(self.Ms) * i + j) % ncopy]
+            for name in self.shapes:
+                W, s, z = cp[name]
+                self.tlq.tl_quant_gemm(self.A[M, name], W, s, z, self.C[M, name], self.bits, self.group, stream)
+
+
+def capture_steps(torch, wl, phases):
+    """One CUDA graph per rotation phase; step i replays graph i % phases."""
+    graphs = []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for p in range(phases):  # warm the launch path outside capture
+            wl.run_step(p)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for p in range(phases):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            wl.run_step(p)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    return graphs
+
+
+def time_graphs(torch, graphs, steps, warmup, dist=None):
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        graphs[i % len(graphs)].replay()
+    e1.record()
+    e1.synchronize()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1)
+
+
+def copies_for(weight_set_bytes, per_step_sets, l2_bytes):
+    """Rotation copies such that a weight set is reused only after more than
+    1.5x L2 of other weights went by (multiple of the per-step sets)."""
+    n = per_step_sets
+    while (n - 1) * weight_set_bytes < 1.5 * l2_bytes:
+        n += per_step_sets
+    return n
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "weight_only_int4_quant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# dram bytes (read + write) per launch of the decode kernel for the headline
+# step, from the ncu capture summarised in profiles/ (None until captured for
+# the current kernel source).
+NCU_TRAFFIC = {"kernel_hash": None, "bytes_per_launch": None}
+
+
+def run_tlq(args, rank, world, dist):
+    import torch
+
+    import weight_only_int4_quant_gb300 as tlq
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    tlq.load()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    peaks = measured_peaks()
+    result = {}
+
+    # ---- headline: INT4 decode, D = 2048 projections, M in {1, 4, 16} ----
+    probe_set = sum(N * K // 2 + 4 * N * K // 128 for (N, K) in synth.SHAPES.values())
+    ncopy = copies_for(probe_set, len(DECODE_MS), l2)
+    wl4 = Workload(tlq, torch, 4, DECODE_MS, synth.SHAPES, ncopy)
+    phases = ncopy // len(DECODE_MS)
+    graphs = capture_steps(torch, wl4, phases)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = time_graphs(torch, graphs, args.steps, args.warmup, dist)
+    clocks = clk.summary()
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    value = world * wl4.step_bytes * args.steps / (ms_max * 1e-3) / 1e9
+    per_rank_gbs = wl4.step_bytes / (ms_step * 1e-3) / 1e9
+    launch_us = ms_step * 1e3 / wl4.launches
+
+    # per-GEMM breakdown (graphs of one GEMM shape, rotated copies)
+    per_gemm = {}
+    for M in DECODE_MS:
+        for name, (N, K) in synth.SHAPES.items():
+            b = gemm_bytes(M, N, K, 4, 128)
+            sub = Workload.__new__(Workload)
+            sub.__dict__.update(wl4.__dict__)
+            sub.Ms = (M,)
+            sub.shapes = {name: (N, K)}
+            gs = capture_steps(torch, sub, ncopy)
+            t = time_graphs(torch, gs, max(60, ncopy * 8), 10)
+            us = t * 1e3 / max(60, ncopy * 8)
+            per_gemm["M%d_%s" % (M, name)] = {"us": round(us, 2), "GBps": round(b / (us * 1e-6) / 1e9, 1)}
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = run_e2e(tlq, torch, wl4, max(20, min(args.steps, 200)))
+
+    # ---- secondary: INT2 decode ----
+    probe2 = sum(N * K // 4 + 4 * N * K // 64 for (N, K) in synth.SHAPES.values())
+    n2 = copies_for(probe2, len(DECODE_MS), l2)
+    wl2 = Workload(tlq, torch, 2, DECODE_MS, synth.SHAPES, n2, seed=1)
+    g2 = capture_steps(torch, wl2, n2 // len(DECODE_MS))
+    k2 = max(50, args.steps // 4)
+    t2 = time_graphs(torch, g2, k2, args.warmup)
+    result["int2_decode"] = {"GBps": round(wl2.step_bytes * k2 / (t2 * 1e-3) / 1e9, 1),
+                             "ms_per_step": round(t2 / k2, 5),
+                             "frac_of_hbm": round(wl2.step_bytes * k2 / (t2 * 1e-3) / 1e9 / peaks["hbm"], 3)}
+    del wl2, g2
+
+    # ---- secondary: prefill GEMMs on tensor cores ----
+    result["prefill"] = run_prefill(tlq, torch, peaks)
+
+    # ---- secondary: loop block ----
+    result["loop_block"] = run_loop_block(tlq, torch)
+
+    torch.cuda.synchronize()
+    traffic = None
+    if NCU_TRAFFIC["kernel_hash"] == kernel_hash() and NCU_TRAFFIC["bytes_per_launch"]:
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    avg_launch_bytes = wl4.step_bytes / wl4.launches
+    achieved = avg_launch_bytes / (launch_us * 1e-6) / 1e9
+    line = {
+        "metric": "quant_gemm GB/s (decode) & TFLOP/s (prefill), % of GB300 roofline",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp16",
+        "data": "synthetic (seeded; codes uniform 0..15, scales U[0.005,0.02], zeros U[6,9], A ~ N(0,1))",
+        "config": {
+            "workload": "INT4 decode, group 128, QKV 2048->6144 / O 2048->2048 / UP 2048->8192 / DOWN "
+                        "8192->2048 at M = 1, 4, 16 (12 GEMMs per step)",
+            "bytes_per_step": wl4.step_bytes,
+            "l2": "weights/scales/zeros rotated over %d copies (%.0f MB > L2 %.0f MB)" % (
+                ncopy, ncopy * wl4.weight_set_bytes / 1e6, l2 / 1e6),
+            "launch": "CUDA graph per step, programmatic dependent launch between GEMMs",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm"], 3), "traffic": traffic,
+                     "peak_source": peaks["src"], "kernel": "decode_kernel (all 12 launches of a step)"},
+        "per_gemm": per_gemm,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": wl4.launches * args.steps,
+    }
+    line.update(result)
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl4)
+    return line
+
+
+def run_e2e(tlq, torch, wl, steps):
+    """Per step: pinned host -> device copy of every activation, the 12 C-ABI
+    calls, device -> pinned host copy of every output."""
+    hostA = {k: v.cpu().pin_memory() for k, v in wl.A.items()}
+    hostC = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in wl.C.items()}
+    h2d = sum(v.numel() * 2 for v in hostA.values())
+    d2h = sum(v.numel() * 2 for v in hostC.values())
+
+    def one(i):
+        for k, v in hostA.items():
+            wl.A[k].copy_(v, non_blocking=True)
+        wl.run_step(i)
+        for k, v in hostC.items():
+            v.copy_(wl.C[k], non_blocking=True)
+
+    for i in range(5):
+        one(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": round(wl.step_bytes * steps / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3 / steps, 4)}
+
+
+def run_prefill(tlq, torch, peaks):
+    out = {}
+    try:
+        for M in PREFILL_MS:
+            wl = Workload(tlq, torch, 4, (M,), synth.SHAPES, 1, seed=2, a_scale=0.5)
+            gs = capture_steps(torch, wl, 1)
+            steps = 20 if M >= 2048 else 50
+            t = time_graphs(torch, gs, steps, 5)
+            tf = wl.step_flops * steps / (t * 1e-3) / 1e12
+            out["M%d" % M] = {"TFLOPs": round(tf, 1), "ms_per_step": round(t / steps, 4),
+                              "frac_of_bf16_peak": round(tf / peaks["bf16"], 3)}
+            del wl, gs
+    except tlq.TLQError as e:
+        return {"unavailable": str(e)}
+    return out
+
+
+def run_loop_block(tlq, torch):
+    out = {}
+    try:
+        for bits in (4, 2):
+            for M in (1, 128):
+                case = synth.block_case(M, bits, seed=3)
+                proj = {}
+                for name, (codes, s, z) in case["proj"].items():
+                    proj[name] = (tlq.pack_weights(torch.from_numpy(codes).cuda(), bits),
+                                  torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda())
+                blk = tlq.LoopBlock(proj, bits, case["group"], M)
+                x0 = torch.from_numpy(case["x0"]).cuda()
+                for L in (4, 8, 16):
+                    x = x0.clone()
+                    blk.forward(x, L)  # warm
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        blk.forward(x, L)
+                    for _ in range(3):
+                        g.replay()
+                    torch.cuda.synchronize()
+                    reps = 20
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(reps):
+                        g.replay()
+                    e1.record()
+                    e1.synchronize()
+                    ms = e0.elapsed_time(e1) / reps
+                    wbytes = sum(N * K * bits // 8 + 4 * N * K // case["group"]
+                                 for (N, K) in [(6144, 2048), (2048, 2048), (8192, 2048), (2048, 8192)])
+                    out["int%d_M%d_L%d" % (bits, M, L)] = {
+                        "ms": round(ms, 4), "us_per_iter": round(ms * 1e3 / L, 2),
+                        "eff_GBps": round(L * wbytes / (ms * 1e-3) / 1e9, 1),
+                        "TFLOPs": round(L * 2 * M * 50331648 / (ms * 1e-3) / 1e12, 2)}
+                del blk, proj
+    except tlq.TLQError as e:
+        out["unavailable"] = str(e)
+    return out
+
+
+def cpu_baseline(wl):
+    """The CPU oracle as it stands (single thread) on one full headline step,
+    on the same inputs (weights of rotation copy 0)."""
+    import oracle
+
+    cp = wl.copies[0]
+    host = {}
+    for name in wl.shapes:
+        W, s, z = cp[name]
+        host[name] = (W.cpu().numpy().view(np.uint32), s.cpu().numpy(), z.cpu().numpy())
+    As = {k: v.cpu().numpy() for k, v in wl.A.items()}
+    t0 = time.perf_counter()
+    for M in wl.Ms:
+        for name in wl.shapes:
+            W, s, z = host[name]
+            oracle.quant_gemm(As[M, name], W, s, z, wl.bits, wl.group)
+    dt = time.perf_counter() - t0
+    return {"value": round(wl.step_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "one full step (12 GEMMs: 4 projections x M = 1, 4, 16), %.1f s" % dt}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def run_reference(args, budget_s=60.0):
+    """Each reference step is the M = 1 slice of the headline step (4 GEMMs),
+    restricted to the first rows of every projection so that the whole run
+    takes about ``budget_s`` seconds of single-thread CPU time."""
+    import oracle
+
+    rng = synth.rng_for(0)
+    host = {}
+    for name, (N, K) in synth.SHAPES.items():
+        codes, s, z = synth.quant_weights(rng, N, K, 4, 128)
+        host[name] = (oracle.pack(codes, 4), s, z)
+    M = 1
+    A = {name: synth.activations(rng, M, K) for name, (N, K) in synth.SHAPES.items()}
+
+    def step(rows):
+        for name in synth.SHAPES:
+            W, s, z = host[name]
+            n = rows[name]
+            oracle.quant_gemm(A[name], W[:n], s[:n], z[:n], 4, 128)
+
+    full = {name: N for name, (N, K) in synth.SHAPES.items()}
+    t0 = time.perf_counter()
+    step(full)  # calibration (untimed)
+    t_full = time.perf_counter() - t0
+    frac = min(1.0, budget_s / max(1e-9, (args.steps + args.warmup) * t_full))
+    rows = {name: max(8, int(N * frac) // 8 * 8) for name, N in full.items()}
+    sample_bytes = sum(gemm_bytes(M, rows[name], K, 4, 128) for name, (N, K) in synth.SHAPES.items())
+    for _ in range(args.warmup):
+        step(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(rows)
+    dt = time.perf_counter() - t0
+    v = sample_bytes * args.steps / dt / 1e9
+    sample = "4 GEMMs at M = 1 per step, first %s output rows of QKV/O/UP/DOWN" % (
+        "/".join(str(rows[n]) for n in synth.SHAPES))
+    return {
+        "impl": "reference",
+        "metric": "quant_gemm GB/s (decode) & TFLOP/s (prefill), % of GB300 roofline",
+        "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same distributions)",
+        "config": {"workload": "INT4 decode, group 128, QKV 2048->6144 / O 2048->2048 / UP 2048->8192 / DOWN "
+                               "8192->2048; reference steps are bounded samples (M = 1 rows)"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--impl", choices=("tlq", "reference"), default="tlq")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = run_tlq(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

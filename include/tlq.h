@@ -1,0 +1,191 @@
+/*
+ * tlq.h -- C ABI of the GB300 (sm_103a) weight-only quantized linear layer.
+ *
+ * One shared library (libtlq.so) implements the hot path of the TinyLoop
+ * looped-transformer runtime: the quantized linear layer quant_gemm (routed
+ * to the INT4 or INT2 kernels) and the shared-weight loop block that reapplies
+ * one set of projections L times.
+ *
+ * Data types in this header are plain C: FP16 values are passed as their
+ * IEEE-754 binary16 bit patterns (uint16_t), FP32 as float.  Every pointer
+ * argument is a DEVICE pointer (cudaMalloc / torch CUDA tensor memory)
+ * unless the comment says otherwise; `stream` is a cudaStream_t passed as
+ * void* (NULL = the legacy default stream).
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: the caller owns all memory.  No entry point allocates device
+ *    memory or keeps state between calls.
+ *  - Ordering: calls are asynchronous and ordered on `stream`.  The library
+ *    holds no shared scratch, so calls on different streams with disjoint
+ *    buffers may run concurrently; one model instance is meant to drive one
+ *    stream ("Model", section "Thread safety": a single CUDA stream for all
+ *    forward-pass work).
+ *  - Errors: arguments are checked on the host before anything is launched.
+ *    A rejected call returns TLQ_EINVAL (bad argument) or TLQ_EUNSUPPORTED
+ *    (valid but not implemented, e.g. a group size the kernels do not take)
+ *    and launches nothing; a failed launch returns TLQ_ECUDA.  The message of
+ *    the last failure on the calling thread names the failing argument or
+ *    step ("Model", section "Raises": errors name the failure point).
+ *  - Device waits are bounded: a kernel that gives up on a wait records
+ *    TLQ_ETIMEOUT in a device status word and returns; tl_check_status()
+ *    reports it.
+ *  - Determinism: identical inputs give bit-identical outputs on every call
+ *    (no floating-point atomics, fixed reduction order) -- "Model", section
+ *    "Determinism".
+ */
+#ifndef TLQ_H_
+#define TLQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TLQ_OK = 0,
+  TLQ_EINVAL = 1,       /* an argument is invalid; nothing was launched      */
+  TLQ_EUNSUPPORTED = 2, /* valid request this build does not implement       */
+  TLQ_ECUDA = 3,        /* a CUDA runtime/driver call failed                 */
+  TLQ_ETIMEOUT = 4      /* a device-side wait hit its limit (see status)     */
+} tlq_status;
+
+/* Message of the last failure on the calling thread ("" if none).  The
+ * string is owned by the library and valid until the next call on the same
+ * thread. */
+const char* tl_last_error(void);
+
+/* Library version string, e.g. "tlq 0.1 sm_103a". */
+const char* tl_version(void);
+
+/*
+ * tl_quant_gemm -- the quantized linear layer (quant_gemm).
+ *
+ *   C[m][n] = fp16( sum_k A[m][k] * w[n][k] ),  w[n][k] = (q[n][k] - z[n][g]) * s[n][g],
+ *   g = k / group, accumulated in FP32 on the GPU.
+ *
+ * Source: "Model" (TinyLoop Python API), "VRAM cost", Weights -- each
+ * quantized layer holds INT2 / INT4 packed data, FP16 scales and FP16 zeros;
+ * "beta-Informed Deployment Features", CTX-TIER, "What Phase 2 ships" -- the
+ * dispatcher routes on the weight's bit width (INT4 kernel or int2_gemm).
+ *
+ *   A       FP16 [M][K], row-major, row stride K elements, 16-byte aligned.
+ *   Wpacked uint32 [N][K*bits/32], the format tl_pack_weights writes: row n
+ *           is K-contiguous, code j of a word at bits [bits*j, bits*j+bits).
+ *           16-byte aligned.
+ *   scales  FP16 [N][K/group], row-major.
+ *   zeros   FP16 [N][K/group], row-major (zero points, need not be integral).
+ *   C       FP16 [M][N], row-major, row stride N; must not overlap A.
+ *   M >= 1; N >= 1 and a multiple of 8; K >= 1 with K % group == 0.
+ *   bits    4 or 2.
+ *   group   a multiple of 32 (bits = 4) or 64 (bits = 2), dividing K;
+ *           group = K (one scale per row) is allowed.
+ *   M <= 16 runs the bandwidth-bound decode kernel, larger M the tensor-core
+ *   (tcgen05) prefill kernel.
+ * Returns TLQ_OK, TLQ_EINVAL (null pointer, misalignment, bad shape/bits/
+ * group), or TLQ_ECUDA.
+ */
+tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint16_t* scales,
+                         const uint16_t* zeros, uint16_t* C, int M, int N, int K, int bits,
+                         int group, void* stream);
+
+/*
+ * tl_pack_weights -- pack quantization codes into the kernels' weight format.
+ *
+ * Source: "beta-Informed Deployment Features", CTX-TIER, "Details of the
+ * shipped kernel": an INT4 row takes K/2 bytes, an INT2 row K/4 bytes, four
+ * INT2 codes per byte.  The bit order is this library's reading (LSB first).
+ *
+ *   codes   uint8 [N][K] device array, one code per byte; only the low `bits`
+ *           bits of each byte are stored.
+ *   Wpacked uint32 [N][K*bits/32] output.
+ *   K % (32/bits) == 0.  Bit-exact; deterministic.
+ */
+tlq_status tl_pack_weights(const uint8_t* codes, uint32_t* Wpacked, int N, int K, int bits,
+                           void* stream);
+
+/* Inverse of tl_pack_weights: codes[n][k] = code k of row n (0 .. 2^bits-1). */
+tlq_status tl_unpack_weights(const uint32_t* Wpacked, uint8_t* codes, int N, int K, int bits,
+                             void* stream);
+
+/* One quantized projection of the loop block: weights [N][K] in the packed
+ * format, FP16 scales/zeros [N][K/group]. */
+typedef struct {
+  const uint32_t* W;
+  const uint16_t* s;
+  const uint16_t* z;
+  int N;
+  int K;
+} tl_qproj;
+
+/*
+ * The shared-weight loop block (one weight set reused every iteration).
+ *   qkv  : N = 3*D, K = D        o    : N = D, K = D
+ *   up   : N = F,   K = D        down : N = D, K = F
+ * Scratch buffers are caller-owned device FP16 arrays with at least M rows:
+ *   h [M][D], qkv_out [M][3D], o_out [M][D], up_out [M][F].
+ * normalize = 1 applies the per-row RMS pre-norm h = fp16(x / sqrt(mean x^2 +
+ * 1e-5)) before the QKV projection (the block's LayerNorm position, "Model",
+ * "VRAM cost", with buf.norm as its FP16 output); 0 feeds fp16(x) directly.
+ */
+typedef struct {
+  tl_qproj qkv, o, up, down;
+  int bits;
+  int group;
+  int D;
+  uint16_t* h;
+  uint16_t* qkv_out;
+  uint16_t* o_out;
+  uint16_t* up_out;
+  int normalize;
+} tl_block;
+
+/*
+ * tl_loop_block_forward -- apply the shared block L times to the FP32
+ * residual stream x[M][D] in place:
+ *
+ *   for l in 0..L-1:
+ *     h   = fp16(rmsnorm(x))            (or fp16(x) when normalize = 0)
+ *     qkv = quant_gemm(h, qkv)          [M][3D]
+ *     o   = quant_gemm(qkv[:, :D], o)   [M][D]   (row stride 3D)
+ *     u   = relu(quant_gemm(o, up))     [M][F]   relu(v) = v > 0 ? v : +0
+ *     x  += float(quant_gemm(u, down))  FP32 add of the FP16 result
+ *
+ * Source: "Model", "VRAM cost", Runtime buffers (buf.main is the FP32
+ * residual, the scratch buffers are FP16); "Warm-start mid-loop", internal
+ * flow, "Extend loop" (the block is re-run in place on the residual, so
+ * running L1 then L - L1 iterations equals running L, bit for bit).
+ *   x      FP32 [M][D] device array, updated in place.
+ *   block  HOST pointer to a tl_block describing device buffers.
+ *   L >= 0 (L = 0 is a no-op); M >= 1.
+ * With TLQ_LOG=1 in the environment the first call on a device prints
+ * whether the block's packed weights fit in L2 and the kernel choice.
+ */
+tlq_status tl_loop_block_forward(float* x, const tl_block* block, int L, int M, void* stream);
+
+/*
+ * Synchronize `stream` and report the device status word: TLQ_OK, or
+ * TLQ_ETIMEOUT if a kernel gave up on a bounded wait since the last
+ * tl_reset_status().  Also returns TLQ_ECUDA on an asynchronous CUDA error.
+ */
+tlq_status tl_check_status(void* stream);
+
+/* Clear the device status word of the current device; synchronizes `stream`. */
+tlq_status tl_reset_status(void* stream);
+
+/*
+ * Self-test of the bounded device waits (no counterpart on the pages; it
+ * backs the library's own failure-detection contract).  Launches a one-thread
+ * kernel that waits on a shared-memory barrier nothing ever arrives at; the
+ * wait gives up after limit_us microseconds (1 .. 1,000,000), records
+ * TLQ_ETIMEOUT in the status word and the kernel returns normally, leaving the
+ * context usable.  Read the result with tl_check_status().
+ */
+tlq_status tl_selftest_wait_timeout(unsigned limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TLQ_H_ */

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every entry point include/tlq.h declares, and rejects
+bad arguments before launching anything."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tlq.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tl_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    import weight_only_int4_quant_gb300 as tlq
+
+    tlq.build()
+    return tlq.load()
+
+
+def test_header_declares_expected_entry_points():
+    import weight_only_int4_quant_gb300 as tlq
+
+    assert header_functions() == sorted(tlq.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(clib):
+    for name in header_functions():
+        assert hasattr(clib, name), name
+        assert ctypes.cast(getattr(clib, name), ctypes.c_void_p).value
+
+
+def test_version(clib):
+    import weight_only_int4_quant_gb300 as tlq
+
+    assert "sm_103a" in tlq.tl_version()
+
+
+def _gemm(clib, A=16, W=16, s=16, z=16, C=4096, M=1, N=8, K=128, bits=4, group=128):
+    return clib.tl_quant_gemm(A, W, s, z, C, M, N, K, bits, group, None)
+
+
+def test_gemm_rejects_bad_arguments_without_launching(clib):
+    import weight_only_int4_quant_gb300 as tlq
+
+    # null pointers
+    assert _gemm(clib, A=None) == tlq.TLQ_EINVAL
+    assert "null" in tlq.tl_last_error()
+    assert _gemm(clib, C=None) == tlq.TLQ_EINVAL
+    # bit width, shapes, groups
+    assert _gemm(clib, bits=3) == tlq.TLQ_EINVAL and "bits" in tlq.tl_last_error()
+    assert _gemm(clib, bits=8) == tlq.TLQ_EINVAL
+    assert _gemm(clib, M=0) == tlq.TLQ_EINVAL and "M=" in tlq.tl_last_error()
+    assert _gemm(clib, N=0) == tlq.TLQ_EINVAL
+    assert _gemm(clib, K=0) == tlq.TLQ_EINVAL
+    assert _gemm(clib, group=48) == tlq.TLQ_EINVAL and "group" in tlq.tl_last_error()
+    assert _gemm(clib, bits=2, group=32) == tlq.TLQ_EINVAL  # INT2 groups are multiples of 64
+    assert _gemm(clib, K=192, group=128) == tlq.TLQ_EINVAL and "multiple of group" in tlq.tl_last_error()
+    assert _gemm(clib, N=12) == tlq.TLQ_EINVAL
+    # alignment and aliasing
+    assert _gemm(clib, A=18) == tlq.TLQ_EINVAL and "aligned" in tlq.tl_last_error()
+    assert _gemm(clib, W=20) == tlq.TLQ_EINVAL
+    assert _gemm(clib, A=4096, C=4096 + 64) == tlq.TLQ_EINVAL and "overlap" in tlq.tl_last_error()
+
+
+def test_pack_and_block_reject_bad_arguments(clib):
+    import weight_only_int4_quant_gb300 as tlq
+
+    assert clib.tl_pack_weights(None, 16, 4, 64, 4, None) == tlq.TLQ_EINVAL
+    assert clib.tl_pack_weights(16, 16, 4, 60, 4, None) == tlq.TLQ_EINVAL  # K % 8
+    assert clib.tl_pack_weights(16, 16, 4, 64, 5, None) == tlq.TLQ_EINVAL
+    assert clib.tl_unpack_weights(16, 16, 4, 72, 2, None) == tlq.TLQ_EINVAL  # K % 16
+    assert clib.tl_loop_block_forward(None, None, 1, 1, None) == tlq.TLQ_EINVAL
+    blk = tlq._Block()
+    blk.D = 64
+    assert clib.tl_loop_block_forward(16, ctypes.byref(blk), 1, 1, None) == tlq.TLQ_EINVAL
+    assert clib.tl_loop_block_forward(16, ctypes.byref(blk), -1, 1, None) == tlq.TLQ_EINVAL
+    assert clib.tl_selftest_wait_timeout(0, None) == tlq.TLQ_EINVAL
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import weight_only_int4_quant_gb300 as tlq
+
+    monkeypatch.setattr(tlq, "_lib", None)
+    monkeypatch.setattr(tlq, "_LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        tlq.load()

@@ -1,0 +1,229 @@
+"""GPU parity of tl_pack_weights / tl_unpack_weights / tl_quant_gemm against
+the CPU oracle, through the C ABI (Python binding = argument marshalling)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import assert_close, assert_points_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_pack(lib, codes, bits):
+    return lib.pack_weights(dev(codes), bits)
+
+
+def run_case(lib, case):
+    bits, group = case["bits"], case["group"]
+    Wd = gpu_pack(lib, case["codes"], bits)
+    C = lib.quant_gemm(dev(case["A"]), Wd, dev(case["scales"]), dev(case["zeros"]), bits, group)
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+    return Wd, C.cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# packing: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("N,K", [(1, 64), (37, 256), (640, 2048), (3, 8192)])
+def test_pack_unpack_bit_exact(lib, bits, N, K):
+    rng = np.random.default_rng(N * 131 + K + bits)
+    codes = rng.integers(0, 256, size=(N, K), dtype=np.uint8)  # high bits must be dropped
+    W = gpu_pack(lib, codes, bits)
+    ref = oracle.pack(codes, bits)
+    assert np.array_equal(W.cpu().numpy().view(np.uint32), ref)
+    back = lib.unpack_weights(W, K, bits).cpu().numpy()
+    assert np.array_equal(back, oracle.unpack(ref, K, bits))
+
+
+# ---------------------------------------------------------------------------
+# decode path (M <= 16): element-wise against the oracle on small shapes that
+# still span several tiles, k-splits and a ragged row tile
+# ---------------------------------------------------------------------------
+
+DECODE_SHAPES = [
+    # bits, group, N, K
+    (4, 128, 256, 1024),
+    (4, 128, 200, 2048),
+    (4, 32, 96, 512),
+    (4, 64, 136, 384),
+    (4, 512, 64, 1024),
+    (4, 4096, 64, 4096),   # one scale per row
+    (2, 64, 256, 1024),
+    (2, 128, 120, 2048),
+    (2, 64, 72, 448),
+    (2, 2048, 64, 2048),   # one scale per row
+]
+
+
+@pytest.mark.parametrize("bits,group,N,K", DECODE_SHAPES)
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+def test_decode_matches_oracle(lib, bits, group, N, K, M):
+    case = synth.gemm_case(M, N, K, bits, group, seed=M * 1000 + N + K)
+    _, C = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(C, ref, "int%d g%d M%d N%d K%d" % (bits, group, M, N, K))
+
+
+@pytest.mark.parametrize("M", [2, 5, 7, 12, 15])
+def test_decode_other_token_counts(lib, M):
+    case = synth.gemm_case(M, 512, 2048, 4, 128, seed=M)
+    _, C = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], 4), case["scales"], case["zeros"], 4, 128)
+    assert_close(C, ref, "M%d" % M)
+
+
+def test_decode_closed_form_zero(lib):
+    """codes 8 with integer zero point 8: every output is 0 up to the FP32
+    cancellation of the kernel's offset terms (sum_k a_k (base_k + q_k) minus
+    its correction sums, |.| ~ 1024 * sum|a| * 2^-24 * s per set), far below
+    the 1e-2 * |row| bound that random weights give (|C| ~ 3 here)."""
+    M, N, K = 4, 256, 1024
+    rng = synth.rng_for(3)
+    A = synth.activations(rng, M, K)
+    codes = np.full((N, K), 8, np.uint8)
+    s = rng.uniform(0.005, 0.02, (N, K // 128)).astype(np.float16)
+    z = np.full((N, K // 128), 8.0, np.float16)
+    C = lib.quant_gemm(dev(A), gpu_pack(lib, codes, 4), dev(s), dev(z), 4, 128).cpu().numpy()
+    assert np.max(np.abs(C.astype(np.float32))) < 1e-3
+
+
+def test_decode_deterministic(lib):
+    case = synth.gemm_case(16, 2048, 8192, 4, 128, seed=7)
+    Wd = gpu_pack(lib, case["codes"], 4)
+    A, s, z = dev(case["A"]), dev(case["scales"]), dev(case["zeros"])
+    c1 = lib.quant_gemm(A, Wd, s, z, 4, 128)
+    c2 = lib.quant_gemm(A, Wd, s, z, 4, 128)
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# full-size decode configurations (the four D = 2048 projections), sampled
+# outputs against the oracle evaluated point by point
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("proj", list(synth.SHAPES))
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_decode_full_size_sampled(lib, bits, proj, M):
+    N, K = synth.SHAPES[proj]
+    group = synth.DIST[bits]["group"]
+    case = synth.gemm_case(M, N, K, bits, group, seed=0)
+    Wd, C = run_case(lib, case)
+    rng = np.random.default_rng(M + N)
+    P = 512
+    pm = rng.integers(0, M, P)
+    pn = rng.integers(0, N, P)
+    ref = oracle.quant_gemm_points(case["A"], Wd.cpu().numpy().view(np.uint32), case["scales"], case["zeros"],
+                                   bits, group, pm, pn)
+    assert_points_close(C[pm, pn], ref, "int%d %s M%d" % (bits, proj, M))
+
+
+def test_gemv_config_full_oracle(lib):
+    """M = 1, K = N = 2048, INT4 group 128: every output against the oracle."""
+    case = synth.gemm_case(1, 2048, 2048, 4, 128, seed=0)
+    _, C = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], 4), case["scales"], case["zeros"], 4, 128)
+    assert_close(C, ref, "gemv")
+
+
+# ---------------------------------------------------------------------------
+# error paths and the bounded-wait self test
+# ---------------------------------------------------------------------------
+
+def test_gpu_argument_errors(lib):
+    A = torch.zeros((1, 128), dtype=torch.float16, device="cuda")
+    W = torch.zeros((8, 16), dtype=torch.int32, device="cuda")
+    s = torch.zeros((8, 1), dtype=torch.float16, device="cuda")
+    C = torch.zeros((1, 8), dtype=torch.float16, device="cuda")
+    with pytest.raises(lib.TLQError, match="group"):
+        lib.tl_quant_gemm(A, W, s, s, C, 4, 96)
+    # a one-row slice at an 8-byte offset is "contiguous" for torch but not
+    # 16-byte aligned: rejected before launch
+    Aoff = torch.zeros((1, 136), dtype=torch.float16, device="cuda")[:, 4:132]
+    assert Aoff.is_contiguous()
+    with pytest.raises(lib.TLQError, match="aligned"):
+        lib.tl_quant_gemm(Aoff, W, s, s, C, 4, 128)
+    lib.tl_quant_gemm(Aoff.clone(), W, s, s, C, 4, 128)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(C) == 0
+
+
+def test_bounded_wait_reports_timeout(lib):
+    lib.tl_reset_status()
+    lib.tl_selftest_wait_timeout(2000)
+    with pytest.raises(lib.TLQError) as ei:
+        lib.tl_check_status()
+    assert ei.value.status == lib.TLQ_ETIMEOUT
+    lib.tl_reset_status()
+    lib.tl_check_status()
+    # the context is still usable
+    case = synth.gemm_case(1, 64, 128, 4, 128, seed=1)
+    run_case(lib, case)
+
+
+# ---------------------------------------------------------------------------
+# prefill path (M > 16, tcgen05): element-wise against the oracle on shapes
+# with ragged token / row / k tails, every k-split, and full-size samples
+# ---------------------------------------------------------------------------
+
+PREFILL_SHAPES = [
+    # bits, group, M, N, K
+    (4, 128, 128, 256, 1024),
+    (4, 128, 17, 264, 512),
+    (4, 128, 200, 512, 2048),
+    (4, 32, 96, 256, 96),      # K not a multiple of the 64-wide stage, two groups per stage
+    (4, 64, 300, 520, 384),
+    (4, 1024, 130, 256, 1024),  # one scale per row
+    (2, 64, 128, 256, 1024),
+    (2, 64, 33, 136, 448),
+    (2, 128, 256, 512, 2048),
+    (2, 512, 160, 256, 512),
+]
+
+
+@pytest.mark.parametrize("bits,group,M,N,K", PREFILL_SHAPES)
+def test_prefill_matches_oracle(lib, bits, group, M, N, K):
+    case = synth.gemm_case(M, N, K, bits, group, seed=M + N + K, a_scale=0.5)
+    _, C = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(C, ref, "prefill int%d g%d M%d N%d K%d" % (bits, group, M, N, K))
+
+
+@pytest.mark.parametrize("ks", ["1", "2", "4", "8"])
+@pytest.mark.parametrize("bits", [4, 2])
+def test_prefill_every_k_split(lib, monkeypatch, bits, ks):
+    group = synth.DIST[bits]["group"]
+    case = synth.gemm_case(150, 512, 2048, bits, group, seed=11, a_scale=0.5)
+    monkeypatch.setenv("TLQ_PREFILL_KSPLIT", ks)
+    Wd, C = run_case(lib, case)
+    C2 = lib.quant_gemm(dev(case["A"]), Wd, dev(case["scales"]), dev(case["zeros"]), bits, group)
+    assert torch.equal(torch.from_numpy(C).cuda().view(torch.int16), C2.view(torch.int16)), "not deterministic"
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(C, ref, "prefill ksplit %s int%d" % (ks, bits))
+
+
+@pytest.mark.parametrize("proj", list(synth.SHAPES))
+@pytest.mark.parametrize("M", [128, 512, 2048])
+def test_prefill_full_size_sampled(lib, proj, M):
+    N, K = synth.SHAPES[proj]
+    case = synth.gemm_case(M, N, K, 4, 128, seed=0, a_scale=0.5)
+    Wd, C = run_case(lib, case)
+    rng = np.random.default_rng(M * 7 + N)
+    P = 512
+    pm = rng.integers(0, M, P)
+    pn = rng.integers(0, N, P)
+    ref = oracle.quant_gemm_points(case["A"], Wd.cpu().numpy().view(np.uint32), case["scales"], case["zeros"],
+                                   4, 128, pm, pn)
+    assert_points_close(C[pm, pn], ref, "prefill %s M%d" % (proj, M))
+    # every row/column finite and the full output in the range the inputs allow
+    assert np.all(np.isfinite(C.astype(np.float32)))

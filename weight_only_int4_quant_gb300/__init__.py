@@ -1,0 +1,245 @@
+"""Python binding of libtlq: the GB300 weight-only INT4/INT2 quantized linear layer.
+
+Argument marshalling only.  Every step of the layer runs in the library's CUDA
+kernels; torch provides device memory and streams.  The C entry points (see
+include/tlq.h) are exposed under the same names; a missing or stale library
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB as _LIB_PATH
+from .build import build as _build
+
+__all__ = [
+    "TLQError", "load", "build", "EXPORTED",
+    "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights", "tl_loop_block_forward",
+    "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout", "tl_last_error", "tl_version",
+    "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
+]
+
+# every symbol include/tlq.h declares
+EXPORTED = (
+    "tl_last_error", "tl_version", "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights",
+    "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
+)
+
+TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
+_STATUS_NAMES = {0: "TLQ_OK", 1: "TLQ_EINVAL", 2: "TLQ_EUNSUPPORTED", 3: "TLQ_ECUDA", 4: "TLQ_ETIMEOUT"}
+
+
+class TLQError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+class _QProj(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("s", ctypes.c_void_p), ("z", ctypes.c_void_p),
+                ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+class _Block(ctypes.Structure):
+    _fields_ = [("qkv", _QProj), ("o", _QProj), ("up", _QProj), ("down", _QProj),
+                ("bits", ctypes.c_int), ("group", ctypes.c_int), ("D", ctypes.c_int),
+                ("h", ctypes.c_void_p), ("qkv_out", ctypes.c_void_p), ("o_out", ctypes.c_void_p),
+                ("up_out", ctypes.c_void_p), ("normalize", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libtlq.so for sm_103a (nvcc) and return its path."""
+    return _build(force=force, verbose=verbose)
+
+
+def load():
+    """Load libtlq.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        try:  # share the process's CUDA runtime with torch
+            import torch  # noqa: F401
+        except ImportError:
+            pass
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libtlq.so is not built (%s); call weight_only_int4_quant_gb300.build()"
+                               % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint
+        sigs = {
+            "tl_last_error": ([], ctypes.c_char_p),
+            "tl_version": ([], ctypes.c_char_p),
+            "tl_quant_gemm": ([P, P, P, P, P, I, I, I, I, I, P], I),
+            "tl_pack_weights": ([P, P, I, I, I, P], I),
+            "tl_unpack_weights": ([P, P, I, I, I, P], I),
+            "tl_loop_block_forward": ([P, ctypes.POINTER(_Block), I, I, P], I),
+            "tl_check_status": ([P], I),
+            "tl_reset_status": ([P], I),
+            "tl_selftest_wait_timeout": ([U, P], I),
+        }
+        for name, (args, res) in sigs.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def _raise_if(st: int):
+    if st != TLQ_OK:
+        raise TLQError(st, load().tl_last_error().decode(errors="replace"))
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev(t, dtype, name):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtype:
+        raise ValueError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def tl_last_error() -> str:
+    return load().tl_last_error().decode(errors="replace")
+
+
+def tl_version() -> str:
+    return load().tl_version().decode()
+
+
+def tl_quant_gemm(A, W, scales, zeros, C, bits: int, group: int, stream=None) -> None:
+    """C[M][N] = fp16(A[M][K] . dequant(W)^T) on the GPU (see include/tlq.h)."""
+    import torch
+
+    M, K = A.shape
+    N = W.shape[0]
+    st = load().tl_quant_gemm(_dev(A, (torch.float16,), "A"), _dev(W, (torch.int32, torch.uint32), "W"),
+                              _dev(scales, (torch.float16,), "scales"), _dev(zeros, (torch.float16,), "zeros"),
+                              _dev(C, (torch.float16,), "C"), M, N, K, bits, group, _stream(stream))
+    _raise_if(st)
+
+
+def tl_pack_weights(codes, W, bits: int, stream=None) -> None:
+    import torch
+
+    N, K = codes.shape
+    _raise_if(load().tl_pack_weights(_dev(codes, (torch.uint8,), "codes"), _dev(W, (torch.int32, torch.uint32), "W"),
+                                     N, K, bits, _stream(stream)))
+
+
+def tl_unpack_weights(W, codes, bits: int, stream=None) -> None:
+    import torch
+
+    N, K = codes.shape
+    _raise_if(load().tl_unpack_weights(_dev(W, (torch.int32, torch.uint32), "W"), _dev(codes, (torch.uint8,), "codes"),
+                                       N, K, bits, _stream(stream)))
+
+
+def tl_loop_block_forward(x, block: "LoopBlock", L: int, stream=None) -> None:
+    import torch
+
+    M = x.shape[0]
+    if M > block.max_rows:
+        raise ValueError("x has %d rows, the block's scratch holds %d" % (M, block.max_rows))
+    _raise_if(load().tl_loop_block_forward(_dev(x, (torch.float32,), "x"), ctypes.byref(block._c), L, M,
+                                           _stream(stream)))
+
+
+def tl_check_status(stream=None) -> None:
+    _raise_if(load().tl_check_status(_stream(stream)))
+
+
+def tl_reset_status(stream=None) -> None:
+    _raise_if(load().tl_reset_status(_stream(stream)))
+
+
+def tl_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    _raise_if(load().tl_selftest_wait_timeout(limit_us, _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# conveniences that allocate their outputs with torch
+# ---------------------------------------------------------------------------
+
+def quant_gemm(A, W, scales, zeros, bits: int, group: int, stream=None):
+    import torch
+
+    C = torch.empty((A.shape[0], W.shape[0]), dtype=torch.float16, device=A.device)
+    tl_quant_gemm(A, W, scales, zeros, C, bits, group, stream)
+    return C
+
+
+def pack_weights(codes, bits: int, stream=None):
+    import torch
+
+    N, K = codes.shape
+    W = torch.empty((N, K * bits // 32), dtype=torch.int32, device=codes.device)
+    tl_pack_weights(codes, W, bits, stream)
+    return W
+
+
+def unpack_weights(W, K: int, bits: int, stream=None):
+    import torch
+
+    codes = torch.empty((W.shape[0], K), dtype=torch.uint8, device=W.device)
+    tl_unpack_weights(W, codes, bits, stream)
+    return codes
+
+
+class LoopBlock:
+    """The shared-weight loop block: four packed projections plus FP16 scratch.
+
+    ``proj`` maps "qkv", "o", "up", "down" to (W packed int32, scales, zeros)
+    CUDA tensors; scratch for up to ``max_rows`` rows is allocated here."""
+
+    def __init__(self, proj: dict, bits: int, group: int, max_rows: int, normalize: bool = True):
+        import torch
+
+        self.proj = proj
+        self.bits, self.group, self.max_rows = bits, group, max_rows
+        cpw = 32 // bits
+        dims = {k: (v[0].shape[0], v[0].shape[1] * cpw) for k, v in proj.items()}
+        D = dims["o"][0]
+        F = dims["up"][0]
+        self.D, self.F = D, F
+        dev = proj["o"][0].device
+        self.h = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
+        self.qkv_out = torch.empty((max_rows, 3 * D), dtype=torch.float16, device=dev)
+        self.o_out = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
+        self.up_out = torch.empty((max_rows, F), dtype=torch.float16, device=dev)
+        c = _Block()
+        for name in ("qkv", "o", "up", "down"):
+            W, s, z = proj[name]
+            N, K = dims[name]
+            setattr(c, name, _QProj(_dev(W, (torch.int32, torch.uint32), name + ".W"),
+                                    _dev(s, (torch.float16,), name + ".s"), _dev(z, (torch.float16,), name + ".z"),
+                                    N, K))
+        c.bits, c.group, c.D = bits, group, D
+        c.h, c.qkv_out, c.o_out, c.up_out = (self.h.data_ptr(), self.qkv_out.data_ptr(), self.o_out.data_ptr(),
+                                             self.up_out.data_ptr())
+        c.normalize = 1 if normalize else 0
+        self._c = c
+
+    def forward(self, x, L: int, stream=None):
+        tl_loop_block_forward(x, self, L, stream)
+        return x

@@ -1,0 +1,299 @@
+// C ABI of libtlq: argument validation, dispatch and error reporting.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace tlq {
+
+namespace {
+thread_local char g_msg[512] = "";
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+tlq_status set_error(tlq_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+tlq_status cuda_error(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return TLQ_OK;
+  return set_error(TLQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("TLQ_LOG");
+    return v && v[0] && strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+
+const DeviceInfo& device_info() {
+  static DeviceInfo info = [] {
+    DeviceInfo d{148, 128 << 20, 227 * 1024};
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+      cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+      cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev);
+      cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    }
+    return d;
+  }();
+  return info;
+}
+
+tlq_status encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                           CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  static cudaError_t load_err = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    load_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (load_err == cudaSuccess && q != cudaDriverEntryPointSuccess) load_err = cudaErrorSymbolNotFound;
+    fn = reinterpret_cast<EncodeFn>(p);
+  });
+  if (load_err != cudaSuccess || !fn) return cuda_error(load_err, "cuTensorMapEncodeTiled lookup");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(TLQ_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d): dims %llu x %llu, row %llu B, box %u x %u",
+                     (int)r, (unsigned long long)inner, (unsigned long long)outer, (unsigned long long)row_bytes,
+                     box_inner, box_outer);
+  return TLQ_OK;
+}
+
+// Shape rules shared by every GEMM entry point.
+tlq_status check_gemm_shape(int M, int N, int K, int bits, int group, const char* who) {
+  if (bits != 4 && bits != 2) return set_error(TLQ_EINVAL, "%s: bits=%d (must be 4 or 2)", who, bits);
+  if (M < 1) return set_error(TLQ_EINVAL, "%s: M=%d (must be >= 1)", who, M);
+  if (N < 1) return set_error(TLQ_EINVAL, "%s: N=%d (must be >= 1)", who, N);
+  if (K < 1) return set_error(TLQ_EINVAL, "%s: K=%d (must be >= 1)", who, K);
+  const int unit = bits == 4 ? 32 : 64;
+  if (group < unit || group % unit)
+    return set_error(TLQ_EINVAL, "%s: group=%d (must be a positive multiple of %d for INT%d)", who, group, unit, bits);
+  if (K % group) return set_error(TLQ_EINVAL, "%s: K=%d is not a multiple of group=%d", who, K, group);
+  return TLQ_OK;
+}
+
+tlq_status run_gemm(const GemmArgs& a, cudaStream_t stream) {
+  if (a.M <= 16) return launch_decode(a, stream);
+  return launch_prefill(a, stream);
+}
+
+}  // namespace tlq
+
+using namespace tlq;
+
+extern "C" {
+
+const char* tl_last_error(void) { return g_msg; }
+
+const char* tl_version(void) { return "tlq 0.1 sm_103a"; }
+
+tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint16_t* scales, const uint16_t* zeros,
+                         uint16_t* C, int M, int N, int K, int bits, int group, void* stream) {
+  g_msg[0] = 0;
+  if (!A || !Wpacked || !scales || !zeros || !C)
+    return set_error(TLQ_EINVAL, "tl_quant_gemm: null pointer (A=%p W=%p scales=%p zeros=%p C=%p)", (const void*)A,
+                     (const void*)Wpacked, (const void*)scales, (const void*)zeros, (const void*)C);
+  tlq_status st = check_gemm_shape(M, N, K, bits, group, "tl_quant_gemm");
+  if (st != TLQ_OK) return st;
+  if (!aligned16(A) || !aligned16(Wpacked) || !aligned16(C))
+    return set_error(TLQ_EINVAL, "tl_quant_gemm: A, Wpacked and C must be 16-byte aligned");
+  if (N % 8) return set_error(TLQ_EINVAL, "tl_quant_gemm: N=%d must be a multiple of 8", N);
+  {
+    const char* a0 = reinterpret_cast<const char*>(A);
+    const char* a1 = a0 + (size_t)M * K * 2;
+    const char* c0 = reinterpret_cast<const char*>(C);
+    const char* c1 = c0 + (size_t)M * N * 2;
+    if (a0 < c1 && c0 < a1) return set_error(TLQ_EINVAL, "tl_quant_gemm: A and C overlap");
+  }
+  GemmArgs a;
+  a.A = reinterpret_cast<const __half*>(A);
+  a.lda = K;
+  a.W = Wpacked;
+  a.S = reinterpret_cast<const __half*>(scales);
+  a.Z = reinterpret_cast<const __half*>(zeros);
+  a.C = reinterpret_cast<__half*>(C);
+  a.ldc = N;
+  a.X = nullptr;
+  a.ldx = 0;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.group = group;
+  a.epi = kEpiStore;
+  return run_gemm(a, static_cast<cudaStream_t>(stream));
+}
+
+tlq_status tl_pack_weights(const uint8_t* codes, uint32_t* Wpacked, int N, int K, int bits, void* stream) {
+  g_msg[0] = 0;
+  if (!codes || !Wpacked) return set_error(TLQ_EINVAL, "tl_pack_weights: null pointer");
+  if (bits != 4 && bits != 2) return set_error(TLQ_EINVAL, "tl_pack_weights: bits=%d (must be 4 or 2)", bits);
+  if (N < 1 || K < 1) return set_error(TLQ_EINVAL, "tl_pack_weights: N=%d K=%d must be >= 1", N, K);
+  if (K % (32 / bits)) return set_error(TLQ_EINVAL, "tl_pack_weights: K=%d not a multiple of %d", K, 32 / bits);
+  return launch_pack(codes, Wpacked, N, K, bits, static_cast<cudaStream_t>(stream));
+}
+
+tlq_status tl_unpack_weights(const uint32_t* Wpacked, uint8_t* codes, int N, int K, int bits, void* stream) {
+  g_msg[0] = 0;
+  if (!codes || !Wpacked) return set_error(TLQ_EINVAL, "tl_unpack_weights: null pointer");
+  if (bits != 4 && bits != 2) return set_error(TLQ_EINVAL, "tl_unpack_weights: bits=%d (must be 4 or 2)", bits);
+  if (N < 1 || K < 1) return set_error(TLQ_EINVAL, "tl_unpack_weights: N=%d K=%d must be >= 1", N, K);
+  if (K % (32 / bits)) return set_error(TLQ_EINVAL, "tl_unpack_weights: K=%d not a multiple of %d", K, 32 / bits);
+  return launch_unpack(Wpacked, codes, N, K, bits, static_cast<cudaStream_t>(stream));
+}
+
+tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void* stream_) {
+  g_msg[0] = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!x || !b) return set_error(TLQ_EINVAL, "tl_loop_block_forward: null x or block");
+  if (L < 0) return set_error(TLQ_EINVAL, "tl_loop_block_forward: L=%d (must be >= 0)", L);
+  if (M < 1) return set_error(TLQ_EINVAL, "tl_loop_block_forward: M=%d (must be >= 1)", M);
+  const int D = b->D, F = b->up.N;
+  if (D < 1 || D % 8) return set_error(TLQ_EINVAL, "tl_loop_block_forward: D=%d must be a positive multiple of 8", D);
+  if (b->qkv.N != 3 * D || b->qkv.K != D) return set_error(TLQ_EINVAL, "tl_loop_block_forward: qkv must be [3D x D]");
+  if (b->o.N != D || b->o.K != D) return set_error(TLQ_EINVAL, "tl_loop_block_forward: o must be [D x D]");
+  if (b->up.K != D || F < 1) return set_error(TLQ_EINVAL, "tl_loop_block_forward: up must be [F x D]");
+  if (b->down.N != D || b->down.K != F) return set_error(TLQ_EINVAL, "tl_loop_block_forward: down must be [D x F]");
+  if (!b->h || !b->qkv_out || !b->o_out || !b->up_out)
+    return set_error(TLQ_EINVAL, "tl_loop_block_forward: null scratch buffer");
+  const tl_qproj* projs[4] = {&b->qkv, &b->o, &b->up, &b->down};
+  const char* names[4] = {"qkv", "o", "up", "down"};
+  for (int i = 0; i < 4; ++i) {
+    const tl_qproj* p = projs[i];
+    if (!p->W || !p->s || !p->z) return set_error(TLQ_EINVAL, "tl_loop_block_forward: %s has a null pointer", names[i]);
+    if (!aligned16(p->W)) return set_error(TLQ_EINVAL, "tl_loop_block_forward: %s weights not 16-byte aligned", names[i]);
+    tlq_status st = check_gemm_shape(M, p->N, p->K, b->bits, b->group, names[i]);
+    if (st != TLQ_OK) return st;
+    if (p->N % 8) return set_error(TLQ_EINVAL, "tl_loop_block_forward: %s N=%d must be a multiple of 8", names[i], p->N);
+  }
+  if (!aligned16(b->h) || !aligned16(b->qkv_out) || !aligned16(b->o_out) || !aligned16(b->up_out))
+    return set_error(TLQ_EINVAL, "tl_loop_block_forward: scratch buffers must be 16-byte aligned");
+
+  static std::once_flag logged;
+  if (log_enabled()) {
+    std::call_once(logged, [&] {
+      const int cpw = 32 / b->bits;
+      size_t wb = 0;
+      for (int i = 0; i < 4; ++i)
+        wb += (size_t)projs[i]->N * (projs[i]->K / cpw) * 4 + (size_t)projs[i]->N * (projs[i]->K / b->group) * 4;
+      fprintf(stderr, "[tlq] loop block: INT%d group %d, packed weights + scales/zeros %.1f MB, L2 %.1f MB -> %s\n",
+              b->bits, b->group, wb / 1e6, device_info().l2_bytes / 1e6,
+              wb <= (size_t)device_info().l2_bytes / 2 ? "L2-resident after the first iteration"
+                                                       : "streamed from HBM every iteration");
+    });
+  }
+
+  for (int l = 0; l < L; ++l) {
+    tlq_status st = launch_rmsnorm(x, reinterpret_cast<__half*>(b->h), M, D, b->normalize, stream);
+    if (st != TLQ_OK) return st;
+    GemmArgs a;
+    a.bits = b->bits;
+    a.group = b->group;
+    a.M = M;
+    a.X = nullptr;
+    a.ldx = 0;
+    // QKV
+    a.A = reinterpret_cast<const __half*>(b->h);
+    a.lda = D;
+    a.W = b->qkv.W;
+    a.S = reinterpret_cast<const __half*>(b->qkv.s);
+    a.Z = reinterpret_cast<const __half*>(b->qkv.z);
+    a.C = reinterpret_cast<__half*>(b->qkv_out);
+    a.ldc = 3 * D;
+    a.N = 3 * D;
+    a.K = D;
+    a.epi = kEpiStore;
+    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
+    // O on qkv[:, :D]
+    a.A = reinterpret_cast<const __half*>(b->qkv_out);
+    a.lda = 3 * D;
+    a.W = b->o.W;
+    a.S = reinterpret_cast<const __half*>(b->o.s);
+    a.Z = reinterpret_cast<const __half*>(b->o.z);
+    a.C = reinterpret_cast<__half*>(b->o_out);
+    a.ldc = D;
+    a.N = D;
+    a.K = D;
+    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
+    // UP + relu
+    a.A = reinterpret_cast<const __half*>(b->o_out);
+    a.lda = D;
+    a.W = b->up.W;
+    a.S = reinterpret_cast<const __half*>(b->up.s);
+    a.Z = reinterpret_cast<const __half*>(b->up.z);
+    a.C = reinterpret_cast<__half*>(b->up_out);
+    a.ldc = F;
+    a.N = F;
+    a.K = D;
+    a.epi = kEpiRelu;
+    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
+    // DOWN + FP32 residual add
+    a.A = reinterpret_cast<const __half*>(b->up_out);
+    a.lda = F;
+    a.W = b->down.W;
+    a.S = reinterpret_cast<const __half*>(b->down.s);
+    a.Z = reinterpret_cast<const __half*>(b->down.z);
+    a.C = nullptr;
+    a.ldc = 0;
+    a.X = x;
+    a.ldx = D;
+    a.N = D;
+    a.K = F;
+    a.epi = kEpiResidual;
+    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
+  }
+  return TLQ_OK;
+}
+
+tlq_status tl_check_status(void* stream) {
+  g_msg[0] = 0;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "tl_check_status: stream synchronize");
+  uint32_t st = 0, where = 0;
+  e = cudaMemcpyFromSymbol(&st, g_status, sizeof(st));
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&where, g_status_where, sizeof(where));
+  if (e != cudaSuccess) return cuda_error(e, "tl_check_status: read status");
+  if (st == kStatusTimeout)
+    return set_error(TLQ_ETIMEOUT, "a device-side wait gave up (site 0x%x); results of that launch are invalid", where);
+  return TLQ_OK;
+}
+
+tlq_status tl_reset_status(void* stream) {
+  g_msg[0] = 0;
+  const uint32_t z = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_status, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_status_where, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return cuda_error(e, "tl_reset_status");
+}
+
+tlq_status tl_selftest_wait_timeout(unsigned limit_us, void* stream) {
+  g_msg[0] = 0;
+  if (limit_us < 1 || limit_us > 1000000)
+    return set_error(TLQ_EINVAL, "tl_selftest_wait_timeout: limit_us=%u outside 1..1000000", limit_us);
+  return launch_timeout_probe(limit_us, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,554 @@
+// Prefill path of quant_gemm (M > 16 tokens): a dense contraction on the
+// 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Layer: C[m][n] = fp16( sum_k A[m][k] * (q[n][k] - z[n][g]) * s[n][g] ).
+// Source: "Model" (TinyLoop Python API), "VRAM cost", Weights (packed INT2 /
+// INT4 + FP16 scales + FP16 zeros per quantized layer); "Model", "Returns",
+// item 2 (weights stay packed in GPU memory; dequantization happens in the
+// GEMM, the FP16 body cache being the opt-in alternative).
+//
+// Tile: 128 tokens (UMMA M) x 256 weight rows (UMMA N) x 64 k per stage,
+// FP32 accumulator in TMEM (256 columns).  Warp roles (320 threads):
+//   warps 0-7  dequantize: each thread owns one weight row of the tile, reads
+//              its packed words straight from global memory (three stages
+//              ahead), rebuilds exact FP16 weights (q - z) * s and stores them
+//              in the UMMA K-major SWIZZLE_128B layout; after the main loop the
+//              same warps drain the accumulator (tcgen05.ld) in the epilogue.
+//   warp 8     TMA producer of the activation tiles (SWIZZLE_128B).
+//   warp 9     one elected thread issues tcgen05.mma (kind::f16, 4 x K=16 per
+//              stage) and commits stage release / accumulator-ready barriers.
+// Short-M problems split K over the CTAs of a thread-block cluster; partial
+// tiles are reduced in a fixed rank order through distributed shared memory
+// (deterministic, no atomics).  Every mbarrier wait is bounded.
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace tlq {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int kStagesP = 4;
+constexpr int kDqWarps = 8;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreadsP = 10 * 32;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 256;
+constexpr int kPrefetch = 3;          // dequant global-load distance (stages)
+constexpr int RED_PITCH = BM + 1;     // floats per column of the split-K partial tile
+
+static_assert(BN == kDqWarps * 32, "one dequant thread per weight row");
+static_assert(BN * RED_PITCH * 4 <= kStagesP * (A_STAGE + B_STAGE), "split-K buffer fits in the stages");
+
+// Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16,
+// both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct PrefillParams {
+  const uint32_t* W;
+  const __half* S;
+  const __half* Z;
+  __half* C;
+  int ldc;
+  float* X;
+  int ldx;
+  int M, N, K, group;
+  int kslice;  // k per cluster rank (multiple of BK)
+  int ksplit;
+};
+
+// Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row atoms of
+// 1024 bytes (stride byte offset 1024), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// 32 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Exact FP16 weights of one packed word: ((base + q) - base - z) * s, both
+// subtractions exact, one rounding in the multiply.  Writes the word's codes
+// in k order as 16-byte chunks (INT4: one chunk, INT2: two).
+template <int BITS>
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t z2, uint32_t (&out)[BITS == 4 ? 4 : 8]) {
+  if constexpr (BITS == 4) {
+    const uint32_t w8 = w >> 8;
+    uint32_t d0 = and_or(w, 0x000F000Fu, 0x64006400u);   // codes 0, 4 (+1024)
+    uint32_t d1 = and_or(w, 0x00F000F0u, 0x54005400u);   // codes 1, 5 (+64)
+    uint32_t d2 = and_or(w8, 0x000F000Fu, 0x64006400u);  // codes 2, 6 (+1024)
+    uint32_t d3 = and_or(w8, 0x00F000F0u, 0x54005400u);  // codes 3, 7 (+64)
+    d0 = hmul2u(hsub2u(hsub2u(d0, 0x64006400u), z2), s2);
+    d1 = hmul2u(hsub2u(hsub2u(d1, 0x54005400u), z2), s2);
+    d2 = hmul2u(hsub2u(hsub2u(d2, 0x64006400u), z2), s2);
+    d3 = hmul2u(hsub2u(hsub2u(d3, 0x54005400u), z2), s2);
+    out[0] = prmt(d0, d1, 0x5410);  // w0 w1
+    out[1] = prmt(d2, d3, 0x5410);  // w2 w3
+    out[2] = prmt(d0, d1, 0x7632);  // w4 w5
+    out[3] = prmt(d2, d3, 0x7632);  // w6 w7
+  } else {
+    const uint32_t w10 = w >> 10;
+    uint32_t d[8];
+    d[0] = and_or(w, 0x00030003u, 0x64006400u);
+    d[1] = and_or(w, 0x000C000Cu, 0x5C005C00u);
+    d[2] = and_or(w, 0x00300030u, 0x54005400u);
+    d[3] = and_or(w, 0x00C000C0u, 0x4C004C00u);
+    d[4] = and_or(w, 0x03000300u, 0x44004400u);
+    d[5] = and_or(w10, 0x00030003u, 0x64006400u);
+    d[6] = and_or(w10, 0x000C000Cu, 0x5C005C00u);
+    d[7] = and_or(w10, 0x00300030u, 0x54005400u);
+    const uint32_t base[8] = {0x64006400u, 0x5C005C00u, 0x54005400u, 0x4C004C00u,
+                              0x44004400u, 0x64006400u, 0x5C005C00u, 0x54005400u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = hmul2u(hsub2u(hsub2u(d[i], base[i]), z2), s2);
+    // d[i] = (w_i, w_{i+8})
+    out[0] = prmt(d[0], d[1], 0x5410);
+    out[1] = prmt(d[2], d[3], 0x5410);
+    out[2] = prmt(d[4], d[5], 0x5410);
+    out[3] = prmt(d[6], d[7], 0x5410);
+    out[4] = prmt(d[0], d[1], 0x7632);
+    out[5] = prmt(d[2], d[3], 0x7632);
+    out[6] = prmt(d[4], d[5], 0x7632);
+    out[7] = prmt(d[6], d[7], 0x7632);
+  }
+}
+
+__device__ __forceinline__ uint32_t half2_bits(__half a) {
+  const uint16_t b = __half_as_ushort(a);
+  return (uint32_t)b | ((uint32_t)b << 16);
+}
+
+template <int EPI>
+__device__ __forceinline__ void store_out(const PrefillParams& p, int m, int n, float v) {
+  __half h = __float2half_rn(v);
+  if constexpr (EPI == kEpiRelu) h = relu_half(h);
+  if constexpr (EPI == kEpiResidual) {
+    float* xp = p.X + (size_t)m * p.ldx + n;
+    *xp = *xp + __half2float(h);
+  } else {
+    p.C[(size_t)m * p.ldc + n] = h;
+  }
+}
+
+template <int BITS, int EPI>
+__global__ void __launch_bounds__(kThreadsP, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap amap, const PrefillParams p) {
+  constexpr int CPW = 32 / BITS;
+  constexpr int WPS = BK / CPW;                 // packed words per row per stage (8 or 4)
+  constexpr int NV = WPS / 4;                   // uint4 loads per row per stage (2 or 1)
+  constexpr int OUTW = BITS == 4 ? 4 : 8;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + kStagesP * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sb + kStagesP * B_STAGE);
+  uint64_t* full_a = bars;
+  uint64_t* full_b = bars + kStagesP;
+  uint64_t* empty = bars + 2 * kStagesP;
+  uint64_t* accum = bars + 3 * kStagesP;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStagesP + 1);
+  float* red = reinterpret_cast<float*>(smem);  // split-K partial tile, after the main loop
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * BM;
+  const int rank = (int)blockIdx.z;  // == %cluster_ctarank (cluster dims (1, 1, ksplit))
+  const int k0 = rank * p.kslice;
+  const int klen = min(p.kslice, p.K - k0);
+  const int nkb = (klen + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesP; ++i) {
+      mbar_init(&full_a[i], 1);
+      mbar_init(&full_b[i], kDqWarps);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(accum, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) pdl_launch_dependents();
+
+  if (warp == kTmaWarp) {
+    // ---------------- activations: TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&amap);
+      pdl_wait();  // A may be written by the preceding kernel
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int slot = kb % kStagesP;
+        if (!mbar_wait(&empty[slot], ((kb / kStagesP) & 1) ^ 1, 0x201)) break;
+        mbar_arrive_expect_tx(&full_a[slot], A_STAGE);
+        tma_load_2d(&amap, &full_a[slot], sa + slot * A_STAGE, k0 + kb * BK, m0);
+      }
+      for (int kb = max(0, nkb - kStagesP); kb < nkb; ++kb)
+        if (!mbar_wait(&full_a[kb % kStagesP], (kb / kStagesP) & 1, 0x202)) break;
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int slot = kb % kStagesP;
+        const uint32_t par = (kb / kStagesP) & 1;
+        ok = mbar_wait(&full_a[slot], par, 0x203) && mbar_wait(&full_b[slot], par, 0x204);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sa + slot * A_STAGE);
+        const uint32_t b0 = smem_u32(sb + slot * B_STAGE);
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+          umma_f16(tmem, sw128_desc(a0 + kk * UMMA_K * 2), sw128_desc(b0 + kk * UMMA_K * 2), (kb | kk) != 0);
+        umma_commit(&empty[slot]);
+      }
+      umma_commit(accum);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- dequantize weights into the B stages ----------------
+    const int r = threadIdx.x;  // weight row inside the tile, 0..255
+    const int n = n0 + r;
+    const bool row_ok = n < p.N;
+    const int wpr = p.K / CPW;
+    const uint32_t* wrow = p.W + (size_t)(row_ok ? n : 0) * wpr;
+    const int G = p.K / p.group;
+    const __half* srow = p.S + (size_t)(row_ok ? n : 0) * G;
+    const __half* zrow = p.Z + (size_t)(row_ok ? n : 0) * G;
+    const bool two_groups = (BITS == 4) && (p.group < BK);  // INT4 with group 32
+
+    uint4 ring[kPrefetch][NV];
+    uint32_t sring[kPrefetch][2], zring[kPrefetch][2];
+    auto issue = [&](int kb, uint4 (&dst)[NV], uint32_t (&sd)[2], uint32_t (&zd)[2]) {
+      const int ks = k0 + kb * BK;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int kv = ks + v * 4 * CPW;
+        dst[v] = (row_ok && kv < p.K) ? ldg_nc_v4(wrow + kv / CPW) : make_uint4(0, 0, 0, 0);
+      }
+      const int g0 = ks / p.group;
+      const int g1 = two_groups ? min(g0 + 1, G - 1) : g0;
+      sd[0] = row_ok ? half2_bits(srow[g0]) : 0u;
+      zd[0] = row_ok ? half2_bits(zrow[g0]) : 0u;
+      sd[1] = row_ok ? half2_bits(srow[g1]) : 0u;
+      zd[1] = row_ok ? half2_bits(zrow[g1]) : 0u;
+    };
+#pragma unroll
+    for (int j = 0; j < kPrefetch; ++j)
+      if (j < nkb) issue(j, ring[j], sring[j], zring[j]);
+
+    bool ok = true;
+    for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
+#pragma unroll
+      for (int j = 0; j < kPrefetch; ++j) {
+        const int kb = kb0 + j;
+        if (kb < nkb && ok) {
+          uint4 cur[NV];
+#pragma unroll
+          for (int v = 0; v < NV; ++v) cur[v] = ring[j][v];
+          const uint32_t s_lo = sring[j][0], z_lo = zring[j][0], s_hi = sring[j][1], z_hi = zring[j][1];
+          if (kb + kPrefetch < nkb) issue(kb + kPrefetch, ring[j], sring[j], zring[j]);
+          const int slot = kb % kStagesP;
+          if (!mbar_wait(&empty[slot], ((kb / kStagesP) & 1) ^ 1, 0x205)) {
+            ok = false;
+            break;
+          }
+          const uint32_t brow = smem_u32(sb + slot * B_STAGE) + (uint32_t)r * 128u;
+          const int ks = k0 + kb * BK;
+          uint32_t wv[WPS];
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            wv[4 * v + 0] = cur[v].x;
+            wv[4 * v + 1] = cur[v].y;
+            wv[4 * v + 2] = cur[v].z;
+            wv[4 * v + 3] = cur[v].w;
+          }
+#pragma unroll
+          for (int wj = 0; wj < WPS; ++wj) {
+            const bool hi = two_groups && (wj >= WPS / 2);
+            uint32_t o[OUTW];
+            dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? z_hi : z_lo, o);
+            const bool valid = row_ok && (ks + wj * CPW < p.K);
+            if constexpr (BITS == 4) {
+              const uint32_t c = (uint32_t)wj;
+              const uint32_t addr = brow + ((c ^ (uint32_t)(r & 7)) << 4);
+              if (valid) sts128(addr, o[0], o[1], o[2], o[3]);
+              else sts128(addr, 0, 0, 0, 0);
+            } else {
+              const uint32_t c0 = (uint32_t)(2 * wj), c1 = c0 + 1;
+              const uint32_t a0 = brow + ((c0 ^ (uint32_t)(r & 7)) << 4);
+              const uint32_t a1 = brow + ((c1 ^ (uint32_t)(r & 7)) << 4);
+              if (valid) {
+                sts128(a0, o[0], o[1], o[2], o[3]);
+                sts128(a1, o[4], o[5], o[6], o[7]);
+              } else {
+                sts128(a0, 0, 0, 0, 0);
+                sts128(a1, 0, 0, 0, 0);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full_b[slot]);
+        }
+      }
+    }
+
+    // ---------------- epilogue: TMEM -> registers -> global ----------------
+    const bool acc_ok = mbar_wait(accum, 0, 0x206);
+    tc_fence_after();
+    const int q = warp & 3;        // TMEM lane quarter this warp may access
+    const int half = warp >> 2;    // column half
+    const int mrow = 32 * q + lane;
+    const int m = m0 + mrow;
+    if (acc_ok) {
+      if (p.ksplit == 1) {
+        pdl_wait();
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int col = half * 128 + cc * 32;
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+          if (m < p.M) {
+            if constexpr (EPI == kEpiResidual) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (n0 + col + i < p.N) store_out<EPI>(p, m, n0 + col + i, __uint_as_float(v[i]));
+            } else {
+#pragma unroll
+              for (int c8 = 0; c8 < 4; ++c8) {
+                const int nb = n0 + col + c8 * 8;
+                if (nb < p.N) {  // N is a multiple of 8
+                  uint32_t h[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    __half lo = __float2half_rn(__uint_as_float(v[c8 * 8 + 2 * i]));
+                    __half hi = __float2half_rn(__uint_as_float(v[c8 * 8 + 2 * i + 1]));
+                    if constexpr (EPI == kEpiRelu) {
+                      lo = relu_half(lo);
+                      hi = relu_half(hi);
+                    }
+                    h[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+                  }
+                  *reinterpret_cast<uint4*>(p.C + (size_t)m * p.ldc + nb) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int col = half * 128 + cc * 32;
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) red[(col + i) * RED_PITCH + mrow] = __uint_as_float(v[i]);
+        }
+      }
+    }
+  }
+
+  // ---------------- split-K: reduce partial tiles across the cluster ----------------
+  if (p.ksplit > 1) {
+    __syncwarp();
+    cluster_sync();
+    pdl_wait();
+    const int cpr = BN / p.ksplit;  // columns finalized by this rank (ksplit divides 256)
+    const int c0 = rank * cpr;
+    const uint32_t red_addr = smem_u32(red);
+    for (int i = threadIdx.x; i < BM * cpr; i += kThreadsP) {
+      const int mm = i / cpr;
+      const int col = c0 + (i - mm * cpr);
+      const int m = m0 + mm, n = n0 + col;
+      float acc = 0.f;
+      for (int j = 0; j < p.ksplit; ++j)
+        acc += ld_shared_cluster_f32(map_shared_rank(red_addr + (uint32_t)((col * RED_PITCH + mm) * 4), (uint32_t)j));
+      if (m < p.M && n < p.N) store_out<EPI>(p, m, n, acc);
+    }
+    __syncwarp();
+    cluster_sync();
+  }
+
+  // ---------------- teardown ----------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BITS, int EPI>
+tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
+  const int sms = device_info().sms;
+  const int ntile = (a.N + BN - 1) / BN;
+  const int mtile = (a.M + BM - 1) / BM;
+  const int nkb = (a.K + BK - 1) / BK;
+  int ks = 1;
+  const char* env = getenv("TLQ_PREFILL_KSPLIT");
+  if (env) {
+    ks = atoi(env);
+  } else {
+    const int tiles = ntile * mtile;
+    while (ks < 8 && tiles * ks * 2 <= sms && nkb / (ks * 2) >= 4) ks *= 2;
+  }
+  if (ks != 1 && ks != 2 && ks != 4 && ks != 8) return set_error(TLQ_EINVAL, "prefill: k split %d", ks);
+  const int per = (nkb + ks - 1) / ks;
+  const int ks_eff = (nkb + per - 1) / per;
+  int ksplit = 1;
+  while (ksplit < ks_eff) ksplit *= 2;  // cluster size must divide the 256 columns
+  if (ksplit > ks_eff) {
+    // fall back to the largest power of two whose slices are all non-empty
+    ksplit = 1;
+    while (ksplit * 2 <= ks_eff) ksplit *= 2;
+  }
+  const int per2 = (nkb + ksplit - 1) / ksplit;
+  PrefillParams p;
+  p.W = a.W;
+  p.S = a.S;
+  p.Z = a.Z;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.X = a.X;
+  p.ldx = a.ldx;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.group = a.group;
+  p.kslice = per2 * BK;
+  p.ksplit = (a.K + p.kslice - 1) / p.kslice;
+  if (p.ksplit != ksplit) return set_error(TLQ_EINVAL, "prefill: inconsistent k split");
+
+  CUtensorMap amap;
+  tlq_status st = encode_tiled_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.A, (uint64_t)a.K, (uint64_t)a.M,
+                                  (uint64_t)a.lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (st != TLQ_OK) return st;
+
+  const size_t smem = 1024 + (size_t)kStagesP * (A_STAGE + B_STAGE) + 256;
+  auto kern = prefill_kernel<BITS, EPI>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (attr_err != cudaSuccess) return cuda_error(attr_err, "prefill: cudaFuncSetAttribute");
+
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)ntile, (unsigned)mtile, (unsigned)p.ksplit);
+  lc.blockDim = dim3(kThreadsP, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (p.ksplit > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = (unsigned)p.ksplit;
+    ++na;
+  }
+  lc.attrs = attrs;
+  lc.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, p);
+  if (e != cudaSuccess) return cuda_error(e, "prefill: launch");
+  if (log_enabled())
+    fprintf(stderr, "[tlq] prefill int%d M=%d N=%d K=%d group=%d: grid %dx%dx%d (ksplit %d, kslice %d) smem=%zu\n", BITS,
+            a.M, a.N, a.K, a.group, ntile, mtile, p.ksplit, p.ksplit, p.kslice, smem);
+  return TLQ_OK;
+}
+
+template <int BITS>
+tlq_status dispatch_epi(const GemmArgs& a, cudaStream_t s) {
+  switch (a.epi) {
+    case kEpiStore: return launch_impl<BITS, kEpiStore>(a, s);
+    case kEpiRelu: return launch_impl<BITS, kEpiRelu>(a, s);
+    default: return launch_impl<BITS, kEpiResidual>(a, s);
+  }
+}
+
+}  // namespace
+
+tlq_status launch_prefill(const GemmArgs& a, cudaStream_t stream) {
+  if (a.lda % 8) return set_error(TLQ_EINVAL, "prefill: lda=%d must be a multiple of 8", a.lda);
+  return a.bits == 4 ? dispatch_epi<4>(a, stream) : dispatch_epi<2>(a, stream);
+}
+
+}  // namespace tlq
