@@ -14,10 +14,12 @@
  *
  * Conventions shared by every entry point
  *  - Ownership: the caller owns all memory.  No entry point allocates device
- *    memory or keeps state between calls.
- *  - Ordering: calls are asynchronous and ordered on `stream`.  The library
- *    holds no shared scratch, so calls on different streams with disjoint
- *    buffers may run concurrently; one model instance is meant to drive one
+ *    memory or keeps state between calls (tl_loop_block_forward_static_scratch
+ *    uses a static array the library owns, see there).
+ *  - Ordering: calls are asynchronous and ordered on `stream`.  Apart from
+ *    tl_loop_block_forward_static_scratch the library holds no shared
+ *    scratch, so calls on different streams with disjoint buffers may run
+ *    concurrently; one model instance is meant to drive one
  *    stream ("Model", section "Thread safety": a single CUDA stream for all
  *    forward-pass work).
  *  - Errors: arguments are checked on the host before anything is launched.
@@ -163,6 +165,31 @@ typedef struct {
  * whether the block's packed weights fit in L2 and the kernel choice.
  */
 tlq_status tl_loop_block_forward(float* x, const tl_block* block, int L, int M, void* stream);
+
+/*
+ * tl_loop_block_forward_static_scratch -- tl_loop_block_forward for callers
+ * that cannot allocate device memory or provide scratch buffers (a serving
+ * runtime that forbids allocation after start-up, a plugin interface that only
+ * passes a layer its inputs and outputs).  There is no counterpart on the
+ * pages: it is a packaging choice of this library.
+ *
+ * Identical arithmetic to tl_loop_block_forward; block->h, qkv_out, o_out and
+ * up_out are ignored (may be NULL).  The four FP16 intermediates live in one
+ * 4 MiB static device array inside the library, which every GPU that loads
+ * the library holds until the process exits.  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *   Size limit: 2*M*(5*D + F) bytes (each buffer rounded up to 256 bytes)
+ *   must fit in 4 MiB -- e.g. M <= 113 at D = 2048, F = 8192 -- otherwise
+ *   TLQ_EINVAL with a message that names the sizes, and nothing is launched.
+ *   First call on a device: looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   All calls on a device share the one array, which keeps whatever the last
+ *   call left in it; every intermediate is fully written before it is read,
+ *   so nothing needs clearing.  Calls whose executions overlap on the GPU
+ *   (other streams, other threads) race on the array: serialize them.
+ */
+tlq_status tl_loop_block_forward_static_scratch(float* x, const tl_block* block, int L, int M, void* stream);
 
 /*
  * Synchronize `stream` and report the device status word: TLQ_OK, or

@@ -18,13 +18,14 @@ __all__ = [
     "TLQError", "load", "build", "EXPORTED",
     "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights", "tl_loop_block_forward",
     "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout", "tl_last_error", "tl_version",
-    "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
+    "tl_loop_block_forward_static_scratch", "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
 ]
 
 # every symbol include/tlq.h declares
 EXPORTED = (
     "tl_last_error", "tl_version", "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights",
     "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
+    "tl_loop_block_forward_static_scratch",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -83,6 +84,7 @@ def load():
             "tl_check_status": ([P], I),
             "tl_reset_status": ([P], I),
             "tl_selftest_wait_timeout": ([U, P], I),
+            "tl_loop_block_forward_static_scratch": ([P, ctypes.POINTER(_Block), I, I, P], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -163,6 +165,16 @@ def tl_loop_block_forward(x, block: "LoopBlock", L: int, stream=None) -> None:
         raise ValueError("x has %d rows, the block's scratch holds %d" % (M, block.max_rows))
     _raise_if(load().tl_loop_block_forward(_dev(x, (torch.float32,), "x"), ctypes.byref(block._c), L, M,
                                            _stream(stream)))
+
+
+def tl_loop_block_forward_static_scratch(x, block: "LoopBlock", L: int, stream=None) -> None:
+    """tl_loop_block_forward with the intermediates in the library's static
+    device scratch (no caller buffers, no allocation); the block's own scratch
+    tensors are not used."""
+    import torch
+
+    _raise_if(load().tl_loop_block_forward_static_scratch(_dev(x, (torch.float32,), "x"), ctypes.byref(block._c), L,
+                                                          x.shape[0], _stream(stream)))
 
 
 def tl_check_status(stream=None) -> None:
