@@ -92,6 +92,31 @@ tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint1
                          const uint16_t* zeros, uint16_t* C, int M, int N, int K, int bits,
                          int group, void* stream);
 
+/* One problem of tl_quant_gemm_batched: the arguments of one tl_quant_gemm
+ * call (device pointers, same layouts and rules). */
+typedef struct {
+  const uint16_t* A;
+  const uint32_t* Wpacked;
+  const uint16_t* scales;
+  const uint16_t* zeros;
+  uint16_t* C;
+  int M, N, K, bits, group;
+} tl_gemm_desc;
+
+/*
+ * tl_quant_gemm_batched -- several independent quant_gemm problems in as few
+ * launches as possible: every problem with M <= 16 of one bit width goes into
+ * one persistent decode launch (up to 16 problems per launch), each larger
+ * problem gets its own tensor-core launch.  Results equal `count` separate
+ * tl_quant_gemm calls.  Same source passages as tl_quant_gemm; batching is a
+ * launch-overhead measure of this library (the layers of one decode step that
+ * do not depend on each other, or several requests at once).
+ *   descs  HOST array of `count` descriptors (count >= 0; 0 is a no-op).
+ *   No C may overlap any A or another C.  Every descriptor is validated
+ *   before anything is launched (TLQ_EINVAL names the offending index).
+ */
+tlq_status tl_quant_gemm_batched(const tl_gemm_desc* descs, int count, void* stream);
+
 /*
  * tl_pack_weights -- pack quantization codes into the kernels' weight format.
  *

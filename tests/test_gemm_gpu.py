@@ -227,3 +227,66 @@ def test_prefill_full_size_sampled(lib, proj, M):
     assert_points_close(C[pm, pn], ref, "prefill %s M%d" % (proj, M))
     # every row/column finite and the full output in the range the inputs allow
     assert np.all(np.isfinite(C.astype(np.float32)))
+
+
+# ---------------------------------------------------------------------------
+# batched launches: several independent problems, one decode launch per bit width
+# ---------------------------------------------------------------------------
+
+def _problems(specs, seed=0):
+    out = []
+    for i, (M, N, K, bits, group) in enumerate(specs):
+        case = synth.gemm_case(M, N, K, bits, group, seed=seed + i, a_scale=0.5 if M > 16 else 1.0)
+        W = torch.from_numpy(oracle.pack(case["codes"], bits).view(np.int32)).cuda()
+        out.append(dict(case=case, A=dev(case["A"]), W=W, s=dev(case["scales"]), z=dev(case["zeros"]),
+                        C=torch.empty((M, N), dtype=torch.float16, device="cuda")))
+    return out
+
+
+def test_batched_equals_separate_calls_bitwise(lib):
+    specs = [(M, N, K, 4, 128) for M in (1, 4, 16) for (N, K) in synth.SHAPES.values()]
+    probs = _problems(specs)
+    lib.tl_quant_gemm_batched([(p["A"], p["W"], p["s"], p["z"], p["C"], 4, 128) for p in probs])
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+    for p, (M, N, K, bits, group) in zip(probs, specs):
+        single = lib.quant_gemm(p["A"], p["W"], p["s"], p["z"], bits, group)
+        assert torch.equal(single.view(torch.int16), p["C"].view(torch.int16)), (M, N, K)
+    # and a sample against the oracle
+    rng = np.random.default_rng(5)
+    for p, (M, N, K, bits, group) in zip(probs, specs):
+        pm, pn = rng.integers(0, M, 64), rng.integers(0, N, 64)
+        c = p["case"]
+        ref = oracle.quant_gemm_points(c["A"], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
+                                       group, pm, pn)
+        assert_points_close(p["C"].cpu().numpy()[pm, pn], ref, "batched M%d N%d K%d" % (M, N, K))
+
+
+def test_batched_mixed_bits_and_paths(lib):
+    specs = [(1, 256, 1024, 4, 128), (9, 136, 448, 2, 64), (40, 264, 512, 4, 128), (3, 512, 2048, 2, 128),
+             (16, 64, 4096, 4, 4096), (130, 256, 1024, 2, 64)]
+    probs = _problems(specs, seed=50)
+    lib.tl_quant_gemm_batched([(p["A"], p["W"], p["s"], p["z"], p["C"], b, g)
+                               for p, (_, _, _, b, g) in zip(probs, specs)])
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+    for p, (M, N, K, bits, group) in zip(probs, specs):
+        c = p["case"]
+        ref = oracle.quant_gemm(c["A"], oracle.pack(c["codes"], bits), c["scales"], c["zeros"], bits, group)
+        assert_close(p["C"].cpu().numpy(), ref, "mixed M%d N%d K%d int%d" % (M, N, K, bits))
+
+
+def test_batched_many_problems_and_errors(lib):
+    specs = [(1 + (i % 16), 64 + 8 * i, 256 * (1 + i % 3), 4, 128) for i in range(20)]  # > 16 decode problems
+    probs = _problems(specs, seed=70)
+    lib.tl_quant_gemm_batched([(p["A"], p["W"], p["s"], p["z"], p["C"], 4, 128) for p in probs])
+    torch.cuda.synchronize()
+    for p, (M, N, K, bits, group) in zip(probs, specs):
+        c = p["case"]
+        ref = oracle.quant_gemm(c["A"], oracle.pack(c["codes"], bits), c["scales"], c["zeros"], bits, group)
+        assert_close(p["C"].cpu().numpy(), ref, "many M%d N%d K%d" % (M, N, K))
+    lib.tl_quant_gemm_batched([])  # no-op
+    p0, p1 = probs[0], probs[1]
+    with pytest.raises(lib.TLQError, match="overlap"):
+        lib.tl_quant_gemm_batched([(p0["A"], p0["W"], p0["s"], p0["z"], p0["C"], 4, 128),
+                                   (p1["A"], p1["W"], p1["s"], p1["z"], p0["C"], 4, 128)])

@@ -18,14 +18,14 @@ __all__ = [
     "TLQError", "load", "build", "EXPORTED",
     "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights", "tl_loop_block_forward",
     "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout", "tl_last_error", "tl_version",
-    "tl_loop_block_forward_static_scratch", "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
+    "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "gemm_descs", "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
 ]
 
 # every symbol include/tlq.h declares
 EXPORTED = (
     "tl_last_error", "tl_version", "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights",
     "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
-    "tl_loop_block_forward_static_scratch",
+    "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -41,6 +41,12 @@ class TLQError(RuntimeError):
 class _QProj(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("s", ctypes.c_void_p), ("z", ctypes.c_void_p),
                 ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+class _GemmDesc(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("Wpacked", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p), ("C", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
+                ("K", ctypes.c_int), ("bits", ctypes.c_int), ("group", ctypes.c_int)]
 
 
 class _Block(ctypes.Structure):
@@ -85,6 +91,7 @@ def load():
             "tl_reset_status": ([P], I),
             "tl_selftest_wait_timeout": ([U, P], I),
             "tl_loop_block_forward_static_scratch": ([P, ctypes.POINTER(_Block), I, I, P], I),
+            "tl_quant_gemm_batched": ([ctypes.POINTER(_GemmDesc), I, P], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -139,6 +146,30 @@ def tl_quant_gemm(A, W, scales, zeros, C, bits: int, group: int, stream=None) ->
                               _dev(scales, (torch.float16,), "scales"), _dev(zeros, (torch.float16,), "zeros"),
                               _dev(C, (torch.float16,), "C"), M, N, K, bits, group, _stream(stream))
     _raise_if(st)
+
+
+def gemm_descs(problems):
+    """ctypes descriptor array for tl_quant_gemm_batched from
+    (A, W, scales, zeros, C, bits, group) tuples of CUDA tensors; build it
+    once and reuse it to keep per-call host work small."""
+    import torch
+
+    arr = (_GemmDesc * len(problems))()
+    for i, (A, W, s, z, C, bits, group) in enumerate(problems):
+        M, K = A.shape
+        arr[i] = _GemmDesc(_dev(A, (torch.float16,), "A"), _dev(W, (torch.int32, torch.uint32), "W"),
+                           _dev(s, (torch.float16,), "scales"), _dev(z, (torch.float16,), "zeros"),
+                           _dev(C, (torch.float16,), "C"), M, W.shape[0], K, bits, group)
+    return arr
+
+
+def tl_quant_gemm_batched(descs, stream=None) -> None:
+    """Run independent quant_gemm problems in as few launches as possible;
+    ``descs`` is a list of (A, W, scales, zeros, C, bits, group) tuples or the
+    array gemm_descs() returns."""
+    if not isinstance(descs, ctypes.Array):
+        descs = gemm_descs(descs)
+    _raise_if(load().tl_quant_gemm_batched(descs, len(descs), _stream(stream)))
 
 
 def tl_pack_weights(codes, W, bits: int, stream=None) -> None:

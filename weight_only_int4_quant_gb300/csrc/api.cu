@@ -36,6 +36,14 @@ bool log_enabled() {
   return on;
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("TLQ_PDL");
+    return !(v && strcmp(v, "0") == 0);
+  }();
+  return on;
+}
+
 const DeviceInfo& device_info() {
   static DeviceInfo info = [] {
     DeviceInfo d{148, 128 << 20, 227 * 1024};
@@ -94,8 +102,49 @@ tlq_status check_gemm_shape(int M, int N, int K, int bits, int group, const char
 }
 
 tlq_status run_gemm(const GemmArgs& a, cudaStream_t stream) {
-  if (a.M <= 16) return launch_decode(a, stream);
+  if (a.M <= 16) return launch_decode(&a, 1, stream);
   return launch_prefill(a, stream);
+}
+
+// Validation shared by tl_quant_gemm and tl_quant_gemm_batched.
+tlq_status check_gemm_call(const uint16_t* A, const uint32_t* W, const uint16_t* S, const uint16_t* Z,
+                           const uint16_t* C, int M, int N, int K, int bits, int group, const char* who) {
+  if (!A || !W || !S || !Z || !C)
+    return set_error(TLQ_EINVAL, "%s: null pointer (A=%p W=%p scales=%p zeros=%p C=%p)", who, (const void*)A,
+                     (const void*)W, (const void*)S, (const void*)Z, (const void*)C);
+  tlq_status st = check_gemm_shape(M, N, K, bits, group, who);
+  if (st != TLQ_OK) return st;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C))
+    return set_error(TLQ_EINVAL, "%s: A, Wpacked and C must be 16-byte aligned", who);
+  if (N % 8) return set_error(TLQ_EINVAL, "%s: N=%d must be a multiple of 8", who, N);
+  return TLQ_OK;
+}
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const char* a0 = static_cast<const char*>(a);
+  const char* b0 = static_cast<const char*>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+GemmArgs plain_args(const uint16_t* A, const uint32_t* W, const uint16_t* S, const uint16_t* Z, uint16_t* C, int M,
+                    int N, int K, int bits, int group) {
+  GemmArgs a;
+  a.A = reinterpret_cast<const __half*>(A);
+  a.lda = K;
+  a.W = W;
+  a.S = reinterpret_cast<const __half*>(S);
+  a.Z = reinterpret_cast<const __half*>(Z);
+  a.C = reinterpret_cast<__half*>(C);
+  a.ldc = N;
+  a.X = nullptr;
+  a.ldx = 0;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.group = group;
+  a.epi = kEpiStore;
+  return a;
 }
 
 }  // namespace tlq
@@ -111,38 +160,58 @@ const char* tl_version(void) { return "tlq 0.1 sm_103a"; }
 tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint16_t* scales, const uint16_t* zeros,
                          uint16_t* C, int M, int N, int K, int bits, int group, void* stream) {
   g_msg[0] = 0;
-  if (!A || !Wpacked || !scales || !zeros || !C)
-    return set_error(TLQ_EINVAL, "tl_quant_gemm: null pointer (A=%p W=%p scales=%p zeros=%p C=%p)", (const void*)A,
-                     (const void*)Wpacked, (const void*)scales, (const void*)zeros, (const void*)C);
-  tlq_status st = check_gemm_shape(M, N, K, bits, group, "tl_quant_gemm");
+  tlq_status st = check_gemm_call(A, Wpacked, scales, zeros, C, M, N, K, bits, group, "tl_quant_gemm");
   if (st != TLQ_OK) return st;
-  if (!aligned16(A) || !aligned16(Wpacked) || !aligned16(C))
-    return set_error(TLQ_EINVAL, "tl_quant_gemm: A, Wpacked and C must be 16-byte aligned");
-  if (N % 8) return set_error(TLQ_EINVAL, "tl_quant_gemm: N=%d must be a multiple of 8", N);
-  {
-    const char* a0 = reinterpret_cast<const char*>(A);
-    const char* a1 = a0 + (size_t)M * K * 2;
-    const char* c0 = reinterpret_cast<const char*>(C);
-    const char* c1 = c0 + (size_t)M * N * 2;
-    if (a0 < c1 && c0 < a1) return set_error(TLQ_EINVAL, "tl_quant_gemm: A and C overlap");
+  if (overlaps(A, (size_t)M * K * 2, C, (size_t)M * N * 2))
+    return set_error(TLQ_EINVAL, "tl_quant_gemm: A and C overlap");
+  return run_gemm(plain_args(A, Wpacked, scales, zeros, C, M, N, K, bits, group), static_cast<cudaStream_t>(stream));
+}
+
+tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_) {
+  g_msg[0] = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!d || count < 0) return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: null descriptors or count %d", count);
+  char who[64];
+  for (int i = 0; i < count; ++i) {
+    snprintf(who, sizeof(who), "tl_quant_gemm_batched[%d]", i);
+    tlq_status st = check_gemm_call(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
+                                    d[i].bits, d[i].group, who);
+    if (st != TLQ_OK) return st;
   }
-  GemmArgs a;
-  a.A = reinterpret_cast<const __half*>(A);
-  a.lda = K;
-  a.W = Wpacked;
-  a.S = reinterpret_cast<const __half*>(scales);
-  a.Z = reinterpret_cast<const __half*>(zeros);
-  a.C = reinterpret_cast<__half*>(C);
-  a.ldc = N;
-  a.X = nullptr;
-  a.ldx = 0;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.bits = bits;
-  a.group = group;
-  a.epi = kEpiStore;
-  return run_gemm(a, static_cast<cudaStream_t>(stream));
+  for (int i = 0; i < count; ++i)
+    for (int j = 0; j < count; ++j) {
+      if (overlaps(d[j].A, (size_t)d[j].M * d[j].K * 2, d[i].C, (size_t)d[i].M * d[i].N * 2))
+        return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: C of problem %d overlaps A of problem %d", i, j);
+      if (i < j && overlaps(d[i].C, (size_t)d[i].M * d[i].N * 2, d[j].C, (size_t)d[j].M * d[j].N * 2))
+        return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: outputs of problems %d and %d overlap", i, j);
+    }
+  // decode-sized problems share launches (one per bit width, up to 16 problems each)
+  for (int bits : {4, 2}) {
+    GemmArgs batch[kMaxDecodeProblems];
+    int n = 0;
+    for (int i = 0; i < count; ++i) {
+      if (d[i].M > 16 || d[i].bits != bits) continue;
+      batch[n++] = plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
+                              d[i].bits, d[i].group);
+      if (n == kMaxDecodeProblems) {
+        tlq_status st = launch_decode(batch, n, stream);
+        if (st != TLQ_OK) return st;
+        n = 0;
+      }
+    }
+    if (n) {
+      tlq_status st = launch_decode(batch, n, stream);
+      if (st != TLQ_OK) return st;
+    }
+  }
+  for (int i = 0; i < count; ++i) {
+    if (d[i].M <= 16) continue;
+    tlq_status st = launch_prefill(plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N,
+                                              d[i].K, d[i].bits, d[i].group),
+                                   stream);
+    if (st != TLQ_OK) return st;
+  }
+  return TLQ_OK;
 }
 
 tlq_status tl_pack_weights(const uint8_t* codes, uint32_t* Wpacked, int N, int K, int bits, void* stream) {

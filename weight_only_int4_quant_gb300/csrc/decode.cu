@@ -1,5 +1,5 @@
 // Decode path of quant_gemm (M <= 16 tokens): bandwidth-bound, one pass over
-// the packed weights.
+// the packed weights, for one or several independent problems per launch.
 //
 // Layer: C[m][n] = fp16( sum_k A[m][k] * (q[n][k] - z[n][g]) * s[n][g] ).
 // Source: "Model" (TinyLoop Python API), "VRAM cost", Weights (INT2 / INT4
@@ -8,31 +8,42 @@
 // speeds decode up, so the kernel is built to stream weight bytes at HBM rate.
 //
 // Design (GB300):
-//  * A producer warp streams 64- or 32-row x 64-byte tiles of packed words into
-//    a ring of shared-memory stages with TMA (SWIZZLE_64B, so that the
-//    transposed word reads below are bank-conflict free).
-//  * Four consumer warps each own whole k-blocks (16 words per row).  A k-block
-//    is split into four "sets"; in a set, lane c of a row takes word c, so the
-//    four lanes that feed one MMA row hold 4*32/bits consecutive codes that lie
-//    in one quantization group.
+//  * Persistent: one CTA per SM walks a list of work units (a 32-row tile of
+//    one problem, all of K).  Problems are ordered by unit cost and units are
+//    dealt to CTAs in snake order, which balances the bytes per SM; a launch
+//    may hold up to 16 independent problems (a whole decode step), so the
+//    ~2-3 us fixed cost of a launch is paid once.
+//  * Each of the 8 warps owns every 8th k-block (16 packed words per row) of a
+//    unit and streams its packed weights through a private 4-stage TMA ring
+//    (SWIZZLE_64B, so that the transposed word reads are bank-conflict free).
+//    The rings run ahead across unit boundaries.
+//  * Scales and zeros of the next unit are prefetched into registers while the
+//    current unit runs and published into shared memory (as {s, z} half pairs)
+//    at the unit's reduction barrier; activations are read straight from
+//    global memory one k-block ahead.
+//  * A k-block is split into four "sets"; in a set, lane c of a row takes word
+//    c, so the four lanes that feed one MMA row hold 4*32/bits consecutive
+//    codes of one quantization group.
 //  * Codes become FP16 MMA operands with one LOP3 per pair: a code at mantissa
 //    bit position p of a half with exponent e reads as 2^e + q exactly (the
-//    "base" of that position: 1024, 256, 64, 16 or 4).  The MMA then sums
-//    a * (base + q); the base term and the zero point are removed per set with
-//    two row-independent correction sums (sum_k base_k a_k and sum_k a_k) that
-//    one extra MMA per word computes for all rows at once:
-//        acc_set = sum_k a_k (base_k + q_k) - sum_k base_k a_k - z * sum_k a_k
-//                = sum_k a_k (q_k - z)
-//        total  += s * acc_set           (FP32)
+//    "base" of that position: 1024, 256, 64, 16 or 4).  Over a span of codes
+//    that share one (scale, zero) the MMA sums a * (base + q); two
+//    row-independent correction sums (sum_k base_k a_k and sum_k a_k), which
+//    one extra MMA per word computes for all rows at once, then remove the
+//    base term and the zero point:
+//        acc_span = sum_k a_k (base_k + q_k) - sum_k base_k a_k - z * sum_k a_k
+//                 = sum_k a_k (q_k - z)
+//        total   += s * acc_span          (FP32)
 //  * Tokens are the MMA's N dimension (one or two 8-wide tiles), weight rows
 //    its M dimension (m16n8k16, "swap AB").
-//  * K is split across the four warps and, for short/wide shapes, across the
-//    CTAs of a thread-block cluster; partial sums are reduced in a fixed order
-//    through shared / distributed shared memory (no atomics: deterministic).
-//  * Programmatic dependent launch: weights and scales are fetched before
-//    griddepcontrol.wait, activations and the output only after it.
+//  * The eight warps' partial sums of a unit are added in a fixed order through
+//    a double-buffered shared-memory tile (deterministic, no atomics).
+//  * Programmatic dependent launch: weights, scales and zeros are fetched
+//    before griddepcontrol.wait, activations and outputs only after it.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -40,44 +51,44 @@
 namespace tlq {
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;                 // multiple of kConsumerWarps
-constexpr int kWordsPerKBlock = 16;        // per row, 64 bytes
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSPW = 4;             // TMA stages per warp
+constexpr int kWordsPerKBlock = 16; // per row: 64 bytes
 constexpr int kStageRowBytes = kWordsPerKBlock * 4;
+constexpr int kMaxProblems = kMaxDecodeProblems;
 
 template <int BITS>
 struct Fmt {
-  static constexpr int CPW = 32 / BITS;            // codes per word
-  static constexpr int KBLK = kWordsPerKBlock * CPW; // codes per k-block
-  static constexpr int SETC = 4 * CPW;             // codes per set
-  static constexpr int MPS = CPW / 4;              // MMAs per word (k16 each)
-  // activation row stride (halves): stride*2 bytes == kActMod (mod 128) makes the
-  // per-lane 16-byte activation loads conflict free.
-  static constexpr int kActMod = BITS == 4 ? 64 : 16;
+  static constexpr int CPW = 32 / BITS;               // codes per word
+  static constexpr int KBLK = kWordsPerKBlock * CPW;  // codes per k-block
+  static constexpr int SETC = 4 * CPW;                // codes per set
+  static constexpr int MPS = CPW / 4;                 // MMAs per word (k16 each)
 };
 
-struct DecodeParams {
+struct DecodeProblem {
   const __half* A;
-  int lda;
   const __half* S;
   const __half* Z;
   __half* C;
-  int ldc;
   float* X;
-  int ldx;
-  int M, N, K, group;
-  int kslice;      // codes per CTA (multiple of KBLK)
-  int act_stride;  // halves
-  int gsp;         // padded groups per row in the s/z tile
-  int gs_count;    // groups touched by one K slice (<= gsp)
-  int ksplit;      // CTAs per cluster along K
+  int lda, ldc, ldx;
+  int M, N, K, G;
+  int epi;
+  int ntiles;           // row tiles
+  int nkb;              // k-blocks
+  int unit_begin;       // first global unit index
+  uint64_t spg_magic;   // set index -> group index: (si * magic) >> 40
+  int spanq;            // sets per accumulation span inside a k-block (4, 2, 1) or 0 (generic)
 };
 
-// Byte offset of word w of row r inside a SWIZZLE_64B stage (64-byte rows).
-__device__ __forceinline__ uint32_t swz64(int r, int w) {
-  return (uint32_t)(r * kStageRowBytes + ((((w >> 2) ^ (r >> 1)) & 3) << 4) + ((w & 3) << 2));
-}
+struct DecodeLaunch {
+  CUtensorMap wmap[kMaxProblems];
+  DecodeProblem prob[kMaxProblems];
+  int count;
+  int total_units;
+  int gmax;  // largest K/group, row pitch bound of the scale/zero buffers
+};
 
 // FP16 pairs (base + q) of one word: pairs[i] holds positions (i, i + CPW/2).
 template <int BITS>
@@ -116,392 +127,558 @@ __device__ __forceinline__ uint4 correction_frag(int e) {
   }
 }
 
-template <int BITS, int RGW, int NT, int EPI>
-__global__ void __launch_bounds__(kThreads, NT == 2 ? 2 : 3)
-    decode_kernel(const __grid_constant__ CUtensorMap wmap, const DecodeParams p) {
+// The CTA's units in snake order: round r takes unit r*P + b (r even) or
+// r*P + P-1-b (r odd).
+struct UnitCursor {
+  int r;
+  int unit;  // global unit index, or -1 past the end
+  __device__ __forceinline__ void set(int round, int b, int P, int total) {
+    r = round;
+    const int u = round * P + ((round & 1) ? (P - 1 - b) : b);
+    unit = u < total ? u : -1;
+  }
+};
+
+__device__ __forceinline__ int problem_of(const DecodeLaunch& L, int unit) {
+  int p = 0;
+#pragma unroll 1
+  for (int i = 1; i < L.count; ++i)
+    if (unit >= L.prob[i].unit_begin) p = i;
+  return p;
+}
+
+// Producer of one warp's TMA ring: items are (unit, k-block) in the order the
+// warp consumes them, issued up to kSPW ahead.
+struct Producer {
+  UnitCursor u;
+  int kb, p, issued, warp, b, P;
+  __device__ __forceinline__ void init(const DecodeLaunch& L, int warp_, int b_, int P_) {
+    warp = warp_;
+    b = b_;
+    P = P_;
+    issued = 0;
+    u.set(0, b, P, L.total_units);
+    p = u.unit >= 0 ? problem_of(L, u.unit) : 0;
+    kb = warp;
+    skip(L);
+  }
+  __device__ __forceinline__ void skip(const DecodeLaunch& L) {  // to the next unit that has a k-block for this warp
+    while (u.unit >= 0 && kb >= L.prob[p].nkb) {
+      u.set(u.r + 1, b, P, L.total_units);
+      kb = warp;
+      if (u.unit >= 0) p = problem_of(L, u.unit);
+    }
+  }
+  template <int ROWS>
+  __device__ __forceinline__ void issue(const DecodeLaunch& L, uint8_t* ring, uint64_t* full, uint64_t pol) {
+    if (u.unit < 0) return;
+    constexpr int STAGE_BYTES = ROWS * kStageRowBytes;
+    const int slot = warp * kSPW + (issued % kSPW);
+    mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
+    tma_load_2d_hint(&L.wmap[p], &full[slot], ring + slot * STAGE_BYTES, kb * kWordsPerKBlock,
+                     (u.unit - L.prob[p].unit_begin) * ROWS, pol);
+    ++issued;
+    kb += kWarps;
+    skip(L);
+  }
+};
+
+// Scales/zeros of one unit as {s, z} half2 pairs, row pitch G + 1 (odd: the
+// per-row reads of a warp hit distinct banks).  Thread t owns row t / 8 and
+// groups t % 8 + 8 j (coalesced 16-byte runs per row, no division).
+constexpr int kSzPerThread = 16;  // groups per row covered by the register prefetch: 8 * 16 = 128
+static_assert(kThreads == 256, "scale/zero staging maps 8 threads to each of 32 rows");
+
+template <int ROWS>
+__device__ __forceinline__ void load_unit_sz(const DecodeLaunch& L, int unit, int tid, uint32_t (&v)[kSzPerThread]) {
+  static_assert(ROWS == 32, "scale/zero staging assumes 32-row units");
+  if (unit < 0) return;
+  const DecodeProblem& pr = L.prob[problem_of(L, unit)];
+  const int n0 = (unit - pr.unit_begin) * ROWS;
+  const int row = tid >> 3;
+  if (n0 + row >= pr.N) return;
+  const int G = pr.G;
+  const size_t o = (size_t)(n0 + row) * G + (tid & 7);
+  const __half* S = pr.S + o;
+  const __half* Z = pr.Z + o;
+#pragma unroll
+  for (int j = 0; j < kSzPerThread; ++j) {
+    if ((tid & 7) + 8 * j < G) {
+      const uint32_t sv = __half_as_ushort(__ldg(S + 8 * j));
+      const uint32_t zv = __half_as_ushort(__ldg(Z + 8 * j));
+      v[j] = sv | (zv << 16);
+    }
+  }
+}
+
+template <int ROWS>
+__device__ __forceinline__ void store_unit_sz(const DecodeLaunch& L, int unit, int tid,
+                                              const uint32_t (&v)[kSzPerThread], uint32_t* dst) {
+  if (unit < 0) return;
+  const DecodeProblem& pr = L.prob[problem_of(L, unit)];
+  const int n0 = (unit - pr.unit_begin) * ROWS;
+  const int row = tid >> 3;
+  if (n0 + row >= pr.N) return;
+  const int G = pr.G;
+  uint32_t* d = dst + row * (G + 1) + (tid & 7);
+#pragma unroll
+  for (int j = 0; j < kSzPerThread; ++j)
+    if ((tid & 7) + 8 * j < G) d[8 * j] = v[j];
+  if (G > 8 * kSzPerThread) {  // more groups than the register prefetch covers: load the rest here
+    const size_t o = (size_t)(n0 + row) * G;
+    for (int gg = (tid & 7) + 8 * kSzPerThread; gg < G; gg += 8)
+      dst[row * (G + 1) + gg] = (uint32_t)__half_as_ushort(__ldg(pr.S + o + gg)) |
+                                ((uint32_t)__half_as_ushort(__ldg(pr.Z + o + gg)) << 16);
+  }
+}
+
+// Per-unit values of the current problem, held in registers.
+struct UnitRegs {
+  const __half* ap[2];  // this lane's activation row (token 8t + g) + its word offset
+  bool av[2];           // token valid
+  int K, nkb, nkb_full, gp;
+  uint64_t magic;
+  uint32_t szbase;
+};
+
+__device__ __forceinline__ void ldg_v4_pred(uint4& v, const __half* p, bool pred) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %5, 0;\n @p ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];\n}"
+      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+      : "l"(p), "r"((int)pred));
+}
+
+// Activations of the four sets of k-block kb for this lane: B-fragment raw
+// data (zero for tokens past M and codes past K).
+template <int BITS, int NTP>
+__device__ __forceinline__ void load_acts(const UnitRegs& ur, int kb, uint4 (&ax)[4][NTP], uint4 (&ay)[4][NTP]) {
   using F = Fmt<BITS>;
+  const bool partial = kb >= ur.nkb_full;
+#pragma unroll
+  for (int t = 0; t < NTP; ++t) {
+    const __half* ap = ur.ap[t] + kb * F::KBLK;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bool ok = ur.av[t] && (!partial || kb * F::KBLK + q * F::SETC < ur.K);
+      ax[q][t] = make_uint4(0, 0, 0, 0);
+      ldg_v4_pred(ax[q][t], ap + q * F::SETC, ok);
+      if constexpr (BITS == 2) {
+        ay[q][t] = make_uint4(0, 0, 0, 0);
+        ldg_v4_pred(ay[q][t], ap + q * F::SETC + 8, ok);
+      }
+    }
+  }
+}
+
+// One k-block (4 sets) of one warp: MMAs over the span(s), correction, and
+// the scaled accumulation into tot.  SPANQ: sets per span (4, 2, 1), or 0 when
+// the group size is not a multiple of the set width pattern (each set then
+// computes its own group index).
+template <int BITS, int RGW, int NTP, int SPANQ, bool FULL>
+__device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0, const uint32_t (&woff)[4], int g,
+                                       const uint4 (&ax)[4][NTP], const uint4 (&ay)[4][NTP],
+                                       float (&tot)[RGW][NTP][4]) {
+  using F = Fmt<BITS>;
+  constexpr bool partial = !FULL;
+  int gbase = 0;
+  if constexpr (SPANQ == 4) gbase = (int)(((uint64_t)(kb * 4) * ur.magic) >> 40);
+  if constexpr (SPANQ == 2) gbase = 2 * kb;
+  if constexpr (SPANQ == 1) gbase = 4 * kb;
+  float acc[RGW][NTP][4];
+  float corr[NTP][4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (partial && kb * F::KBLK + q * F::SETC >= ur.K) break;
+    constexpr int SQ = SPANQ == 0 ? 1 : SPANQ;
+    const bool span_start = (q % SQ) == 0;
+    const bool span_end = ((q % SQ) == SQ - 1) || (partial && kb * F::KBLK + (q + 1) * F::SETC >= ur.K);
+    // ---- B fragments (activations) ----
+    uint32_t bf[NTP][F::MPS][2];
+#pragma unroll
+    for (int t = 0; t < NTP; ++t) {
+      const uint4 x = ax[q][t];
+      if constexpr (BITS == 4) {
+        // x = (a0,a1)(a2,a3)(a4,a5)(a6,a7); pairs (0,4)(1,5) | (2,6)(3,7)
+        bf[t][0][0] = prmt(x.x, x.z, 0x5410);
+        bf[t][0][1] = prmt(x.x, x.z, 0x7632);
+        bf[t][1][0] = prmt(x.y, x.w, 0x5410);
+        bf[t][1][1] = prmt(x.y, x.w, 0x7632);
+      } else {
+        // x = a0..a7, y = a8..a15; pairs (2e, 2e+8) and (2e+1, 2e+9)
+        const uint4 y = ay[q][t];
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        const uint32_t ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          bf[t][e][0] = prmt(xs[e], ys[e], 0x5410);
+          bf[t][e][1] = prmt(xs[e], ys[e], 0x7632);
+        }
+      }
+    }
+    // ---- correction sums over the span ----
+#pragma unroll
+    for (int t = 0; t < NTP; ++t) {
+      if (span_start) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) corr[t][u] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < F::MPS; ++e) {
+        const uint4 ka = correction_frag<BITS>(e);
+        mma_16816(corr[t], ka.x, ka.y, ka.z, ka.w, bf[t][e][0], bf[t][e][1]);
+      }
+    }
+    // ---- weight rows: sums of a * (base + q) over the span ----
+    const uint32_t wq = wq0 + woff[q];
+#pragma unroll
+    for (int r = 0; r < RGW; ++r) {
+      const uint32_t wg = lds32(wq + (uint32_t)(16 * r) * kStageRowBytes);
+      const uint32_t wh = lds32(wq + (uint32_t)(16 * r + 8) * kStageRowBytes);
+      uint32_t pg[F::CPW / 2], ph[F::CPW / 2];
+      unpack_word<BITS>(wg, pg);
+      unpack_word<BITS>(wh, ph);
+#pragma unroll
+      for (int t = 0; t < NTP; ++t) {
+        if (span_start) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc[r][t][u] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < F::MPS; ++e)
+          mma_16816(acc[r][t], pg[2 * e], ph[2 * e], pg[2 * e + 1], ph[2 * e + 1], bf[t][e][0], bf[t][e][1]);
+      }
+    }
+    // ---- span end: remove base and zero point, apply the scale ----
+    if (span_end) {
+      int gi;
+      if constexpr (SPANQ == 0) gi = (int)(((uint64_t)(kb * 4 + q) * ur.magic) >> 40);
+      else gi = gbase + q / SQ;
+      const uint32_t sza = ur.szbase + (uint32_t)((g * ur.gp + gi) * 4);
+#pragma unroll
+      for (int r = 0; r < RGW; ++r) {
+        const uint32_t szg = lds32(sza + (uint32_t)(16 * r * ur.gp) * 4);
+        const uint32_t szh = lds32(sza + (uint32_t)((16 * r + 8) * ur.gp) * 4);
+        const float2 fg = __half22float2(*reinterpret_cast<const __half2*>(&szg));
+        const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&szh));
+#pragma unroll
+        for (int t = 0; t < NTP; ++t) {
+          // acc + corr0 + z * corr2 = sum a (q - z); then * s
+          tot[r][t][0] = fmaf(fg.x, fmaf(fg.y, corr[t][2], acc[r][t][0] + corr[t][0]), tot[r][t][0]);
+          tot[r][t][1] = fmaf(fg.x, fmaf(fg.y, corr[t][3], acc[r][t][1] + corr[t][1]), tot[r][t][1]);
+          tot[r][t][2] = fmaf(fh.x, fmaf(fh.y, corr[t][2], acc[r][t][2] + corr[t][0]), tot[r][t][2]);
+          tot[r][t][3] = fmaf(fh.x, fmaf(fh.y, corr[t][3], acc[r][t][3] + corr[t][1]), tot[r][t][3]);
+        }
+      }
+    }
+  }
+}
+
+// All k-blocks of one unit for this warp; activations are loaded one k-block
+// ahead.  Returns the partial sums in tot (NTP token tiles).
+template <int BITS, int RGW, int NTP, int SPANQ>
+__device__ __forceinline__ void run_unit(const DecodeLaunch& L, const UnitRegs& ur, int warp, int lane,
+                                         const uint32_t (&woff)[4], uint32_t ring_base, uint8_t* ring,
+                                         uint64_t* full, uint64_t pol, Producer& prod, int& consumed, bool& ok,
+                                         float (&tot)[RGW][NTP][4]) {
   constexpr int ROWS = 16 * RGW;
   constexpr int STAGE_BYTES = ROWS * kStageRowBytes;
-  constexpr int MT = 8 * NT;  // token slots
+  const int g = lane >> 2;
+#pragma unroll
+  for (int r = 0; r < RGW; ++r)
+#pragma unroll
+    for (int t = 0; t < NTP; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tot[r][t][i] = 0.f;
+  if (warp >= ur.nkb) return;
+  uint4 nx[4][NTP], ny[4][NTP];
+  load_acts<BITS, NTP>(ur, warp, nx, ny);
+  for (int kb = warp; kb < ur.nkb; kb += kWarps) {
+    uint4 ax[4][NTP], ay[4][NTP];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int t = 0; t < NTP; ++t) {
+        ax[q][t] = nx[q][t];
+        ay[q][t] = ny[q][t];
+      }
+    if (kb + kWarps < ur.nkb) load_acts<BITS, NTP>(ur, kb + kWarps, nx, ny);
+    const int slot = warp * kSPW + (consumed % kSPW);
+    if (ok) ok = mbar_wait(&full[slot], (consumed / kSPW) & 1, 0x112);
+    if (kb < ur.nkb_full)
+      kblock<BITS, RGW, NTP, SPANQ, true>(ur, kb, ring_base + (uint32_t)slot * STAGE_BYTES, woff, g, ax, ay, tot);
+    else
+      kblock<BITS, RGW, NTP, SPANQ, false>(ur, kb, ring_base + (uint32_t)slot * STAGE_BYTES, woff, g, ax, ay, tot);
+    ++consumed;
+    // this slot is free again: refill it with the warp's next item
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) prod.template issue<ROWS>(L, ring, full, pol);
+  }
+}
+
+template <int BITS, int RGW, int NT>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeLaunch L) {
+  constexpr int ROWS = 16 * RGW;
+  constexpr int STAGE_BYTES = ROWS * kStageRowBytes;
+  constexpr int MT = 8 * NT;    // token slots
+  constexpr int RP = ROWS + 4;  // reduction row pitch (conflict-free)
+  using F = Fmt<BITS>;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = smem;
-  __half* act = reinterpret_cast<__half*>(smem + kStages * STAGE_BYTES);
-  float2* sz = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(act) + (size_t)p.M * p.act_stride * 2);
-  float* part = reinterpret_cast<float*>(sz + ROWS * p.gsp);          // [ROWS][MT]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(part + ROWS * MT);     // full[S], empty[S]
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  float* red = reinterpret_cast<float*>(stages);  // reused after the main loop
+  uint8_t* ring = smem;  // [warp][kSPW][STAGE_BYTES]
+  const int szpitch = ROWS * (L.gmax + 1);  // uint32 {s,z} pairs per buffer
+  uint32_t* szb = reinterpret_cast<uint32_t*>(ring + kWarps * kSPW * STAGE_BYTES);  // [par][ROWS][G+1]
+  float* red = reinterpret_cast<float*>(szb + 2 * szpitch);                         // [par][warp][MT][RP]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kWarps * MT * RP);         // [warp][kSPW]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int row0 = blockIdx.x * ROWS;
-  const int rank = (int)blockIdx.y;  // == %cluster_ctarank (cluster dims (1, ksplit, 1))
-  const int kslice0 = rank * p.kslice;
-  const int klen = min(p.kslice, p.K - kslice0);
-  const int nkb = (klen + F::KBLK - 1) / F::KBLK;
-  const int gs0 = kslice0 / p.group;
+  const int g = lane >> 2;
+  const int c = lane & 3;
+  const int P = gridDim.x;
+  const int b = blockIdx.x;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
+    for (int i = 0; i < kWarps * kSPW; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
   if (tid == 0) pdl_launch_dependents();
 
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: TMA weight tiles ----------------
-    if (lane == 0) {
-      tma_prefetch_desc(&wmap);
-      const uint64_t pol = policy_evict_first();
-      const int x0 = kslice0 / F::CPW;
-      bool ok = true;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int slot = kb % kStages;
-        ok = mbar_wait(&empty[slot], ((kb / kStages) & 1) ^ 1, 0x101);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
-        tma_load_2d_hint(&wmap, &full[slot], stages + slot * STAGE_BYTES, x0 + kb * kWordsPerKBlock, row0, pol);
-      }
-      // drain: every issued copy has landed before the CTA may exit
-      for (int kb = max(0, nkb - kStages); kb < nkb; ++kb)
-        if (!mbar_wait(&full[kb % kStages], (kb / kStages) & 1, 0x102)) break;
-    }
-    __syncwarp();
-  } else {
-    // ---------------- consumers ----------------
-    // scales / zeros of this CTA's rows and K slice (independent of the previous kernel)
-    const int G = p.K / p.group;
-    for (int i = tid; i < ROWS * p.gs_count; i += kConsumerWarps * 32) {
-      const int r = i / p.gs_count, j = i - r * p.gs_count;
-      const int n = row0 + r;
-      float2 v = make_float2(0.f, 0.f);
-      if (n < p.N && gs0 + j < G) {
-        const size_t o = (size_t)n * G + gs0 + j;
-        v.x = __half2float(p.S[o]);
-        v.y = __half2float(p.Z[o]);
-      }
-      sz[r * p.gsp + j] = v;
-    }
-    pdl_wait();  // activations may come from the preceding kernel
-    // activations of this K slice, zero beyond K
-    {
-      const int chunks = p.kslice / 8;  // 16-byte chunks per token row
-      for (int i = tid; i < p.M * chunks; i += kConsumerWarps * 32) {
-        const int m = i / chunks, ch = i - m * chunks;
-        const int k = kslice0 + ch * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (k < p.K) v = *reinterpret_cast<const uint4*>(p.A + (size_t)m * p.lda + k);
-        *reinterpret_cast<uint4*>(act + (size_t)m * p.act_stride + ch * 8) = v;
-      }
-    }
-    named_barrier(1, kConsumerWarps * 32);
+  const uint64_t pol = policy_evict_first();
+  Producer prod;
+  prod.init(L, warp, b, P);
+  if (lane == 0) {
+    tma_prefetch_desc(&L.wmap[0]);
+    for (int i = 0; i < kSPW; ++i) prod.template issue<ROWS>(L, ring, full, pol);
+  }
+  // scales/zeros of the first unit (weights-side data: before the dependency wait)
+  {
+    UnitCursor u0;
+    u0.set(0, b, P, L.total_units);
+    uint32_t v[kSzPerThread];
+    load_unit_sz<ROWS>(L, u0.unit, tid, v);
+    store_unit_sz<ROWS>(L, u0.unit, tid, v, szb);
+  }
+  pdl_wait();  // activations (and the residual) may come from the preceding kernel
 
-    const int g = lane >> 2;
-    const int c = lane & 3;
+  // per-lane parts of the swizzled word addresses: row g of set q -> word 4q + c
+  uint32_t woff[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) woff[q] = (uint32_t)(g * kStageRowBytes + (((q ^ (g >> 1)) & 3) << 4) + (c << 2));
+
+  const uint32_t ring_base = smem_u32(ring);
+  const uint32_t szb_base = smem_u32(szb);
+  int consumed = 0;
+  bool ok = true;
+  __syncthreads();  // first unit's scales/zeros are in shared memory
+
+  UnitCursor uc;
+  uc.set(0, b, P, L.total_units);
+  for (int s = 0; uc.unit >= 0; ++s, uc.set(uc.r + 1, b, P, L.total_units)) {
+    const int par = s & 1;
+    const int p = problem_of(L, uc.unit);
+    const DecodeProblem& pr = L.prob[p];
+    const int n0 = (uc.unit - pr.unit_begin) * ROWS;
+    const int M = pr.M;
+    // next unit's scales/zeros: into registers now, into shared memory at this unit's barrier
+    UnitCursor un;
+    un.set(uc.r + 1, b, P, L.total_units);
+    uint32_t szn[kSzPerThread];
+    load_unit_sz<ROWS>(L, un.unit, tid, szn);
+
+    UnitRegs ur;
+    ur.K = pr.K;
+    ur.nkb = pr.nkb;
+    ur.nkb_full = pr.K / F::KBLK;
+    ur.gp = pr.G + 1;
+    ur.magic = pr.spg_magic;
+    ur.szbase = szb_base + (uint32_t)(par * szpitch) * 4;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int tok = 8 * t + g;
+      ur.av[t] = tok < M;
+      ur.ap[t] = pr.A + (size_t)(tok < M ? tok : 0) * pr.lda + c * F::CPW;
+    }
+    const int spanq = pr.spanq;
+
     float tot[RGW][NT][4];
-#pragma unroll
-    for (int r = 0; r < RGW; ++r)
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tot[r][t][i] = 0.f;
-
-    const uint32_t act_base = smem_u32(act);
-    const uint32_t sz_base = smem_u32(sz);
-    for (int kb = warp; kb < nkb; kb += kConsumerWarps) {
-      const int slot = kb % kStages;
-      if (!mbar_wait(&full[slot], (kb / kStages) & 1, 0x103)) break;
-      const uint32_t wbase = smem_u32(stages + slot * STAGE_BYTES);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int set_rel = kb * F::KBLK + q * F::SETC;
-        if (set_rel >= klen) break;
-        const int gl = (kslice0 + set_rel) / p.group - gs0;
-        // ---- B fragments (activations) and the per-set correction sums ----
-        uint32_t bf[NT][F::MPS][2];
-        float corr[NT][4];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const int tok = 8 * t + g;
-          uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
-          if (tok < p.M) {
-            const uint32_t a = act_base + (uint32_t)((tok * p.act_stride + set_rel + c * F::CPW) * 2);
-            x = lds128(a);
-            if constexpr (BITS == 2) y = lds128(a + 16);
-          }
-          if constexpr (BITS == 4) {
-            // codes of the word: x = (a0,a1)(a2,a3)(a4,a5)(a6,a7); pairs (0,4)(1,5) | (2,6)(3,7)
-            bf[t][0][0] = prmt(x.x, x.z, 0x5410);
-            bf[t][0][1] = prmt(x.x, x.z, 0x7632);
-            bf[t][1][0] = prmt(x.y, x.w, 0x5410);
-            bf[t][1][1] = prmt(x.y, x.w, 0x7632);
-          } else {
-            // x = a0..a7, y = a8..a15; pairs (2e, 2e+8) and (2e+1, 2e+9)
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-            const uint32_t ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              bf[t][e][0] = prmt(xs[e], ys[e], 0x5410);
-              bf[t][e][1] = prmt(xs[e], ys[e], 0x7632);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) corr[t][i] = 0.f;
-#pragma unroll
-          for (int e = 0; e < F::MPS; ++e) {
-            const uint4 ka = correction_frag<BITS>(e);
-            mma_16816(corr[t], ka.x, ka.y, ka.z, ka.w, bf[t][e][0], bf[t][e][1]);
-          }
-        }
-        // ---- weight rows ----
-#pragma unroll
-        for (int r = 0; r < RGW; ++r) {
-          const int rg = 16 * r + g;
-          const uint32_t wg = lds32(wbase + swz64(rg, 4 * q + c));
-          const uint32_t wh = lds32(wbase + swz64(rg + 8, 4 * q + c));
-          const float2 szg = lds64f(sz_base + (uint32_t)((rg * p.gsp + gl) * 8));
-          const float2 szh = lds64f(sz_base + (uint32_t)(((rg + 8) * p.gsp + gl) * 8));
-          uint32_t pg[F::CPW / 2], ph[F::CPW / 2];
-          unpack_word<BITS>(wg, pg);
-          unpack_word<BITS>(wh, ph);
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            float acc[4];
-            acc[0] = fmaf(szg.y, corr[t][2], corr[t][0]);
-            acc[1] = fmaf(szg.y, corr[t][3], corr[t][1]);
-            acc[2] = fmaf(szh.y, corr[t][2], corr[t][0]);
-            acc[3] = fmaf(szh.y, corr[t][3], corr[t][1]);
-#pragma unroll
-            for (int e = 0; e < F::MPS; ++e)
-              mma_16816(acc, pg[2 * e], ph[2 * e], pg[2 * e + 1], ph[2 * e + 1], bf[t][e][0], bf[t][e][1]);
-            tot[r][t][0] = fmaf(szg.x, acc[0], tot[r][t][0]);
-            tot[r][t][1] = fmaf(szg.x, acc[1], tot[r][t][1]);
-            tot[r][t][2] = fmaf(szh.x, acc[2], tot[r][t][2]);
-            tot[r][t][3] = fmaf(szh.x, acc[3], tot[r][t][3]);
-          }
+    bool done = false;
+    if constexpr (NT == 2) {
+      if (M > 8) {
+        done = true;
+        switch (spanq) {
+          case 4: run_unit<BITS, RGW, 2, 4>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
+          case 2: run_unit<BITS, RGW, 2, 2>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
+          case 1: run_unit<BITS, RGW, 2, 1>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
+          default: run_unit<BITS, RGW, 2, 0>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    // all consumers done with the stage buffers -> reuse them for the reduction
-    named_barrier(1, kConsumerWarps * 32);
-    {
-      float* my = red + warp * (ROWS * MT);
+    if (!done) {
+      float t1[RGW][1][4];
+      switch (spanq) {
+        case 4: run_unit<BITS, RGW, 1, 4>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
+        case 2: run_unit<BITS, RGW, 1, 2>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
+        case 1: run_unit<BITS, RGW, 1, 1>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
+        default: run_unit<BITS, RGW, 1, 0>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
+      }
 #pragma unroll
       for (int r = 0; r < RGW; ++r)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const int ra = 16 * r + g, tk = 8 * t + 2 * c;
-          my[ra * MT + tk] = tot[r][t][0];
-          my[ra * MT + tk + 1] = tot[r][t][1];
-          my[(ra + 8) * MT + tk] = tot[r][t][2];
-          my[(ra + 8) * MT + tk + 1] = tot[r][t][3];
-        }
-    }
-    named_barrier(1, kConsumerWarps * 32);
-    for (int i = tid; i < ROWS * MT; i += kConsumerWarps * 32) {
-      float v = red[i];
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) v += red[w * ROWS * MT + i];
-      part[i] = v;
+          for (int i = 0; i < 4; ++i) tot[r][t][i] = t == 0 ? t1[r][0][i] : 0.f;
     }
-  }
 
-  // ---------------- cross-CTA (cluster) reduction and epilogue ----------------
-  __syncwarp();
-  if (p.ksplit > 1) cluster_sync();
-  else __syncthreads();
-  {
-    // rank r finalizes rows [r * rpr, min(ROWS, (r + 1) * rpr)) of the tile
-    const int rpr = (ROWS + p.ksplit - 1) / p.ksplit;
-    const int rbeg = rank * rpr;
-    const int rcnt = max(0, min(ROWS, rbeg + rpr) - rbeg);
-    const int mt = p.M < MT ? p.M : MT;
-    const uint32_t part_addr = smem_u32(part);
-    for (int i = tid; i < rcnt * mt; i += kThreads) {
-      const int tk = i / rcnt;
-      const int r = rbeg + (i - tk * rcnt);
-      const int n = row0 + r;
-      float v;
-      if (p.ksplit > 1) {
-        v = 0.f;
-        for (int j = 0; j < p.ksplit; ++j)
-          v += ld_shared_cluster_f32(map_shared_rank(part_addr + (uint32_t)((r * MT + tk) * 4), (uint32_t)j));
-      } else {
-        v = part[r * MT + tk];
+    // ---- unit reduction: fixed-order sum of the eight warps' partials ----
+    float* myred = red + (size_t)(par * kWarps + warp) * MT * RP;
+#pragma unroll
+    for (int r = 0; r < RGW; ++r)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int ra = 16 * r + g, tk = 8 * t + 2 * c;
+        myred[tk * RP + ra] = tot[r][t][0];
+        myred[(tk + 1) * RP + ra] = tot[r][t][1];
+        myred[tk * RP + ra + 8] = tot[r][t][2];
+        myred[(tk + 1) * RP + ra + 8] = tot[r][t][3];
       }
-      if (n < p.N) {
+    // publish the next unit's scales/zeros into the other buffer
+    store_unit_sz<ROWS>(L, un.unit, tid, szn, szb + (par ^ 1) * szpitch);
+    named_barrier(1, kThreads);
+    {
+      const float* rb = red + (size_t)par * kWarps * MT * RP;
+      const int rows = min(ROWS, pr.N - n0);
+      const int epi = pr.epi;
+      for (int i = tid; i < ROWS * M; i += kThreads) {
+        const int row = i % ROWS, tk = i / ROWS;
+        if (row >= rows) continue;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += rb[(w * MT + tk) * RP + row];
+        const int n = n0 + row;
         __half h = __float2half_rn(v);
-        if constexpr (EPI == kEpiRelu) h = relu_half(h);
-        if constexpr (EPI == kEpiResidual) {
-          float* xp = p.X + (size_t)tk * p.ldx + n;
+        if (epi == kEpiRelu) h = relu_half(h);
+        if (epi == kEpiResidual) {
+          float* xp = pr.X + (size_t)tk * pr.ldx + n;
           *xp = *xp + __half2float(h);
         } else {
-          p.C[(size_t)tk * p.ldc + n] = h;
+          pr.C[(size_t)tk * pr.ldc + n] = h;
         }
       }
     }
   }
-  __syncwarp();
-  if (p.ksplit > 1) cluster_sync();  // keep shared memory alive until all ranks have read it
+
+  // error path only: copies still in flight land before the CTA exits
+  if (!ok && lane == 0) {
+    for (int j = consumed; j < prod.issued; ++j)
+      if (!mbar_wait(&full[warp * kSPW + (j % kSPW)], (j / kSPW) & 1, 0x113)) break;
+  }
 }
 
-struct DecodeCfg {
-  int rgw;     // row groups (16 rows) per warp: 4 or 2
-  int ksplit;  // cluster size along K
-  int kslice;  // codes per CTA
-};
+uint64_t magic_div40(int d) { return (((uint64_t)1) << 40) / (uint64_t)d + 1; }
 
-template <int BITS>
-DecodeCfg choose_cfg(int M, int N, int K, int sms) {
-  const int kblk = Fmt<BITS>::KBLK;
-  const int nkb = (K + kblk - 1) / kblk;
-  DecodeCfg best{4, 1, nkb * kblk};
-  long best_score = -1;
-  const char* env = getenv("TLQ_DECODE_CFG");  // "rgw,ksplit" (tuning sweeps)
-  if (env) {
-    int a = 0, b = 0;
-    if (sscanf(env, "%d,%d", &a, &b) == 2 && (a == 2 || a == 4) && b >= 1 && b <= 8) {
-      const int per = (nkb + b - 1) / b;
-      return DecodeCfg{a, (nkb + per - 1) / per, per * kblk};
-    }
-  }
-  for (int rgw : {4, 2}) {
-    for (int ks : {1, 2, 4, 8}) {
-      if (ks > nkb) continue;
-      const int per = (nkb + ks - 1) / ks;
-      const int ks_eff = (nkb + per - 1) / per;
-      const long ctas = (long)((N + 16 * rgw - 1) / (16 * rgw)) * ks_eff;
-      // score: enough CTAs to cover the GPU twice, all four warps busy, then
-      // prefer fewer cluster ranks and wider row tiles
-      long score = 0;
-      score += (ctas >= 2L * sms) ? 4000 : (ctas * 4000) / (2L * sms);
-      score += (per >= kConsumerWarps) ? 1000 : per * 250;
-      score -= ks_eff * 10;
-      score += rgw * 5;
-      if ((long)M * (per * kblk + 64) * 2 > 96 * 1024) score -= 100000;  // activation tile too large
-      if (score > best_score) {
-        best_score = score;
-        best = DecodeCfg{rgw, ks_eff, per * kblk};
-      }
-    }
-  }
-  return best;
-}
-
-template <int BITS, int RGW, int NT, int EPI>
-tlq_status launch_impl(const GemmArgs& a, const DecodeCfg& cfg, cudaStream_t stream) {
+template <int BITS, int RGW, int NT>
+tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   using F = Fmt<BITS>;
   constexpr int ROWS = 16 * RGW;
   constexpr int MT = 8 * NT;
-  DecodeParams p;
-  p.A = a.A;
-  p.lda = a.lda;
-  p.S = a.S;
-  p.Z = a.Z;
-  p.C = a.C;
-  p.ldc = a.ldc;
-  p.X = a.X;
-  p.ldx = a.ldx;
-  p.M = a.M;
-  p.N = a.N;
-  p.K = a.K;
-  p.group = a.group;
-  p.kslice = cfg.kslice;
-  p.ksplit = cfg.ksplit;
-  // activation row stride: >= kslice, stride*2 == kActMod (mod 128)
-  {
-    int s = cfg.kslice;
-    while ((s * 2) % 128 != F::kActMod) s += 8;
-    p.act_stride = s;
+  static_assert(sizeof(DecodeLaunch) < 30000, "kernel parameter space");
+  DecodeLaunch L;
+  memset(&L, 0, sizeof(L));
+  // problems with more k-blocks per unit first (snake order then balances)
+  int order[kMaxProblems];
+  for (int i = 0; i < count; ++i) order[i] = i;
+  std::stable_sort(order, order + count, [&](int x, int y) { return a[x].K > a[y].K; });
+  int units = 0;
+  int gmax = 1;
+  for (int j = 0; j < count; ++j) {
+    const GemmArgs& g = a[order[j]];
+    DecodeProblem& pr = L.prob[j];
+    pr.A = g.A;
+    pr.S = g.S;
+    pr.Z = g.Z;
+    pr.C = g.C;
+    pr.X = g.X;
+    pr.lda = g.lda;
+    pr.ldc = g.ldc;
+    pr.ldx = g.ldx;
+    pr.M = g.M;
+    pr.N = g.N;
+    pr.K = g.K;
+    pr.G = g.K / g.group;
+    pr.epi = g.epi;
+    pr.ntiles = (g.N + ROWS - 1) / ROWS;
+    pr.nkb = (g.K + F::KBLK - 1) / F::KBLK;
+    pr.unit_begin = units;
+    {
+      const int spg = g.group / F::SETC;  // sets per group
+      pr.spanq = (spg % 4 == 0) ? 4 : (spg == 2 ? 2 : (spg == 1 ? 1 : 0));
+      pr.spg_magic = magic_div40(pr.spanq == 4 ? spg : spg);
+    }
+    units += pr.ntiles;
+    gmax = std::max(gmax, pr.G);
+    const uint64_t wpr = (uint64_t)g.K / F::CPW;
+    tlq_status st = encode_tiled_2d(&L.wmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT32, g.W, wpr, (uint64_t)g.N, wpr * 4,
+                                    kWordsPerKBlock, ROWS, CU_TENSOR_MAP_SWIZZLE_64B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (st != TLQ_OK) return st;
   }
-  // groups touched by one slice: at most kslice/group + 1 (slices start on k-block bounds)
-  const int gcount = (cfg.kslice + a.group - 1) / a.group + 1;
-  p.gs_count = gcount;
-  p.gsp = gcount | 1;
+  L.count = count;
+  L.total_units = units;
+  L.gmax = gmax;
 
-  CUtensorMap map;
-  const uint64_t wpr = (uint64_t)a.K / F::CPW;
-  tlq_status st = encode_tiled_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, wpr, (uint64_t)a.N, wpr * 4,
-                                  kWordsPerKBlock, ROWS, CU_TENSOR_MAP_SWIZZLE_64B,
-                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  if (st != TLQ_OK) return st;
-
-  const size_t smem = 1024 + (size_t)kStages * ROWS * kStageRowBytes + (size_t)a.M * p.act_stride * 2 +
-                      (size_t)ROWS * p.gsp * 8 + (size_t)ROWS * MT * 4 + 2 * kStages * 8;
-  static_assert(kConsumerWarps * ROWS * MT * 4 <= kStages * ROWS * kStageRowBytes, "reduction buffer");
+  const size_t smem = 1024 + (size_t)kWarps * kSPW * ROWS * kStageRowBytes + (size_t)2 * ROWS * (gmax + 1) * 4 +
+                      (size_t)2 * kWarps * MT * (ROWS + 4) * 4 + kWarps * kSPW * 8;
   if (smem > (size_t)device_info().smem_optin)
-    return set_error(TLQ_EUNSUPPORTED, "decode: shared memory %zu exceeds the device limit", smem);
-
-  auto kern = decode_kernel<BITS, RGW, NT, EPI>;
+    return set_error(TLQ_EUNSUPPORTED, "decode: K/group = %d needs %zu bytes of shared memory (limit %d)", gmax,
+                     smem, device_info().smem_optin);
+  auto kern = decode_kernel<BITS, RGW, NT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    device_info().smem_optin);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, device_info().smem_optin);
   });
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "decode: cudaFuncSetAttribute");
 
+  const int grid = std::max(1, std::min(units, device_info().sms));
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)((a.N + ROWS - 1) / ROWS), (unsigned)cfg.ksplit, 1);
+  lc.gridDim = dim3((unsigned)grid, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
-  cudaLaunchAttribute attrs[2];
-  int na = 0;
-  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
-  if (cfg.ksplit > 1) {
-    attrs[na].id = cudaLaunchAttributeClusterDimension;
-    attrs[na].val.clusterDim.x = 1;
-    attrs[na].val.clusterDim.y = (unsigned)cfg.ksplit;
-    attrs[na].val.clusterDim.z = 1;
-    ++na;
-  }
-  lc.attrs = attrs;
-  lc.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&lc, kern, map, p);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = &attr;
+  lc.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&lc, kern, L);
   if (e != cudaSuccess) return cuda_error(e, "decode: launch");
-  if (log_enabled()) {
-    fprintf(stderr, "[tlq] decode int%d M=%d N=%d K=%d group=%d: rows/CTA=%d ksplit=%d kslice=%d grid=%u smem=%zu\n",
-            BITS, a.M, a.N, a.K, a.group, ROWS, cfg.ksplit, cfg.kslice, lc.gridDim.x * lc.gridDim.y, smem);
-  }
+  if (log_enabled())
+    fprintf(stderr, "[tlq] decode int%d: %d problem(s), %d units of %d rows, grid %d, smem %zu\n", BITS, count, units,
+            ROWS, grid, smem);
   return TLQ_OK;
 }
 
-template <int BITS, int RGW, int NT>
-tlq_status dispatch_epi(const GemmArgs& a, const DecodeCfg& cfg, cudaStream_t s) {
-  switch (a.epi) {
-    case kEpiStore: return launch_impl<BITS, RGW, NT, kEpiStore>(a, cfg, s);
-    case kEpiRelu: return launch_impl<BITS, RGW, NT, kEpiRelu>(a, cfg, s);
-    default: return launch_impl<BITS, RGW, NT, kEpiResidual>(a, cfg, s);
-  }
-}
-
 template <int BITS>
-tlq_status dispatch_bits(const GemmArgs& a, cudaStream_t s) {
-  const DecodeCfg cfg = choose_cfg<BITS>(a.M, a.N, a.K, device_info().sms);
-  const bool two = a.M > 8;
-  if (cfg.rgw == 4) return two ? dispatch_epi<BITS, 4, 2>(a, cfg, s) : dispatch_epi<BITS, 4, 1>(a, cfg, s);
-  return two ? dispatch_epi<BITS, 2, 2>(a, cfg, s) : dispatch_epi<BITS, 2, 1>(a, cfg, s);
+tlq_status dispatch_bits(const GemmArgs* a, int count, cudaStream_t s) {
+  bool two = false;
+  for (int i = 0; i < count; ++i) two |= a[i].M > 8;
+  return two ? launch_impl<BITS, 2, 2>(a, count, s) : launch_impl<BITS, 2, 1>(a, count, s);
 }
 
 }  // namespace
 
-tlq_status launch_decode(const GemmArgs& a, cudaStream_t stream) {
-  if (a.M < 1 || a.M > 16) return set_error(TLQ_EINVAL, "decode: M=%d outside 1..16", a.M);
-  return a.bits == 4 ? dispatch_bits<4>(a, stream) : dispatch_bits<2>(a, stream);
+tlq_status launch_decode(const GemmArgs* a, int count, cudaStream_t stream) {
+  if (count < 1 || count > kMaxProblems)
+    return set_error(TLQ_EINVAL, "decode: %d problems (1..%d per launch)", count, kMaxProblems);
+  for (int i = 0; i < count; ++i) {
+    if (a[i].M < 1 || a[i].M > 16) return set_error(TLQ_EINVAL, "decode: M=%d outside 1..16", a[i].M);
+    if (a[i].bits != a[0].bits) return set_error(TLQ_EINVAL, "decode: mixed bit widths in one launch");
+  }
+  return a[0].bits == 4 ? dispatch_bits<4>(a, count, stream) : dispatch_bits<2>(a, count, stream);
 }
 
 }  // namespace tlq

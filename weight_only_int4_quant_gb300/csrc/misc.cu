@@ -124,7 +124,7 @@ tlq_status launch_rmsnorm(const float* x, __half* h, int M, int D, int normalize
   at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at.val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = &at;
-  lc.numAttrs = 1;
+  lc.numAttrs = pdl_enabled() ? 1 : 0;
   return cuda_error(cudaLaunchKernelEx(&lc, rmsnorm_kernel, x, h, D, normalize), "rmsnorm: launch");
 }
 
