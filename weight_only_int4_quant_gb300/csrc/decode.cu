@@ -8,13 +8,13 @@
 // speeds decode up, so the kernel is built to stream weight bytes at HBM rate.
 //
 // Design (GB300):
-//  * Persistent: one CTA per SM walks a list of work units (a 32-row tile of
+//  * Persistent: one CTA per SM walks a list of work units (a 64-row tile of
 //    one problem, all of K).  Problems are ordered by unit cost and units are
 //    dealt to CTAs in snake order, which balances the bytes per SM; a launch
 //    may hold up to 16 independent problems (a whole decode step), so the
 //    ~2-3 us fixed cost of a launch is paid once.
 //  * Each of the 8 warps owns every 8th k-block (16 packed words per row) of a
-//    unit and streams its packed weights through a private 4-stage TMA ring
+//    unit and streams its packed weights through a private 2-stage TMA ring
 //    (SWIZZLE_64B, so that the transposed word reads are bank-conflict free).
 //    The rings run ahead across unit boundaries.
 //  * Scales and zeros of the next unit are prefetched into registers while the
@@ -53,7 +53,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSPW = 4;             // TMA stages per warp
+constexpr int kSPW = 2;             // TMA stages per warp
 constexpr int kWordsPerKBlock = 16; // per row: 64 bytes
 constexpr int kStageRowBytes = kWordsPerKBlock * 4;
 constexpr int kMaxProblems = kMaxDecodeProblems;
@@ -127,17 +127,16 @@ __device__ __forceinline__ uint4 correction_frag(int e) {
   }
 }
 
-// The CTA's units in snake order: round r takes unit r*P + b (r even) or
-// r*P + P-1-b (r odd).
-struct UnitCursor {
-  int r;
-  int unit;  // global unit index, or -1 past the end
-  __device__ __forceinline__ void set(int round, int b, int P, int total) {
-    r = round;
-    const int u = round * P + ((round & 1) ? (P - 1 - b) : b);
-    unit = u < total ? u : -1;
-  }
+// The CTA's units, dealt in snake order (round r takes global unit r*P + b
+// when r is even, r*P + P-1-b when odd) and tabulated once in shared memory:
+// problem index, first row and k-block count of each of the CTA's units.
+struct Sched {
+  int p;
+  int n0;
+  int nkb;
+  int pad;
 };
+constexpr int kMaxRounds = 256;  // units per CTA; the launcher caps total units at kMaxRounds * grid
 
 __device__ __forceinline__ int problem_of(const DecodeLaunch& L, int unit) {
   int p = 0;
@@ -150,85 +149,90 @@ __device__ __forceinline__ int problem_of(const DecodeLaunch& L, int unit) {
 // Producer of one warp's TMA ring: items are (unit, k-block) in the order the
 // warp consumes them, issued up to kSPW ahead.
 struct Producer {
-  UnitCursor u;
-  int kb, p, issued, warp, b, P;
-  __device__ __forceinline__ void init(const DecodeLaunch& L, int warp_, int b_, int P_) {
-    warp = warp_;
-    b = b_;
-    P = P_;
-    issued = 0;
-    u.set(0, b, P, L.total_units);
-    p = u.unit >= 0 ? problem_of(L, u.unit) : 0;
-    kb = warp;
-    skip(L);
-  }
-  __device__ __forceinline__ void skip(const DecodeLaunch& L) {  // to the next unit that has a k-block for this warp
-    while (u.unit >= 0 && kb >= L.prob[p].nkb) {
-      u.set(u.r + 1, b, P, L.total_units);
+  int ri, kb, issued, warp, nrounds;
+  __device__ __forceinline__ void skip(const Sched* tab) {  // to the next unit with a k-block for this warp
+    while (ri < nrounds && kb >= tab[ri].nkb) {
+      ++ri;
       kb = warp;
-      if (u.unit >= 0) p = problem_of(L, u.unit);
     }
   }
+  __device__ __forceinline__ void init(const Sched* tab, int warp_, int nrounds_) {
+    warp = warp_;
+    nrounds = nrounds_;
+    issued = 0;
+    ri = 0;
+    kb = warp;
+    skip(tab);
+  }
   template <int ROWS>
-  __device__ __forceinline__ void issue(const DecodeLaunch& L, uint8_t* ring, uint64_t* full, uint64_t pol) {
-    if (u.unit < 0) return;
+  __device__ __forceinline__ void issue(const DecodeLaunch& L, const Sched* tab, uint8_t* ring, uint64_t* full,
+                                        uint64_t pol) {
+    if (ri >= nrounds) return;
     constexpr int STAGE_BYTES = ROWS * kStageRowBytes;
     const int slot = warp * kSPW + (issued % kSPW);
+    const Sched e = tab[ri];
     mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
-    tma_load_2d_hint(&L.wmap[p], &full[slot], ring + slot * STAGE_BYTES, kb * kWordsPerKBlock,
-                     (u.unit - L.prob[p].unit_begin) * ROWS, pol);
+    tma_load_2d_hint(&L.wmap[e.p], &full[slot], ring + slot * STAGE_BYTES, kb * kWordsPerKBlock, e.n0, pol);
     ++issued;
     kb += kWarps;
-    skip(L);
+    skip(tab);
   }
 };
 
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Scales/zeros of one unit as {s, z} half2 pairs, row pitch G + 1 (odd: the
-// per-row reads of a warp hit distinct banks).  Thread t owns row t / 8 and
-// groups t % 8 + 8 j (coalesced 16-byte runs per row, no division).
-constexpr int kSzPerThread = 16;  // groups per row covered by the register prefetch: 8 * 16 = 128
-static_assert(kThreads == 256, "scale/zero staging maps 8 threads to each of 32 rows");
+// per-row reads of a warp hit distinct banks).  With TPR = kThreads / ROWS
+// threads per row, thread t owns row t / TPR and groups t % TPR + TPR * j
+// (coalesced runs per row, no division).
+constexpr int kSzPerThread = 16;  // groups per thread held in registers by the one-unit-ahead prefetch
 
 template <int ROWS>
-__device__ __forceinline__ void load_unit_sz(const DecodeLaunch& L, int unit, int tid, uint32_t (&v)[kSzPerThread]) {
-  static_assert(ROWS == 32, "scale/zero staging assumes 32-row units");
-  if (unit < 0) return;
-  const DecodeProblem& pr = L.prob[problem_of(L, unit)];
-  const int n0 = (unit - pr.unit_begin) * ROWS;
-  const int row = tid >> 3;
+__device__ __forceinline__ void load_unit_sz(const DecodeProblem& pr, int n0, int tid, uint32_t (&v)[kSzPerThread]) {
+  constexpr int TPR = kThreads / ROWS;
+  const int row = tid / TPR;
+  const int g0 = tid % TPR;
   if (n0 + row >= pr.N) return;
   const int G = pr.G;
-  const size_t o = (size_t)(n0 + row) * G + (tid & 7);
+  const size_t o = (size_t)(n0 + row) * G + g0;
   const __half* S = pr.S + o;
   const __half* Z = pr.Z + o;
 #pragma unroll
   for (int j = 0; j < kSzPerThread; ++j) {
-    if ((tid & 7) + 8 * j < G) {
-      const uint32_t sv = __half_as_ushort(__ldg(S + 8 * j));
-      const uint32_t zv = __half_as_ushort(__ldg(Z + 8 * j));
+    if (TPR * j >= G) break;
+    if (g0 + TPR * j < G) {
+      const uint32_t sv = __half_as_ushort(__ldg(S + TPR * j));
+      const uint32_t zv = __half_as_ushort(__ldg(Z + TPR * j));
       v[j] = sv | (zv << 16);
     }
   }
 }
 
 template <int ROWS>
-__device__ __forceinline__ void store_unit_sz(const DecodeLaunch& L, int unit, int tid,
-                                              const uint32_t (&v)[kSzPerThread], uint32_t* dst) {
-  if (unit < 0) return;
-  const DecodeProblem& pr = L.prob[problem_of(L, unit)];
-  const int n0 = (unit - pr.unit_begin) * ROWS;
-  const int row = tid >> 3;
+__device__ __forceinline__ void store_unit_sz(const DecodeProblem& pr, int n0, int tid,
+                                              const uint32_t (&v)[kSzPerThread], uint32_t dst) {
+  constexpr int TPR = kThreads / ROWS;
+  const int row = tid / TPR;
+  const int g0 = tid % TPR;
   if (n0 + row >= pr.N) return;
   const int G = pr.G;
-  uint32_t* d = dst + row * (G + 1) + (tid & 7);
+  const uint32_t d = dst + (uint32_t)(row * (G + 1) + g0) * 4;
 #pragma unroll
-  for (int j = 0; j < kSzPerThread; ++j)
-    if ((tid & 7) + 8 * j < G) d[8 * j] = v[j];
-  if (G > 8 * kSzPerThread) {  // more groups than the register prefetch covers: load the rest here
+  for (int j = 0; j < kSzPerThread; ++j) {
+    if (TPR * j >= G) break;
+    if (g0 + TPR * j < G) sts32(d + 4 * TPR * j, v[j]);
+  }
+  if (G > TPR * kSzPerThread) {  // more groups than the register prefetch covers: load the rest here
     const size_t o = (size_t)(n0 + row) * G;
-    for (int gg = (tid & 7) + 8 * kSzPerThread; gg < G; gg += 8)
-      dst[row * (G + 1) + gg] = (uint32_t)__half_as_ushort(__ldg(pr.S + o + gg)) |
-                                ((uint32_t)__half_as_ushort(__ldg(pr.Z + o + gg)) << 16);
+    for (int gg = g0 + TPR * kSzPerThread; gg < G; gg += TPR)
+      sts32(dst + (uint32_t)(row * (G + 1) + gg) * 4,
+            (uint32_t)__half_as_ushort(__ldg(pr.S + o + gg)) | ((uint32_t)__half_as_ushort(__ldg(pr.Z + o + gg)) << 16));
   }
 }
 
@@ -373,13 +377,16 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
   }
 }
 
-// All k-blocks of one unit for this warp; activations are loaded one k-block
-// ahead.  Returns the partial sums in tot (NTP token tiles).
-template <int BITS, int RGW, int NTP, int SPANQ>
-__device__ __forceinline__ void run_unit(const DecodeLaunch& L, const UnitRegs& ur, int warp, int lane,
+// All k-blocks of one unit for this warp.  Activations run one k-block ahead
+// in nx/ny (NT tiles): on entry they hold this warp's first k-block of the
+// unit, on exit the first k-block of the next unit (nu), so no unit starts
+// on an exposed global load.
+template <int BITS, int RGW, int NTP, int SPANQ, int NT>
+__device__ __forceinline__ void run_unit(const DecodeLaunch& L, const Sched* tab, const UnitRegs& ur,
+                                         const UnitRegs& nu, bool has_next, int warp, int lane,
                                          const uint32_t (&woff)[4], uint32_t ring_base, uint8_t* ring,
                                          uint64_t* full, uint64_t pol, Producer& prod, int& consumed, bool& ok,
-                                         float (&tot)[RGW][NTP][4]) {
+                                         uint4 (&nx)[4][NT], uint4 (&ny)[4][NT], float (&tot)[RGW][NTP][4]) {
   constexpr int ROWS = 16 * RGW;
   constexpr int STAGE_BYTES = ROWS * kStageRowBytes;
   const int g = lane >> 2;
@@ -389,9 +396,6 @@ __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const UnitRegs& 
     for (int t = 0; t < NTP; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) tot[r][t][i] = 0.f;
-  if (warp >= ur.nkb) return;
-  uint4 nx[4][NTP], ny[4][NTP];
-  load_acts<BITS, NTP>(ur, warp, nx, ny);
   for (int kb = warp; kb < ur.nkb; kb += kWarps) {
     uint4 ax[4][NTP], ay[4][NTP];
 #pragma unroll
@@ -401,7 +405,10 @@ __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const UnitRegs& 
         ax[q][t] = nx[q][t];
         ay[q][t] = ny[q][t];
       }
-    if (kb + kWarps < ur.nkb) load_acts<BITS, NTP>(ur, kb + kWarps, nx, ny);
+    if (kb + kWarps < ur.nkb)
+      load_acts<BITS, NT>(ur, kb + kWarps, nx, ny);
+    else if (has_next && warp < nu.nkb)
+      load_acts<BITS, NT>(nu, warp, nx, ny);
     const int slot = warp * kSPW + (consumed % kSPW);
     if (ok) ok = mbar_wait(&full[slot], (consumed / kSPW) & 1, 0x112);
     if (kb < ur.nkb_full)
@@ -412,8 +419,9 @@ __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const UnitRegs& 
     // this slot is free again: refill it with the warp's next item
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) prod.template issue<ROWS>(L, ring, full, pol);
+    if (lane == 0) prod.template issue<ROWS>(L, tab, ring, full, pol);
   }
+  if (warp >= ur.nkb && has_next && warp < nu.nkb) load_acts<BITS, NT>(nu, warp, nx, ny);
 }
 
 template <int BITS, int RGW, int NT>
@@ -431,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   uint32_t* szb = reinterpret_cast<uint32_t*>(ring + kWarps * kSPW * STAGE_BYTES);  // [par][ROWS][G+1]
   float* red = reinterpret_cast<float*>(szb + 2 * szpitch);                         // [par][warp][MT][RP]
   uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kWarps * MT * RP);         // [warp][kSPW]
+  Sched* tab = reinterpret_cast<Sched*>(full + kWarps * kSPW);                      // [kMaxRounds]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -444,23 +453,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     for (int i = 0; i < kWarps * kSPW; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
   }
-  __syncthreads();
+  // this CTA's units: round r = tid
+  int nrounds;
+  {
+    const int r = tid;
+    const int u = r * P + ((r & 1) ? (P - 1 - b) : b);
+    const bool valid = r < kMaxRounds && u < L.total_units;
+    if (valid) {
+      const int p = problem_of(L, u);
+      Sched e;
+      e.p = p;
+      e.n0 = (u - L.prob[p].unit_begin) * ROWS;
+      e.nkb = L.prob[p].nkb;
+      e.pad = 0;
+      tab[r] = e;
+    }
+    nrounds = __syncthreads_count(valid);  // also publishes the barrier inits and the table
+  }
   if (tid == 0) pdl_launch_dependents();
 
   const uint64_t pol = policy_evict_first();
   Producer prod;
-  prod.init(L, warp, b, P);
+  prod.init(tab, warp, nrounds);
   if (lane == 0) {
     tma_prefetch_desc(&L.wmap[0]);
-    for (int i = 0; i < kSPW; ++i) prod.template issue<ROWS>(L, ring, full, pol);
+    for (int i = 0; i < kSPW; ++i) prod.template issue<ROWS>(L, tab, ring, full, pol);
   }
+  const uint32_t szb_base = smem_u32(szb);
   // scales/zeros of the first unit (weights-side data: before the dependency wait)
-  {
-    UnitCursor u0;
-    u0.set(0, b, P, L.total_units);
+  if (nrounds > 0) {
     uint32_t v[kSzPerThread];
-    load_unit_sz<ROWS>(L, u0.unit, tid, v);
-    store_unit_sz<ROWS>(L, u0.unit, tid, v, szb);
+    const DecodeProblem& pr0 = L.prob[tab[0].p];
+    load_unit_sz<ROWS>(pr0, tab[0].n0, tid, v);
+    store_unit_sz<ROWS>(pr0, tab[0].n0, tid, v, szb_base);
   }
   pdl_wait();  // activations (and the residual) may come from the preceding kernel
 
@@ -470,37 +495,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   for (int q = 0; q < 4; ++q) woff[q] = (uint32_t)(g * kStageRowBytes + (((q ^ (g >> 1)) & 3) << 4) + (c << 2));
 
   const uint32_t ring_base = smem_u32(ring);
-  const uint32_t szb_base = smem_u32(szb);
+  const uint32_t red_base = smem_u32(red);
   int consumed = 0;
   bool ok = true;
   __syncthreads();  // first unit's scales/zeros are in shared memory
 
-  UnitCursor uc;
-  uc.set(0, b, P, L.total_units);
-  for (int s = 0; uc.unit >= 0; ++s, uc.set(uc.r + 1, b, P, L.total_units)) {
-    const int par = s & 1;
-    const int p = problem_of(L, uc.unit);
-    const DecodeProblem& pr = L.prob[p];
-    const int n0 = (uc.unit - pr.unit_begin) * ROWS;
-    const int M = pr.M;
-    // next unit's scales/zeros: into registers now, into shared memory at this unit's barrier
-    UnitCursor un;
-    un.set(uc.r + 1, b, P, L.total_units);
-    uint32_t szn[kSzPerThread];
-    load_unit_sz<ROWS>(L, un.unit, tid, szn);
-
-    UnitRegs ur;
+  auto make_regs = [&](int s_, UnitRegs& ur) {
+    const Sched e = tab[s_];
+    const DecodeProblem& pr = L.prob[e.p];
     ur.K = pr.K;
-    ur.nkb = pr.nkb;
+    ur.nkb = e.nkb;
     ur.nkb_full = pr.K / F::KBLK;
     ur.gp = pr.G + 1;
     ur.magic = pr.spg_magic;
-    ur.szbase = szb_base + (uint32_t)(par * szpitch) * 4;
+    ur.szbase = szb_base + (uint32_t)((s_ & 1) * szpitch) * 4;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int tok = 8 * t + g;
-      ur.av[t] = tok < M;
-      ur.ap[t] = pr.A + (size_t)(tok < M ? tok : 0) * pr.lda + c * F::CPW;
+      ur.av[t] = tok < pr.M;
+      ur.ap[t] = pr.A + (size_t)(tok < pr.M ? tok : 0) * pr.lda + c * F::CPW;
+    }
+  };
+  // activations of this warp's first k-block of the first unit
+  uint4 nx[4][NT], ny[4][NT];
+  UnitRegs ur, nu;
+  if (nrounds > 0) {
+    make_regs(0, ur);
+    if (warp < ur.nkb) load_acts<BITS, NT>(ur, warp, nx, ny);
+  }
+
+  for (int s = 0; s < nrounds; ++s) {
+    const int par = s & 1;
+    const Sched e = tab[s];
+    const DecodeProblem& pr = L.prob[e.p];
+    const int n0 = e.n0;
+    const int M = pr.M;
+    const bool has_next = s + 1 < nrounds;
+    // next unit's scales/zeros: into registers now, into shared memory at this unit's barrier
+    uint32_t szn[kSzPerThread];
+    if (has_next) {
+      load_unit_sz<ROWS>(L.prob[tab[s + 1].p], tab[s + 1].n0, tid, szn);
+      make_regs(s + 1, nu);
     }
     const int spanq = pr.spanq;
 
@@ -510,20 +545,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       if (M > 8) {
         done = true;
         switch (spanq) {
-          case 4: run_unit<BITS, RGW, 2, 4>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
-          case 2: run_unit<BITS, RGW, 2, 2>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
-          case 1: run_unit<BITS, RGW, 2, 1>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
-          default: run_unit<BITS, RGW, 2, 0>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, tot); break;
+          case 4: run_unit<BITS, RGW, 2, 4, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+          case 2: run_unit<BITS, RGW, 2, 2, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+          case 1: run_unit<BITS, RGW, 2, 1, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+          default: run_unit<BITS, RGW, 2, 0, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
         }
       }
     }
     if (!done) {
       float t1[RGW][1][4];
       switch (spanq) {
-        case 4: run_unit<BITS, RGW, 1, 4>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
-        case 2: run_unit<BITS, RGW, 1, 2>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
-        case 1: run_unit<BITS, RGW, 1, 1>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
-        default: run_unit<BITS, RGW, 1, 0>(L, ur, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, t1); break;
+        case 4: run_unit<BITS, RGW, 1, 4, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+        case 2: run_unit<BITS, RGW, 1, 2, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+        case 1: run_unit<BITS, RGW, 1, 1, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+        default: run_unit<BITS, RGW, 1, 0, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
       }
 #pragma unroll
       for (int r = 0; r < RGW; ++r)
@@ -534,19 +569,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
 
     // ---- unit reduction: fixed-order sum of the eight warps' partials ----
-    float* myred = red + (size_t)(par * kWarps + warp) * MT * RP;
+    {
+      const uint32_t myred = red_base + (uint32_t)((par * kWarps + warp) * MT * RP) * 4;
 #pragma unroll
-    for (int r = 0; r < RGW; ++r)
+      for (int r = 0; r < RGW; ++r)
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int ra = 16 * r + g, tk = 8 * t + 2 * c;
-        myred[tk * RP + ra] = tot[r][t][0];
-        myred[(tk + 1) * RP + ra] = tot[r][t][1];
-        myred[tk * RP + ra + 8] = tot[r][t][2];
-        myred[(tk + 1) * RP + ra + 8] = tot[r][t][3];
-      }
+        for (int t = 0; t < NT; ++t) {
+          if (t == 1 && M <= 8) continue;
+          const int ra = 16 * r + g, tk = 8 * t + 2 * c;
+          sts_f32(myred + (uint32_t)(tk * RP + ra) * 4, tot[r][t][0]);
+          sts_f32(myred + (uint32_t)((tk + 1) * RP + ra) * 4, tot[r][t][1]);
+          sts_f32(myred + (uint32_t)(tk * RP + ra + 8) * 4, tot[r][t][2]);
+          sts_f32(myred + (uint32_t)((tk + 1) * RP + ra + 8) * 4, tot[r][t][3]);
+        }
+    }
     // publish the next unit's scales/zeros into the other buffer
-    store_unit_sz<ROWS>(L, un.unit, tid, szn, szb + (par ^ 1) * szpitch);
+    if (s + 1 < nrounds)
+      store_unit_sz<ROWS>(L.prob[tab[s + 1].p], tab[s + 1].n0, tid, szn, szb_base + (uint32_t)((par ^ 1) * szpitch) * 4);
     named_barrier(1, kThreads);
     {
       const float* rb = red + (size_t)par * kWarps * MT * RP;
@@ -569,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
       }
     }
+    if (has_next) ur = nu;
   }
 
   // error path only: copies still in flight land before the CTA exits
@@ -631,7 +671,7 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   L.gmax = gmax;
 
   const size_t smem = 1024 + (size_t)kWarps * kSPW * ROWS * kStageRowBytes + (size_t)2 * ROWS * (gmax + 1) * 4 +
-                      (size_t)2 * kWarps * MT * (ROWS + 4) * 4 + kWarps * kSPW * 8;
+                      (size_t)2 * kWarps * MT * (ROWS + 4) * 4 + kWarps * kSPW * 8 + (size_t)kMaxRounds * sizeof(Sched);
   if (smem > (size_t)device_info().smem_optin)
     return set_error(TLQ_EUNSUPPORTED, "decode: K/group = %d needs %zu bytes of shared memory (limit %d)", gmax,
                      smem, device_info().smem_optin);
@@ -644,6 +684,8 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "decode: cudaFuncSetAttribute");
 
   const int grid = std::max(1, std::min(units, device_info().sms));
+  if (units > kMaxRounds * grid)
+    return set_error(TLQ_EUNSUPPORTED, "decode: %d row tiles exceed %d per launch", units, kMaxRounds * grid);
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
@@ -666,7 +708,7 @@ template <int BITS>
 tlq_status dispatch_bits(const GemmArgs* a, int count, cudaStream_t s) {
   bool two = false;
   for (int i = 0; i < count; ++i) two |= a[i].M > 8;
-  return two ? launch_impl<BITS, 2, 2>(a, count, s) : launch_impl<BITS, 2, 1>(a, count, s);
+  return two ? launch_impl<BITS, 4, 2>(a, count, s) : launch_impl<BITS, 4, 1>(a, count, s);
 }
 
 }  // namespace
