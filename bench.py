@@ -240,7 +240,7 @@ def kernel_hash():
 # dram bytes (read + write) per launch of the decode kernel for the headline
 # step, from the ncu capture summarised in profiles/ (None until captured for
 # the current kernel source).
-NCU_TRAFFIC = {"kernel_hash": None, "bytes_per_launch": None}
+NCU_TRAFFIC = {"kernel_hash": "32975138245c6b89", "bytes_per_launch": 82885632}  # profiles/decode_kernel_int4_decode_step.md
 
 
 def run_tlq(args, rank, world, dist):
