@@ -82,12 +82,21 @@ struct DecodeProblem {
   int spanq;            // sets per accumulation span inside a k-block (4, 2, 1) or 0 (generic)
 };
 
+// Per-CTA unit lists built on the host (longest-first greedy on estimated
+// unit cost), for launches of up to kMaxListUnits units on up to kMaxListGrid
+// CTAs; larger launches deal units in snake order on the device instead.
+constexpr int kMaxListUnits = 2048;
+constexpr int kMaxListGrid = 256;
+
 struct DecodeLaunch {
   CUtensorMap wmap[kMaxProblems];
   DecodeProblem prob[kMaxProblems];
   int count;
   int total_units;
-  int gmax;  // largest K/group, row pitch bound of the scale/zero buffers
+  int gmax;    // largest K/group, row pitch bound of the scale/zero buffers
+  int listed;  // 1: CTA b runs units[cta_off[b] .. cta_off[b+1]); 0: snake order
+  uint16_t cta_off[kMaxListGrid + 1];
+  uint16_t units[kMaxListUnits];
 };
 
 // FP16 pairs (base + q) of one word: pairs[i] holds positions (i, i + CPW/2).
@@ -127,9 +136,10 @@ __device__ __forceinline__ uint4 correction_frag(int e) {
   }
 }
 
-// The CTA's units, dealt in snake order (round r takes global unit r*P + b
-// when r is even, r*P + P-1-b when odd) and tabulated once in shared memory:
-// problem index, first row and k-block count of each of the CTA's units.
+// The CTA's units, tabulated once in shared memory (problem index, first row
+// and k-block count of each): from the host-built list when there is one,
+// else dealt in snake order (round r takes global unit r*P + b when r is
+// even, r*P + P-1-b when odd).
 struct Sched {
   int p;
   int n0;
@@ -457,8 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   int nrounds;
   {
     const int r = tid;
-    const int u = r * P + ((r & 1) ? (P - 1 - b) : b);
-    const bool valid = r < kMaxRounds && u < L.total_units;
+    int u = -1;
+    if (L.listed) {
+      const int off = L.cta_off[b];
+      if (r < L.cta_off[b + 1] - off) u = L.units[off + r];
+    } else {
+      const int su = r * P + ((r & 1) ? (P - 1 - b) : b);
+      if (r < kMaxRounds && su < L.total_units) u = su;
+    }
+    const bool valid = u >= 0;
     if (valid) {
       const int p = problem_of(L, u);
       Sched e;
@@ -620,6 +637,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
 uint64_t magic_div40(int d) { return (((uint64_t)1) << 40) / (uint64_t)d + 1; }
 
+// Longest-processing-time-first assignment of the launch's units to `grid`
+// CTAs: units in decreasing cost order, each to the CTA with the smallest
+// load so far (ties: lowest index).  A unit's cost is its k-block count
+// weighted by the token tiles it computes (two tiles cost about 1.7x one,
+// measured).  Returns false when some CTA would hold more than kMaxRounds
+// units.
+bool build_unit_lists(DecodeLaunch& L, int grid) {
+  const int units = L.total_units;
+  if (units > kMaxListUnits || grid > kMaxListGrid) return false;
+  int pord[kMaxProblems];
+  uint32_t cost[kMaxProblems];
+  for (int j = 0; j < L.count; ++j) {
+    pord[j] = j;
+    cost[j] = (uint32_t)L.prob[j].nkb * (L.prob[j].M > 8 ? 17u : 10u);
+  }
+  std::stable_sort(pord, pord + L.count, [&](int x, int y) { return cost[x] > cost[y]; });
+  // binary min-heap of (load, cta)
+  uint64_t heap[kMaxListGrid];
+  for (int i = 0; i < grid; ++i) heap[i] = (uint64_t)i;  // load 0: already a heap
+  uint16_t cta_of[kMaxListUnits];
+  uint16_t count_of[kMaxListGrid] = {};
+  for (int j = 0; j < L.count; ++j) {
+    const DecodeProblem& pr = L.prob[pord[j]];
+    for (int t = 0; t < pr.ntiles; ++t) {
+      const uint64_t top = heap[0];
+      const int c = (int)(top & 0xFFFFu);
+      if (++count_of[c] > kMaxRounds) return false;
+      cta_of[pr.unit_begin + t] = (uint16_t)c;
+      uint64_t v = top + ((uint64_t)cost[pord[j]] << 16);
+      int i = 0;  // sift down
+      for (;;) {
+        const int l = 2 * i + 1, r = l + 1;
+        int m = i;
+        uint64_t mv = v;
+        if (l < grid && heap[l] < mv) { m = l; mv = heap[l]; }
+        if (r < grid && heap[r] < mv) { m = r; mv = heap[r]; }
+        if (m == i) break;
+        heap[i] = heap[m];
+        i = m;
+      }
+      heap[i] = v;
+    }
+  }
+  L.cta_off[0] = 0;
+  for (int c = 0; c < grid; ++c) L.cta_off[c + 1] = (uint16_t)(L.cta_off[c] + count_of[c]);
+  uint16_t fill[kMaxListGrid];
+  for (int c = 0; c < grid; ++c) fill[c] = L.cta_off[c];
+  // each CTA's list in assignment order (costliest units first)
+  for (int j = 0; j < L.count; ++j) {
+    const DecodeProblem& pr = L.prob[pord[j]];
+    for (int t = 0; t < pr.ntiles; ++t) {
+      const int u = pr.unit_begin + t;
+      L.units[fill[cta_of[u]]++] = (uint16_t)u;
+    }
+  }
+  return true;
+}
+
 template <int BITS, int RGW, int NT>
 tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   using F = Fmt<BITS>;
@@ -684,6 +759,7 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "decode: cudaFuncSetAttribute");
 
   const int grid = std::max(1, std::min(units, device_info().sms));
+  L.listed = build_unit_lists(L, grid) ? 1 : 0;
   if (units > kMaxRounds * grid)
     return set_error(TLQ_EUNSUPPORTED, "decode: %d row tiles exceed %d per launch", units, kMaxRounds * grid);
   cudaLaunchConfig_t lc = {};
