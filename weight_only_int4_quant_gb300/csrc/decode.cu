@@ -343,25 +343,30 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
       }
     }
     // ---- weight rows: sums of a * (base + q) over the span ----
+    // All row groups are unpacked first; the MMAs then run k-slice-major, so
+    // consecutive MMAs of one accumulator are RGW * NTP issues apart.
     const uint32_t wq = wq0 + woff[q];
+    uint32_t pg[RGW][F::CPW / 2], ph[RGW][F::CPW / 2];
 #pragma unroll
     for (int r = 0; r < RGW; ++r) {
-      const uint32_t wg = lds32(wq + (uint32_t)(16 * r) * kStageRowBytes);
-      const uint32_t wh = lds32(wq + (uint32_t)(16 * r + 8) * kStageRowBytes);
-      uint32_t pg[F::CPW / 2], ph[F::CPW / 2];
-      unpack_word<BITS>(wg, pg);
-      unpack_word<BITS>(wh, ph);
+      unpack_word<BITS>(lds32(wq + (uint32_t)(16 * r) * kStageRowBytes), pg[r]);
+      unpack_word<BITS>(lds32(wq + (uint32_t)(16 * r + 8) * kStageRowBytes), ph[r]);
+    }
+    if (span_start) {
 #pragma unroll
-      for (int t = 0; t < NTP; ++t) {
-        if (span_start) {
+      for (int r = 0; r < RGW; ++r)
+#pragma unroll
+        for (int t = 0; t < NTP; ++t)
 #pragma unroll
           for (int u = 0; u < 4; ++u) acc[r][t][u] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < F::MPS; ++e)
-          mma_16816(acc[r][t], pg[2 * e], ph[2 * e], pg[2 * e + 1], ph[2 * e + 1], bf[t][e][0], bf[t][e][1]);
-      }
     }
+#pragma unroll
+    for (int e = 0; e < F::MPS; ++e)
+#pragma unroll
+      for (int t = 0; t < NTP; ++t)
+#pragma unroll
+        for (int r = 0; r < RGW; ++r)
+          mma_16816(acc[r][t], pg[r][2 * e], ph[r][2 * e], pg[r][2 * e + 1], ph[r][2 * e + 1], bf[t][e][0], bf[t][e][1]);
     // ---- span end: remove base and zero point, apply the scale ----
     if (span_end) {
       int gi;
