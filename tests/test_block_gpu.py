@@ -43,6 +43,17 @@ def test_block_small_matches_oracle(lib, bits, M, L):
 
 
 @pytest.mark.parametrize("bits", [4, 2])
+def test_block_two_token_tiles_per_cta(lib, monkeypatch, bits):
+    """Prefill with two 128-token tiles per CTA (forced) in all three epilogues: store, ReLU, residual."""
+    monkeypatch.setenv("TLQ_PREFILL_NMT", "2")
+    case = synth.block_case(200, bits, seed=41, D=256, F=512)
+    blk, host = make_block(lib, case)
+    got = run_gpu(lib, blk, case["x0"], 2)
+    ref = oracle.loop_block(case["x0"], host, bits, case["group"], 2, normalize=True)
+    assert_close(got, ref, "block two token tiles int%d" % bits)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
 def test_block_without_norm_one_iteration(lib, bits):
     case = synth.block_case(4, bits, seed=31, D=256, F=512)
     blk, host = make_block(lib, case, normalize=False)

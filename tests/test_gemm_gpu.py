@@ -212,6 +212,30 @@ def test_prefill_every_k_split(lib, monkeypatch, bits, ks):
     assert_close(C, ref, "prefill ksplit %s int%d" % (ks, bits))
 
 
+@pytest.mark.parametrize("nmt", ["1", "2"])
+@pytest.mark.parametrize("bits,group,M,N,K", [
+    (4, 128, 129, 256, 512),   # second token tile holds one row
+    (4, 128, 200, 520, 1024),  # ragged tokens and rows
+    (4, 32, 300, 264, 96),     # ragged K, two groups per stage
+    (4, 128, 512, 512, 2048),
+    (2, 64, 257, 256, 448),
+    (2, 128, 384, 512, 1024),
+])
+def test_prefill_token_tiles_per_cta(lib, monkeypatch, nmt, bits, group, M, N, K):
+    """One and two 128-token tiles per CTA (forced) both match the oracle, and each other bit for bit when
+    neither splits K (a k split changes the FP32 summation order)."""
+    case = synth.gemm_case(M, N, K, bits, group, seed=3 * M + K, a_scale=0.5)
+    monkeypatch.setenv("TLQ_PREFILL_KSPLIT", "1")
+    monkeypatch.setenv("TLQ_PREFILL_NMT", nmt)
+    Wd, C = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(C, ref, "prefill nmt %s int%d M%d N%d K%d" % (nmt, bits, M, N, K))
+    monkeypatch.setenv("TLQ_PREFILL_NMT", "2" if nmt == "1" else "1")
+    C2 = lib.quant_gemm(dev(case["A"]), Wd, dev(case["scales"]), dev(case["zeros"]), bits, group)
+    assert torch.equal(torch.from_numpy(C).cuda().view(torch.int16), C2.view(torch.int16)), \
+        "one and two token tiles per CTA differ"
+
+
 @pytest.mark.parametrize("proj", list(synth.SHAPES))
 @pytest.mark.parametrize("M", [128, 512, 2048])
 def test_prefill_full_size_sampled(lib, proj, M):

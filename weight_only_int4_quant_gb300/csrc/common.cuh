@@ -192,6 +192,11 @@ __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 // Arrive (release, cluster scope) on an mbarrier given by its shared::cluster
 // address, possibly in another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {

@@ -7,8 +7,10 @@
 // item 2 (weights stay packed in GPU memory; dequantization happens in the
 // GEMM, the FP16 body cache being the opt-in alternative).
 //
-// Tile: 128 tokens (UMMA M) x 256 weight rows (UMMA N) x 64 k per stage,
-// FP32 accumulator in TMEM (256 columns).  Warp roles (320 threads):
+// Tile: NMT x 128 tokens (UMMA M, NMT = 1 or 2) x 256 weight rows (UMMA N) x
+// 64 k per stage, FP32 accumulators in TMEM (256 columns per 128 tokens).
+// With NMT = 2 one dequantized weight tile feeds two token tiles, halving the
+// dequantization work per MMA.  Warp roles (320 threads):
 //   warps 0-7  dequantize: each thread owns one weight row of the tile, reads
 //              its packed words straight from global memory (three stages
 //              ahead), rebuilds exact FP16 weights (q - z) * s and stores them
@@ -33,19 +35,24 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int kStagesP = 4;
 constexpr int kDqWarps = 8;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreadsP = 10 * 32;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
-constexpr uint32_t kTmemCols = 256;
 constexpr int kPrefetch = 3;          // dequant global-load distance (stages)
-constexpr int RED_PITCH = BM + 1;     // floats per column of the split-K partial tile
+
+template <int NMT>
+struct PCfg {
+  static constexpr int STAGES = NMT == 1 ? 4 : 3;
+  static constexpr int STAGE = NMT * A_STAGE + B_STAGE;
+  static constexpr uint32_t TMEM_COLS = 256u * NMT;
+};
 
 static_assert(BN == kDqWarps * 32, "one dequant thread per weight row");
-static_assert(BN * RED_PITCH * 4 <= kStagesP * (A_STAGE + B_STAGE), "split-K buffer fits in the stages");
+// split-K slots: ksplit x BM rows x (BN / ksplit + 4) floats, largest at ksplit = 8
+static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::STAGES * PCfg<1>::STAGE, "split-K slots fit in the stages");
 
 // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16,
 // both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -134,56 +141,36 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// Exact FP16 weights of one packed word: ((base + q) - base - z) * s, both
-// subtractions exact, one rounding in the multiply.  Writes the word's codes
-// in k order as 16-byte chunks (INT4: one chunk, INT2: two).
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// FP16 weights of one packed word in k order, w = q * s + (-(z * s)): byte j
+// of the word is copied into both halves (one PRMT), the codes it holds are
+// masked into the mantissas of (base + q) halves (one LOP3 per pair), the
+// bases are removed exactly (one HSUB2) and one FMA applies scale and zero
+// point.  INT4: out[j] = (w_2j, w_2j+1); INT2: out[2j], out[2j+1] =
+// (w_4j, w_4j+1), (w_4j+2, w_4j+3).
 template <int BITS>
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t z2, uint32_t (&out)[BITS == 4 ? 4 : 8]) {
-  if constexpr (BITS == 4) {
-    const uint32_t w8 = w >> 8;
-    uint32_t d0 = and_or(w, 0x000F000Fu, 0x64006400u);   // codes 0, 4 (+1024)
-    uint32_t d1 = and_or(w, 0x00F000F0u, 0x54005400u);   // codes 1, 5 (+64)
-    uint32_t d2 = and_or(w8, 0x000F000Fu, 0x64006400u);  // codes 2, 6 (+1024)
-    uint32_t d3 = and_or(w8, 0x00F000F0u, 0x54005400u);  // codes 3, 7 (+64)
-    d0 = hmul2u(hsub2u(hsub2u(d0, 0x64006400u), z2), s2);
-    d1 = hmul2u(hsub2u(hsub2u(d1, 0x54005400u), z2), s2);
-    d2 = hmul2u(hsub2u(hsub2u(d2, 0x64006400u), z2), s2);
-    d3 = hmul2u(hsub2u(hsub2u(d3, 0x54005400u), z2), s2);
-    out[0] = prmt(d0, d1, 0x5410);  // w0 w1
-    out[1] = prmt(d2, d3, 0x5410);  // w2 w3
-    out[2] = prmt(d0, d1, 0x7632);  // w4 w5
-    out[3] = prmt(d2, d3, 0x7632);  // w6 w7
-  } else {
-    const uint32_t w10 = w >> 10;
-    uint32_t d[8];
-    d[0] = and_or(w, 0x00030003u, 0x64006400u);
-    d[1] = and_or(w, 0x000C000Cu, 0x5C005C00u);
-    d[2] = and_or(w, 0x00300030u, 0x54005400u);
-    d[3] = and_or(w, 0x00C000C0u, 0x4C004C00u);
-    d[4] = and_or(w, 0x03000300u, 0x44004400u);
-    d[5] = and_or(w10, 0x00030003u, 0x64006400u);
-    d[6] = and_or(w10, 0x000C000Cu, 0x5C005C00u);
-    d[7] = and_or(w10, 0x00300030u, 0x54005400u);
-    const uint32_t base[8] = {0x64006400u, 0x5C005C00u, 0x54005400u, 0x4C004C00u,
-                              0x44004400u, 0x64006400u, 0x5C005C00u, 0x54005400u};
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t nzs2, uint32_t (&out)[BITS == 4 ? 4 : 8]) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = hmul2u(hsub2u(hsub2u(d[i], base[i]), z2), s2);
-    // d[i] = (w_i, w_{i+8})
-    out[0] = prmt(d[0], d[1], 0x5410);
-    out[1] = prmt(d[2], d[3], 0x5410);
-    out[2] = prmt(d[4], d[5], 0x5410);
-    out[3] = prmt(d[6], d[7], 0x5410);
-    out[4] = prmt(d[0], d[1], 0x7632);
-    out[5] = prmt(d[2], d[3], 0x7632);
-    out[6] = prmt(d[4], d[5], 0x7632);
-    out[7] = prmt(d[6], d[7], 0x7632);
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t x = prmt(w, 0u, (uint32_t)(j | (j << 8)));  // byte j in bytes 0 and 2
+    if constexpr (BITS == 4) {
+      const uint32_t h = and_or(x, 0x00F0000Fu, 0x54006400u);  // (1024 + q_2j, 64 + q_2j+1)
+      out[j] = hfma2u(hsub2u(h, 0x54006400u), s2, nzs2);
+    } else {
+      const uint32_t ha = and_or(x, 0x000C0003u, 0x5C006400u);  // (1024 + q_4j, 256 + q_4j+1)
+      const uint32_t hb = and_or(x, 0x00C00030u, 0x4C005400u);  // (64 + q_4j+2, 16 + q_4j+3)
+      out[2 * j] = hfma2u(hsub2u(ha, 0x5C006400u), s2, nzs2);
+      out[2 * j + 1] = hfma2u(hsub2u(hb, 0x4C005400u), s2, nzs2);
+    }
   }
 }
 
-__device__ __forceinline__ uint32_t half2_bits(__half a) {
-  const uint16_t b = __half_as_ushort(a);
-  return (uint32_t)b | ((uint32_t)b << 16);
-}
+__device__ __forceinline__ uint32_t bcast16(unsigned short b) { return (uint32_t)b * 0x00010001u; }
 
 template <int EPI>
 __device__ __forceinline__ void store_out(const PrefillParams& p, int m, int n, float v) {
@@ -197,9 +184,11 @@ __device__ __forceinline__ void store_out(const PrefillParams& p, int m, int n, 
   }
 }
 
-template <int BITS, int EPI>
+template <int BITS, int EPI, int NMT>
 __global__ void __launch_bounds__(kThreadsP, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap amap, const PrefillParams p) {
+  constexpr int kStagesP = PCfg<NMT>::STAGES;
+  constexpr uint32_t kTmemCols = PCfg<NMT>::TMEM_COLS;
   constexpr int CPW = 32 / BITS;
   constexpr int WPS = BK / CPW;                 // packed words per row per stage (8 or 4)
   constexpr int NV = WPS / 4;                   // uint4 loads per row per stage (2 or 1)
@@ -207,20 +196,20 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sa = smem;
-  uint8_t* sb = smem + kStagesP * A_STAGE;
+  uint8_t* sa = smem;                                // [stage][NMT][A_STAGE]
+  uint8_t* sb = smem + kStagesP * NMT * A_STAGE;     // [stage][B_STAGE]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sb + kStagesP * B_STAGE);
   uint64_t* full_a = bars;
   uint64_t* full_b = bars + kStagesP;
   uint64_t* empty = bars + 2 * kStagesP;
   uint64_t* accum = bars + 3 * kStagesP;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStagesP + 1);
-  float* red = reinterpret_cast<float*>(smem);  // split-K partial tile, after the main loop
+  float* red = reinterpret_cast<float*>(smem);  // split-K slots, after the main loop
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * BM;
+  const int m0 = blockIdx.y * BM * NMT;
   const int rank = (int)blockIdx.z;  // == %cluster_ctarank (cluster dims (1, 1, ksplit))
   const int k0 = rank * p.kslice;
   const int klen = min(p.kslice, p.K - k0);
@@ -241,6 +230,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) pdl_launch_dependents();
+  bool acc_ok = true;  // dequant warps: the accumulator is complete
 
   if (warp == kTmaWarp) {
     // ---------------- activations: TMA producer ----------------
@@ -250,8 +240,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       for (int kb = 0; kb < nkb; ++kb) {
         const int slot = kb % kStagesP;
         if (!mbar_wait(&empty[slot], ((kb / kStagesP) & 1) ^ 1, 0x201)) break;
-        mbar_arrive_expect_tx(&full_a[slot], A_STAGE);
-        tma_load_2d(&amap, &full_a[slot], sa + slot * A_STAGE, k0 + kb * BK, m0);
+        mbar_arrive_expect_tx(&full_a[slot], NMT * A_STAGE);
+#pragma unroll
+        for (int i = 0; i < NMT; ++i)
+          tma_load_2d(&amap, &full_a[slot], sa + (slot * NMT + i) * A_STAGE, k0 + kb * BK, m0 + i * BM);
       }
       for (int kb = max(0, nkb - kStagesP); kb < nkb; ++kb)
         if (!mbar_wait(&full_a[kb % kStagesP], (kb / kStagesP) & 1, 0x202)) break;
@@ -267,11 +259,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         ok = mbar_wait(&full_a[slot], par, 0x203) && mbar_wait(&full_b[slot], par, 0x204);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sa + slot * A_STAGE);
         const uint32_t b0 = smem_u32(sb + slot * B_STAGE);
 #pragma unroll
-        for (int kk = 0; kk < BK / UMMA_K; ++kk)
-          umma_f16(tmem, sw128_desc(a0 + kk * UMMA_K * 2), sw128_desc(b0 + kk * UMMA_K * 2), (kb | kk) != 0);
+        for (int i = 0; i < NMT; ++i) {
+          const uint32_t a0 = smem_u32(sa + (slot * NMT + i) * A_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk)
+            umma_f16(tmem + 256u * i, sw128_desc(a0 + kk * UMMA_K * 2), sw128_desc(b0 + kk * UMMA_K * 2),
+                     (kb | kk) != 0);
+        }
         umma_commit(&empty[slot]);
       }
       umma_commit(accum);
@@ -289,9 +285,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const __half* zrow = p.Z + (size_t)(row_ok ? n : 0) * G;
     const bool two_groups = (BITS == 4) && (p.group < BK);  // INT4 with group 32
 
+    // packed words and raw 16-bit scale/zero bits, kPrefetch stages ahead (the
+    // half2 broadcast happens at use, so no load is waited on at issue)
     uint4 ring[kPrefetch][NV];
-    uint32_t sring[kPrefetch][2], zring[kPrefetch][2];
-    auto issue = [&](int kb, uint4 (&dst)[NV], uint32_t (&sd)[2], uint32_t (&zd)[2]) {
+    unsigned short sring[kPrefetch][2], zring[kPrefetch][2];
+    auto issue = [&](int kb, uint4 (&dst)[NV], unsigned short (&sd)[2], unsigned short (&zd)[2]) {
       const int ks = k0 + kb * BK;
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
@@ -300,10 +298,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       const int g0 = ks / p.group;
       const int g1 = two_groups ? min(g0 + 1, G - 1) : g0;
-      sd[0] = row_ok ? half2_bits(srow[g0]) : 0u;
-      zd[0] = row_ok ? half2_bits(zrow[g0]) : 0u;
-      sd[1] = row_ok ? half2_bits(srow[g1]) : 0u;
-      zd[1] = row_ok ? half2_bits(zrow[g1]) : 0u;
+      const unsigned short* sp = reinterpret_cast<const unsigned short*>(srow);
+      const unsigned short* zp = reinterpret_cast<const unsigned short*>(zrow);
+      sd[0] = row_ok ? __ldg(sp + g0) : (unsigned short)0;
+      zd[0] = row_ok ? __ldg(zp + g0) : (unsigned short)0;
+      sd[1] = row_ok ? __ldg(sp + g1) : (unsigned short)0;
+      zd[1] = row_ok ? __ldg(zp + g1) : (unsigned short)0;
     };
 #pragma unroll
     for (int j = 0; j < kPrefetch; ++j)
@@ -318,7 +318,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           uint4 cur[NV];
 #pragma unroll
           for (int v = 0; v < NV; ++v) cur[v] = ring[j][v];
-          const uint32_t s_lo = sring[j][0], z_lo = zring[j][0], s_hi = sring[j][1], z_hi = zring[j][1];
+          const uint32_t s_lo = bcast16(sring[j][0]), s_hi = bcast16(sring[j][1]);
+          const uint32_t nzs_lo = hmul2u(bcast16(zring[j][0]), s_lo) ^ 0x80008000u;  // -(z * s)
+          const uint32_t nzs_hi = hmul2u(bcast16(zring[j][1]), s_hi) ^ 0x80008000u;
           if (kb + kPrefetch < nkb) issue(kb + kPrefetch, ring[j], sring[j], zring[j]);
           const int slot = kb % kStagesP;
           if (!mbar_wait(&empty[slot], ((kb / kStagesP) & 1) ^ 1, 0x205)) {
@@ -335,11 +337,25 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             wv[4 * v + 2] = cur[v].z;
             wv[4 * v + 3] = cur[v].w;
           }
+          if (row_ok && ks + BK <= p.K) {  // full stage: no per-word checks
+#pragma unroll
+            for (int wj = 0; wj < WPS; ++wj) {
+              const bool hi = two_groups && (wj >= WPS / 2);
+              uint32_t o[OUTW];
+              dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
+              if constexpr (BITS == 4) {
+                sts128(brow + (((uint32_t)wj ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
+              } else {
+                sts128(brow + (((uint32_t)(2 * wj) ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                sts128(brow + (((uint32_t)(2 * wj + 1) ^ (uint32_t)(r & 7)) << 4), o[4], o[5], o[6], o[7]);
+              }
+            }
+          } else {
 #pragma unroll
           for (int wj = 0; wj < WPS; ++wj) {
             const bool hi = two_groups && (wj >= WPS / 2);
             uint32_t o[OUTW];
-            dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? z_hi : z_lo, o);
+            dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
             const bool valid = row_ok && (ks + wj * CPW < p.K);
             if constexpr (BITS == 4) {
               const uint32_t c = (uint32_t)wj;
@@ -359,6 +375,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
               }
             }
           }
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&full_b[slot]);
@@ -367,20 +384,22 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
 
     // ---------------- epilogue: TMEM -> registers -> global ----------------
-    const bool acc_ok = mbar_wait(accum, 0, 0x206);
+    acc_ok = mbar_wait(accum, 0, 0x206);
     tc_fence_after();
     const int q = warp & 3;        // TMEM lane quarter this warp may access
     const int half = warp >> 2;    // column half
     const int mrow = 32 * q + lane;
-    const int m = m0 + mrow;
     if (acc_ok) {
       if (p.ksplit == 1) {
         pdl_wait();
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int ic = 0; ic < 4 * NMT; ++ic) {
+          const int cc = ic & 3;
+          const int mt = ic >> 2;  // token tile
+          const int m = m0 + mt * BM + mrow;
           const int col = half * 128 + cc * 32;
           uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * mt + col), v);
           if (m < p.M) {
             if constexpr (EPI == kEpiResidual) {
 #pragma unroll
@@ -408,38 +427,60 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
           }
         }
-      } else {
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int col = half * 128 + cc * 32;
-          uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) red[(col + i) * RED_PITCH + mrow] = __uint_as_float(v[i]);
-        }
       }
     }
   }
 
   // ---------------- split-K: reduce partial tiles across the cluster ----------------
-  if (p.ksplit > 1) {
+  // Rank o owns columns [o * cpr, (o + 1) * cpr).  After a first cluster
+  // barrier (every rank's stage memory is idle), each rank pushes its partial
+  // tile's columns to their owners with remote stores, slot = its own rank;
+  // after a second barrier each owner sums its slots in rank order (fixed,
+  // deterministic) with local loads and writes the outputs.
+  if (NMT == 1 && p.ksplit > 1) {
+    const int ks = p.ksplit;
+    const int cpr = BN / ks;  // 32, 64 or 128: a 32-column TMEM block never straddles two owners
+    const int pitch = cpr + 4;  // floats per row of a slot (16-byte aligned, staggered banks)
+    const uint32_t red_addr = smem_u32(red);
     __syncwarp();
     cluster_sync();
-    pdl_wait();
-    const int cpr = BN / p.ksplit;  // columns finalized by this rank (ksplit divides 256)
-    const int c0 = rank * cpr;
-    const uint32_t red_addr = smem_u32(red);
-    for (int i = threadIdx.x; i < BM * cpr; i += kThreadsP) {
-      const int mm = i / cpr;
-      const int col = c0 + (i - mm * cpr);
-      const int m = m0 + mm, n = n0 + col;
-      float acc = 0.f;
-      for (int j = 0; j < p.ksplit; ++j)
-        acc += ld_shared_cluster_f32(map_shared_rank(red_addr + (uint32_t)((col * RED_PITCH + mm) * 4), (uint32_t)j));
-      if (m < p.M && n < p.N) store_out<EPI>(p, m, n, acc);
+    if (warp < kDqWarps && acc_ok) {
+      const int q = warp & 3, half = warp >> 2;
+      const int mrow = 32 * q + lane;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        const int col = half * 128 + cc * 32;
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+        const int owner = col / cpr;
+        const uint32_t dst = map_shared_rank(
+            red_addr + (uint32_t)(((rank * BM + mrow) * pitch + (col - owner * cpr)) * 4), (uint32_t)owner);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) st_shared_cluster_v4(dst + 16u * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
     }
     __syncwarp();
     cluster_sync();
+    pdl_wait();
+    const int quads = cpr / 4;
+    for (int it = threadIdx.x; it < BM * quads; it += kThreadsP) {
+      const int mm = it / quads;
+      const int c4 = 4 * (it - mm * quads);
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < ks; ++j) {
+        const float4 x = *reinterpret_cast<const float4*>(red + ((size_t)(j * BM + mm) * pitch + c4));
+        a[0] += x.x;
+        a[1] += x.y;
+        a[2] += x.z;
+        a[3] += x.w;
+      }
+      const int m = m0 + mm, n = n0 + rank * cpr + c4;
+      if (m < p.M) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (n + i < p.N) store_out<EPI>(p, m, n + i, a[i]);
+      }
+    }
   }
 
   // ---------------- teardown ----------------
@@ -451,15 +492,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
 }
 
-template <int BITS, int EPI>
+template <int BITS, int EPI, int NMT>
 tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   const int sms = device_info().sms;
   const int ntile = (a.N + BN - 1) / BN;
-  const int mtile = (a.M + BM - 1) / BM;
+  const int mtile = (a.M + BM * NMT - 1) / (BM * NMT);
   const int nkb = (a.K + BK - 1) / BK;
   int ks = 1;
   const char* env = getenv("TLQ_PREFILL_KSPLIT");
-  if (env) {
+  if (NMT == 2) {
+    ks = 1;  // the split-K reduction buffer holds one token tile
+  } else if (env) {
     ks = atoi(env);
   } else {
     const int tiles = ntile * mtile;
@@ -498,8 +541,8 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (st != TLQ_OK) return st;
 
-  const size_t smem = 1024 + (size_t)kStagesP * (A_STAGE + B_STAGE) + 256;
-  auto kern = prefill_kernel<BITS, EPI>;
+  const size_t smem = 1024 + (size_t)PCfg<NMT>::STAGES * PCfg<NMT>::STAGE + 256;
+  auto kern = prefill_kernel<BITS, EPI, NMT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -531,17 +574,33 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, p);
   if (e != cudaSuccess) return cuda_error(e, "prefill: launch");
   if (log_enabled())
-    fprintf(stderr, "[tlq] prefill int%d M=%d N=%d K=%d group=%d: grid %dx%dx%d (ksplit %d, kslice %d) smem=%zu\n", BITS,
-            a.M, a.N, a.K, a.group, ntile, mtile, p.ksplit, p.ksplit, p.kslice, smem);
+    fprintf(stderr,
+            "[tlq] prefill int%d M=%d N=%d K=%d group=%d: %d token tile(s) per CTA, grid %dx%dx%d (kslice %d) "
+            "smem=%zu\n",
+            BITS, a.M, a.N, a.K, a.group, NMT, ntile, mtile, p.ksplit, p.kslice, smem);
   return TLQ_OK;
+}
+
+// Two token tiles per CTA when that still gives at least one CTA per SM
+// (TLQ_PREFILL_NMT=1|2 forces the choice; a forced k split implies one tile).
+template <int BITS, int EPI>
+tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
+  int nmt = 0;
+  if (const char* e = getenv("TLQ_PREFILL_NMT")) nmt = atoi(e);
+  if (nmt != 1 && nmt != 2) {
+    const int ntile = (a.N + BN - 1) / BN;
+    const int mt2 = (a.M + 2 * BM - 1) / (2 * BM);
+    nmt = (getenv("TLQ_PREFILL_KSPLIT") == nullptr && a.M > BM && ntile * mt2 >= device_info().sms) ? 2 : 1;
+  }
+  return nmt == 2 ? launch_impl<BITS, EPI, 2>(a, s) : launch_impl<BITS, EPI, 1>(a, s);
 }
 
 template <int BITS>
 tlq_status dispatch_epi(const GemmArgs& a, cudaStream_t s) {
   switch (a.epi) {
-    case kEpiStore: return launch_impl<BITS, kEpiStore>(a, s);
-    case kEpiRelu: return launch_impl<BITS, kEpiRelu>(a, s);
-    default: return launch_impl<BITS, kEpiResidual>(a, s);
+    case kEpiStore: return launch_pick<BITS, kEpiStore>(a, s);
+    case kEpiRelu: return launch_pick<BITS, kEpiRelu>(a, s);
+    default: return launch_pick<BITS, kEpiResidual>(a, s);
   }
 }
 
