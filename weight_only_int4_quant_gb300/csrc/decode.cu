@@ -248,12 +248,33 @@ __device__ __forceinline__ void store_unit_sz(const DecodeProblem& pr, int n0, i
 
 // Per-unit values of the current problem, held in registers.
 struct UnitRegs {
-  const __half* ap[2];  // this lane's activation row (token 8t + g) + its word offset
-  bool av[2];           // token valid
+  const __half* ap[2];  // this lane's activation row (token 8t + g, clamped to token 0 past M) + word offset
+  int qs;               // codes between this lane's words of consecutive sets
   int K, nkb, nkb_full, gp;
   uint64_t magic;
   uint32_t szbase;
 };
+
+// INT4 with whole-k-block groups uses the contiguous word mapping: lane c of
+// a row takes words 4c .. 4c+3 (one per set, one 16-byte shared load), else
+// set q of lane c is word 4q + c.  The k order inside a span does not matter
+// for a sum, only that the activations follow the same mapping.
+template <int BITS, int SPANQ>
+struct WordMap {
+  static constexpr bool CONTIG = (BITS == 4 && SPANQ == 4);
+};
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const __half* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
 
 __device__ __forceinline__ void ldg_v4_pred(uint4& v, const __half* p, bool pred) {
   asm volatile(
@@ -263,22 +284,35 @@ __device__ __forceinline__ void ldg_v4_pred(uint4& v, const __half* p, bool pred
 }
 
 // Activations of the four sets of k-block kb for this lane: B-fragment raw
-// data (zero for tokens past M and codes past K).
+// data.  Tokens past M read token 0 (their sums are never stored); in the
+// last, partial k-block the codes past K read zero (only the word-4q+c
+// mapping has partial k-blocks: the contiguous one needs K % 128 == 0).
 template <int BITS, int NTP>
 __device__ __forceinline__ void load_acts(const UnitRegs& ur, int kb, uint4 (&ax)[4][NTP], uint4 (&ay)[4][NTP]) {
   using F = Fmt<BITS>;
-  const bool partial = kb >= ur.nkb_full;
+  if (kb < ur.nkb_full) {
 #pragma unroll
-  for (int t = 0; t < NTP; ++t) {
-    const __half* ap = ur.ap[t] + kb * F::KBLK;
+    for (int t = 0; t < NTP; ++t) {
+      const __half* ap = ur.ap[t] + kb * F::KBLK;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const bool ok = ur.av[t] && (!partial || kb * F::KBLK + q * F::SETC < ur.K);
-      ax[q][t] = make_uint4(0, 0, 0, 0);
-      ldg_v4_pred(ax[q][t], ap + q * F::SETC, ok);
-      if constexpr (BITS == 2) {
-        ay[q][t] = make_uint4(0, 0, 0, 0);
-        ldg_v4_pred(ay[q][t], ap + q * F::SETC + 8, ok);
+      for (int q = 0; q < 4; ++q) {
+        ax[q][t] = ldg_nc_v4(ap + q * ur.qs);
+        if constexpr (BITS == 2) ay[q][t] = ldg_nc_v4(ap + q * ur.qs + 8);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < NTP; ++t) {
+      const __half* ap = ur.ap[t] + kb * F::KBLK;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const bool ok = kb * F::KBLK + q * F::SETC < ur.K;
+        ax[q][t] = make_uint4(0, 0, 0, 0);
+        ldg_v4_pred(ax[q][t], ap + q * ur.qs, ok);
+        if constexpr (BITS == 2) {
+          ay[q][t] = make_uint4(0, 0, 0, 0);
+          ldg_v4_pred(ay[q][t], ap + q * ur.qs + 8, ok);
+        }
       }
     }
   }
@@ -289,7 +323,7 @@ __device__ __forceinline__ void load_acts(const UnitRegs& ur, int kb, uint4 (&ax
 // the group size is not a multiple of the set width pattern (each set then
 // computes its own group index).
 template <int BITS, int RGW, int NTP, int SPANQ, bool FULL>
-__device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0, const uint32_t (&woff)[4], int g,
+__device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0, const uint32_t (&woff)[5], int g,
                                        const uint4 (&ax)[4][NTP], const uint4 (&ay)[4][NTP],
                                        float (&tot)[RGW][NTP][4]) {
   using F = Fmt<BITS>;
@@ -300,6 +334,15 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
   if constexpr (SPANQ == 1) gbase = 4 * kb;
   float acc[RGW][NTP][4];
   float corr[NTP][4];
+  constexpr bool CONTIG = WordMap<BITS, SPANQ>::CONTIG;
+  uint4 wv[CONTIG ? RGW : 1][2];  // contiguous mapping: this lane's 4 words of rows 16r+g and 16r+g+8
+  if constexpr (CONTIG) {
+#pragma unroll
+    for (int r = 0; r < RGW; ++r) {
+      wv[r][0] = lds128(wq0 + woff[4] + (uint32_t)(16 * r) * kStageRowBytes);
+      wv[r][1] = lds128(wq0 + woff[4] + (uint32_t)(16 * r + 8) * kStageRowBytes);
+    }
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (partial && kb * F::KBLK + q * F::SETC >= ur.K) break;
@@ -349,8 +392,13 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
     uint32_t pg[RGW][F::CPW / 2], ph[RGW][F::CPW / 2];
 #pragma unroll
     for (int r = 0; r < RGW; ++r) {
-      unpack_word<BITS>(lds32(wq + (uint32_t)(16 * r) * kStageRowBytes), pg[r]);
-      unpack_word<BITS>(lds32(wq + (uint32_t)(16 * r + 8) * kStageRowBytes), ph[r]);
+      if constexpr (CONTIG) {
+        unpack_word<BITS>(q == 0 ? wv[r][0].x : q == 1 ? wv[r][0].y : q == 2 ? wv[r][0].z : wv[r][0].w, pg[r]);
+        unpack_word<BITS>(q == 0 ? wv[r][1].x : q == 1 ? wv[r][1].y : q == 2 ? wv[r][1].z : wv[r][1].w, ph[r]);
+      } else {
+        unpack_word<BITS>(lds32(wq + (uint32_t)(16 * r) * kStageRowBytes), pg[r]);
+        unpack_word<BITS>(lds32(wq + (uint32_t)(16 * r + 8) * kStageRowBytes), ph[r]);
+      }
     }
     if (span_start) {
 #pragma unroll
@@ -399,7 +447,7 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
 template <int BITS, int RGW, int NTP, int SPANQ, int NT>
 __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const Sched* tab, const UnitRegs& ur,
                                          const UnitRegs& nu, bool has_next, int warp, int lane,
-                                         const uint32_t (&woff)[4], uint32_t ring_base, uint8_t* ring,
+                                         const uint32_t (&woff)[5], uint32_t ring_base, uint8_t* ring,
                                          uint64_t* full, uint64_t pol, Producer& prod, int& consumed, bool& ok,
                                          uint4 (&nx)[4][NT], uint4 (&ny)[4][NT], float (&tot)[RGW][NTP][4]) {
   constexpr int ROWS = 16 * RGW;
@@ -511,10 +559,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   }
   pdl_wait();  // activations (and the residual) may come from the preceding kernel
 
-  // per-lane parts of the swizzled word addresses: row g of set q -> word 4q + c
-  uint32_t woff[4];
+  // per-lane parts of the word addresses: [q] row g of set q -> word 4q + c in a
+  // SWIZZLE_64B tile; [4] row g, words 4c .. 4c+3 in an unswizzled tile
+  uint32_t woff[5];
 #pragma unroll
   for (int q = 0; q < 4; ++q) woff[q] = (uint32_t)(g * kStageRowBytes + (((q ^ (g >> 1)) & 3) << 4) + (c << 2));
+  woff[4] = (uint32_t)(g * kStageRowBytes + (c << 4));
 
   const uint32_t ring_base = smem_u32(ring);
   const uint32_t red_base = smem_u32(red);
@@ -531,11 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     ur.gp = pr.G + 1;
     ur.magic = pr.spg_magic;
     ur.szbase = szb_base + (uint32_t)((s_ & 1) * szpitch) * 4;
+    const bool contig = BITS == 4 && pr.spanq == 4;
+    ur.qs = contig ? F::CPW : F::SETC;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int tok = 8 * t + g;
-      ur.av[t] = tok < pr.M;
-      ur.ap[t] = pr.A + (size_t)(tok < pr.M ? tok : 0) * pr.lda + c * F::CPW;
+      ur.ap[t] = pr.A + (size_t)(tok < pr.M ? tok : 0) * pr.lda + c * (contig ? 4 * F::CPW : F::CPW);
     }
   };
   // activations of this warp's first k-block of the first unit
@@ -741,8 +792,10 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
     units += pr.ntiles;
     gmax = std::max(gmax, pr.G);
     const uint64_t wpr = (uint64_t)g.K / F::CPW;
+    const bool contig = BITS == 4 && pr.spanq == 4;  // see WordMap
     tlq_status st = encode_tiled_2d(&L.wmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT32, g.W, wpr, (uint64_t)g.N, wpr * 4,
-                                    kWordsPerKBlock, ROWS, CU_TENSOR_MAP_SWIZZLE_64B,
+                                    kWordsPerKBlock, ROWS,
+                                    contig ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (st != TLQ_OK) return st;
   }
