@@ -79,6 +79,7 @@ struct DecodeProblem {
   int nkb;              // k-blocks
   int unit_begin;       // first global unit index
   uint64_t spg_magic;   // set index -> group index: (si * magic) >> 40
+  int szvec;            // scale/zero rows copied in 16-byte pieces (K/group % 8 == 0, 16-byte aligned arrays)
   int spanq;            // sets per accumulation span inside a k-block (4, 2, 1) or 0 (generic)
 };
 
@@ -93,7 +94,9 @@ struct DecodeLaunch {
   DecodeProblem prob[kMaxProblems];
   int count;
   int total_units;
-  int gmax;    // largest K/group, row pitch bound of the scale/zero buffers
+  int gmax;    // largest K/group
+  int gpitch;  // row pitch of the scale/zero tiles in halves: gmax rounded up to 8, plus 8
+  int nsz;     // scale/zero buffers (3 or 2, by shared memory)
   int listed;  // 1: CTA b runs units[cta_off[b] .. cta_off[b+1]); 0: snake order
   uint16_t cta_off[kMaxListGrid + 1];
   uint16_t units[kMaxListUnits];
@@ -189,70 +192,71 @@ struct Producer {
   }
 };
 
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Scales/zeros of one unit as {s, z} half2 pairs, row pitch G + 1 (odd: the
-// per-row reads of a warp hit distinct banks).  With TPR = kThreads / ROWS
-// threads per row, thread t owns row t / TPR and groups t % TPR + TPR * j
-// (coalesced runs per row, no division).
-constexpr int kSzPerThread = 16;  // groups per thread held in registers by the one-unit-ahead prefetch
+// Scales and zeros of one unit in shared memory: an S tile [ROWS][gp] then a
+// Z tile [ROWS][gp] of halves, gp = (K/group rounded up to 8) + 8, so rows
+// are 16-byte aligned and the eight rows a warp reads at once fall in
+// different banks.  Rows with K/group a multiple of 8 (and 16-byte aligned
+// scale/zero arrays) are copied with cp.async 16-byte copies that need no
+// registers and complete in the background; other shapes copy element by
+// element.  Every thread commits one copy group per call, so the counts the
+// waits rely on are uniform.  Rows past N copy row N - 1 (never used).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-template <int ROWS>
-__device__ __forceinline__ void load_unit_sz(const DecodeProblem& pr, int n0, int tid, uint32_t (&v)[kSzPerThread]) {
-  constexpr int TPR = kThreads / ROWS;
-  const int row = tid / TPR;
-  const int g0 = tid % TPR;
-  if (n0 + row >= pr.N) return;
-  const int G = pr.G;
-  const size_t o = (size_t)(n0 + row) * G + g0;
-  const __half* S = pr.S + o;
-  const __half* Z = pr.Z + o;
-#pragma unroll
-  for (int j = 0; j < kSzPerThread; ++j) {
-    if (TPR * j >= G) break;
-    if (g0 + TPR * j < G) {
-      const uint32_t sv = __half_as_ushort(__ldg(S + TPR * j));
-      const uint32_t zv = __half_as_ushort(__ldg(Z + TPR * j));
-      v[j] = sv | (zv << 16);
-    }
-  }
+__device__ __forceinline__ void sts16(uint32_t addr, unsigned short v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ float lds_half(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return __half2float(__ushort_as_half(v));
 }
 
 template <int ROWS>
-__device__ __forceinline__ void store_unit_sz(const DecodeProblem& pr, int n0, int tid,
-                                              const uint32_t (&v)[kSzPerThread], uint32_t dst) {
-  constexpr int TPR = kThreads / ROWS;
-  const int row = tid / TPR;
-  const int g0 = tid % TPR;
-  if (n0 + row >= pr.N) return;
+__device__ __forceinline__ void stage_unit_sz(const DecodeProblem& pr, int n0, int tid, uint32_t dst, int gp) {
   const int G = pr.G;
-  const uint32_t d = dst + (uint32_t)(row * (G + 1) + g0) * 4;
-#pragma unroll
-  for (int j = 0; j < kSzPerThread; ++j) {
-    if (TPR * j >= G) break;
-    if (g0 + TPR * j < G) sts32(d + 4 * TPR * j, v[j]);
+  if (pr.szvec) {
+    const int cpr = G >> 3;  // 16-byte chunks per row
+    const int per = ROWS * cpr;
+    for (int i = tid; i < 2 * per; i += kThreads) {
+      const int arr = i >= per;  // 0: S, 1: Z
+      const int j = i - arr * per;
+      const int row = j / cpr, ch = j - row * cpr;
+      const int n = min(n0 + row, pr.N - 1);
+      cp_async16(dst + (uint32_t)((arr * ROWS + row) * gp + ch * 8) * 2, (arr ? pr.Z : pr.S) + (size_t)n * G + ch * 8);
+    }
+  } else {
+    const int per = ROWS * G;
+    for (int i = tid; i < 2 * per; i += kThreads) {
+      const int arr = i >= per;
+      const int j = i - arr * per;
+      const int row = j / G, gg = j - row * G;
+      const int n = min(n0 + row, pr.N - 1);
+      const __half* src = (arr ? pr.Z : pr.S) + (size_t)n * G + gg;
+      sts16(dst + (uint32_t)((arr * ROWS + row) * gp + gg) * 2, __half_as_ushort(__ldg(src)));
+    }
   }
-  if (G > TPR * kSzPerThread) {  // more groups than the register prefetch covers: load the rest here
-    const size_t o = (size_t)(n0 + row) * G;
-    for (int gg = g0 + TPR * kSzPerThread; gg < G; gg += TPR)
-      sts32(dst + (uint32_t)(row * (G + 1) + gg) * 4,
-            (uint32_t)__half_as_ushort(__ldg(pr.S + o + gg)) | ((uint32_t)__half_as_ushort(__ldg(pr.Z + o + gg)) << 16));
-  }
+  cp_async_commit();
 }
 
 // Per-unit values of the current problem, held in registers.
 struct UnitRegs {
   const __half* ap[2];  // this lane's activation row (token 8t + g, clamped to token 0 past M) + word offset
   int qs;               // codes between this lane's words of consecutive sets
-  int K, nkb, nkb_full, gp;
+  int K, nkb, nkb_full, gp;  // gp: row pitch of the scale/zero tiles (halves)
   uint64_t magic;
-  uint32_t szbase;
+  uint32_t szbase;           // S tile of this unit; the Z tile follows at + ROWS * gp halves
 };
 
 // INT4 with whole-k-block groups uses the contiguous word mapping: lane c of
@@ -420,13 +424,15 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
       int gi;
       if constexpr (SPANQ == 0) gi = (int)(((uint64_t)(kb * 4 + q) * ur.magic) >> 40);
       else gi = gbase + q / SQ;
-      const uint32_t sza = ur.szbase + (uint32_t)((g * ur.gp + gi) * 4);
+      const uint32_t sa = ur.szbase + (uint32_t)((g * ur.gp + gi) * 2);
+      const uint32_t za = sa + (uint32_t)(16 * RGW * ur.gp * 2);
 #pragma unroll
       for (int r = 0; r < RGW; ++r) {
-        const uint32_t szg = lds32(sza + (uint32_t)(16 * r * ur.gp) * 4);
-        const uint32_t szh = lds32(sza + (uint32_t)((16 * r + 8) * ur.gp) * 4);
-        const float2 fg = __half22float2(*reinterpret_cast<const __half2*>(&szg));
-        const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&szh));
+        // (x, y) = (s, z) of rows 16r + g and 16r + g + 8
+        const float2 fg = make_float2(lds_half(sa + (uint32_t)(16 * r * ur.gp) * 2),
+                                      lds_half(za + (uint32_t)(16 * r * ur.gp) * 2));
+        const float2 fh = make_float2(lds_half(sa + (uint32_t)((16 * r + 8) * ur.gp) * 2),
+                                      lds_half(za + (uint32_t)((16 * r + 8) * ur.gp) * 2));
 #pragma unroll
         for (int t = 0; t < NTP; ++t) {
           // acc + corr0 + z * corr2 = sum a (q - z); then * s
@@ -498,9 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;  // [warp][kSPW][STAGE_BYTES]
-  const int szpitch = ROWS * (L.gmax + 1);  // uint32 {s,z} pairs per buffer
-  uint32_t* szb = reinterpret_cast<uint32_t*>(ring + kWarps * kSPW * STAGE_BYTES);  // [par][ROWS][G+1]
-  float* red = reinterpret_cast<float*>(szb + 2 * szpitch);                         // [par][warp][MT][RP]
+  const int gp = L.gpitch;
+  const int szbytes = 4 * ROWS * gp;  // one unit's S and Z tiles
+  const int nsz = L.nsz;              // scale/zero buffers: 3 (staged two units ahead) or 2 (one ahead)
+  uint8_t* szb = ring + kWarps * kSPW * STAGE_BYTES;                          // [nsz][S, Z][ROWS][gp]
+  float* red = reinterpret_cast<float*>(szb + nsz * szbytes);                 // [par][warp][MT][RP]
   uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kWarps * MT * RP);         // [warp][kSPW]
   Sched* tab = reinterpret_cast<Sched*>(full + kWarps * kSPW);                      // [kMaxRounds]
 
@@ -550,13 +558,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     for (int i = 0; i < kSPW; ++i) prod.template issue<ROWS>(L, tab, ring, full, pol);
   }
   const uint32_t szb_base = smem_u32(szb);
-  // scales/zeros of the first unit (weights-side data: before the dependency wait)
-  if (nrounds > 0) {
-    uint32_t v[kSzPerThread];
-    const DecodeProblem& pr0 = L.prob[tab[0].p];
-    load_unit_sz<ROWS>(pr0, tab[0].n0, tid, v);
-    store_unit_sz<ROWS>(pr0, tab[0].n0, tid, v, szb_base);
+  // scales/zeros of the first nsz - 1 units (weights-side data: before the dependency wait)
+  for (int i = 0; i < nsz - 1; ++i) {
+    if (i < nrounds) stage_unit_sz<ROWS>(L.prob[tab[i].p], tab[i].n0, tid, szb_base + (uint32_t)(i * szbytes), gp);
+    else cp_async_commit();
   }
+  if (nsz == 3) cp_async_wait<1>();  // unit 0's copies (unit 1's may still be in flight)
+  else cp_async_wait<0>();
   pdl_wait();  // activations (and the residual) may come from the preceding kernel
 
   // per-lane parts of the word addresses: [q] row g of set q -> word 4q + c in a
@@ -578,9 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     ur.K = pr.K;
     ur.nkb = e.nkb;
     ur.nkb_full = pr.K / F::KBLK;
-    ur.gp = pr.G + 1;
+    ur.gp = gp;
     ur.magic = pr.spg_magic;
-    ur.szbase = szb_base + (uint32_t)((s_ & 1) * szpitch) * 4;
+    ur.szbase = szb_base + (uint32_t)((s_ % nsz) * szbytes);
     const bool contig = BITS == 4 && pr.spanq == 4;
     ur.qs = contig ? F::CPW : F::SETC;
 #pragma unroll
@@ -604,12 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int n0 = e.n0;
     const int M = pr.M;
     const bool has_next = s + 1 < nrounds;
-    // next unit's scales/zeros: into registers now, into shared memory at this unit's barrier
-    uint32_t szn[kSzPerThread];
-    if (has_next) {
-      load_unit_sz<ROWS>(L.prob[tab[s + 1].p], tab[s + 1].n0, tid, szn);
-      make_regs(s + 1, nu);
+    // scales/zeros of unit s + nsz - 1 into the buffer unit s - 1 used (every
+    // thread passed that unit's barrier, so no one reads it any more)
+    {
+      const int su = s + nsz - 1;
+      if (su < nrounds)
+        stage_unit_sz<ROWS>(L.prob[tab[su].p], tab[su].n0, tid, szb_base + (uint32_t)((su % nsz) * szbytes), gp);
+      else
+        cp_async_commit();
     }
+    if (has_next) make_regs(s + 1, nu);
     const int spanq = pr.spanq;
 
     float tot[RGW][NT][4];
@@ -656,9 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           sts_f32(myred + (uint32_t)((tk + 1) * RP + ra + 8) * 4, tot[r][t][3]);
         }
     }
-    // publish the next unit's scales/zeros into the other buffer
-    if (s + 1 < nrounds)
-      store_unit_sz<ROWS>(L.prob[tab[s + 1].p], tab[s + 1].n0, tid, szn, szb_base + (uint32_t)((par ^ 1) * szpitch) * 4);
+    // the next unit's scales/zeros have landed (only unit s + 2's group may
+    // still be in flight); the barrier publishes them to every thread
+    if (nsz == 3) cp_async_wait<1>();
+    else cp_async_wait<0>();
     named_barrier(1, kThreads);
     {
       const float* rb = red + (size_t)par * kWarps * MT * RP;
@@ -684,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (has_next) ur = nu;
   }
 
+  cp_async_wait<0>();  // (only empty groups can remain here)
   // error path only: copies still in flight land before the CTA exits
   if (!ok && lane == 0) {
     for (int j = consumed; j < prod.issued; ++j)
@@ -780,6 +794,7 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
     pr.N = g.N;
     pr.K = g.K;
     pr.G = g.K / g.group;
+    pr.szvec = (pr.G % 8 == 0) && ((reinterpret_cast<uintptr_t>(g.S) | reinterpret_cast<uintptr_t>(g.Z)) % 16 == 0);
     pr.epi = g.epi;
     pr.ntiles = (g.N + ROWS - 1) / ROWS;
     pr.nkb = (g.K + F::KBLK - 1) / F::KBLK;
@@ -803,8 +818,12 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   L.total_units = units;
   L.gmax = gmax;
 
-  const size_t smem = 1024 + (size_t)kWarps * kSPW * ROWS * kStageRowBytes + (size_t)2 * ROWS * (gmax + 1) * 4 +
-                      (size_t)2 * kWarps * MT * (ROWS + 4) * 4 + kWarps * kSPW * 8 + (size_t)kMaxRounds * sizeof(Sched);
+  L.gpitch = (gmax + 7) / 8 * 8 + 8;
+  const size_t fixed = 1024 + (size_t)kWarps * kSPW * ROWS * kStageRowBytes +
+                       (size_t)2 * kWarps * MT * (ROWS + 4) * 4 + kWarps * kSPW * 8 + (size_t)kMaxRounds * sizeof(Sched);
+  const size_t szbuf = (size_t)4 * ROWS * L.gpitch;
+  L.nsz = fixed + 3 * szbuf <= (size_t)device_info().smem_optin ? 3 : 2;
+  const size_t smem = fixed + (size_t)L.nsz * szbuf;
   if (smem > (size_t)device_info().smem_optin)
     return set_error(TLQ_EUNSUPPORTED, "decode: K/group = %d needs %zu bytes of shared memory (limit %d)", gmax,
                      smem, device_info().smem_optin);
