@@ -121,6 +121,15 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the library arm
 # ---------------------------------------------------------------------------
+def batched_launches(Ms, nshapes):
+    """Kernel launches of one tl_quant_gemm_batched call over len(Ms) x nshapes
+    problems of one bit width: M <= 16 problems go in chunks of 16, one decode
+    launch per chunk; every M > 16 problem is one prefill launch."""
+    ms = [M for M in Ms for _ in range(nshapes)]
+    ndec = sum(1 for M in ms if M <= 16)
+    return (ndec + 15) // 16 + sum(1 for M in ms if M > 16)
+
+
 class Workload:
     """Packed weights (rotated copies), activations and outputs on the GPU."""
 
@@ -147,6 +156,7 @@ class Workload:
         self.step_bytes = sum(gemm_bytes(M, N, K, bits, self.group) for M in Ms for (N, K) in shapes.values())
         self.step_flops = sum(2 * M * N * K for M in Ms for (N, K) in shapes.values())
         self.launches = len(Ms) * len(shapes)
+        self.batched_launches = batched_launches(Ms, len(shapes))
         self.weight_set_bytes = sum(N * K * bits // 8 + 4 * N * K // self.group for (N, K) in shapes.values())
 
     def descs(self, i):
@@ -240,7 +250,7 @@ def kernel_hash():
 # dram bytes (read + write) per launch of the decode kernel for the headline
 # step, from the ncu capture summarised in profiles/ (None until captured for
 # the current kernel source).
-NCU_TRAFFIC = {"kernel_hash": "32975138245c6b89", "bytes_per_launch": 82885632}  # profiles/decode_kernel_int4_decode_step.md
+NCU_TRAFFIC = {"kernel_hash": None, "bytes_per_step": None}  # profiles/decode_kernel_int4_decode_step.md
 
 
 def run_tlq(args, rank, world, dist):
@@ -326,9 +336,11 @@ def run_tlq(args, rank, world, dist):
 
     torch.cuda.synchronize()
     traffic = None
-    if NCU_TRAFFIC["kernel_hash"] == kernel_hash() and NCU_TRAFFIC["bytes_per_launch"]:
-        traffic = NCU_TRAFFIC["bytes_per_launch"]
-    achieved = wl4.step_bytes / (ms_step * 1e-3) / 1e9  # one decode launch per step
+    if NCU_TRAFFIC["kernel_hash"] == kernel_hash() and NCU_TRAFFIC["bytes_per_step"]:
+        traffic = NCU_TRAFFIC["bytes_per_step"]
+    # the step is the decode kernel's launch(es): algorithmic bytes of the step /
+    # their summed duration
+    achieved = wl4.step_bytes / (ms_step * 1e-3) / 1e9
     line = {
         "metric": "quant_gemm GB/s (decode) & TFLOP/s (prefill), % of GB300 roofline",
         "value": round(value, 1),
@@ -348,18 +360,19 @@ def run_tlq(args, rank, world, dist):
             "bytes_per_step": wl4.step_bytes,
             "l2": "weights/scales/zeros rotated over %d copies (%.0f MB > L2 %.0f MB)" % (
                 ncopy, ncopy * wl4.weight_set_bytes / 1e6, l2 / 1e6),
-            "launch": "one tl_quant_gemm_batched call per step (one persistent decode launch for the 12 "
-                      "problems), replayed from a CUDA graph",
+            "launch": "one tl_quant_gemm_batched call per step (%d persistent decode launch for the 12 "
+                      "problems), replayed from a CUDA graph" % wl4.batched_launches,
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm"], 3), "traffic": traffic,
-                     "peak_source": peaks["src"], "kernel": "decode_kernel (one launch per step)"},
+                     "peak_source": peaks["src"],
+                     "kernel": "decode_kernel (%d launches per step; traffic per step)" % wl4.batched_launches},
         "per_gemm": per_gemm,
         "separate_launches": separate,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * wl4.batched_launches,
     }
     line.update(result)
     if rank == 0 and world == 1:

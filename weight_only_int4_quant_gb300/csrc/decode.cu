@@ -677,20 +677,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const float* rb = red + (size_t)par * kWarps * MT * RP;
       const int rows = min(ROWS, pr.N - n0);
       const int epi = pr.epi;
-      for (int i = tid; i < ROWS * M; i += kThreads) {
-        const int row = i % ROWS, tk = i / ROWS;
+      // items of four consecutive rows of one token: eight 16-byte partial
+      // loads, one 8-byte store (rows is a multiple of 8, ldc of 4)
+      for (int i = tid; i < (ROWS / 4) * M; i += kThreads) {
+        const int tk = i / (ROWS / 4), row = 4 * (i % (ROWS / 4));
         if (row >= rows) continue;
-        float v = 0.f;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += rb[(w * MT + tk) * RP + row];
+        for (int w = 0; w < kWarps; ++w) {
+          const float4 x = *reinterpret_cast<const float4*>(rb + (w * MT + tk) * RP + row);
+          v.x += x.x;
+          v.y += x.y;
+          v.z += x.z;
+          v.w += x.w;
+        }
         const int n = n0 + row;
-        __half h = __float2half_rn(v);
-        if (epi == kEpiRelu) h = relu_half(h);
+        __half h[4] = {__float2half_rn(v.x), __float2half_rn(v.y), __float2half_rn(v.z), __float2half_rn(v.w)};
         if (epi == kEpiResidual) {
           float* xp = pr.X + (size_t)tk * pr.ldx + n;
-          *xp = *xp + __half2float(h);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) xp[j] = xp[j] + __half2float(h[j]);
         } else {
-          pr.C[(size_t)tk * pr.ldc + n] = h;
+          if (epi == kEpiRelu) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[j] = relu_half(h[j]);
+          }
+          uint2 o;
+          o.x = (uint32_t)__half_as_ushort(h[0]) | ((uint32_t)__half_as_ushort(h[1]) << 16);
+          o.y = (uint32_t)__half_as_ushort(h[2]) | ((uint32_t)__half_as_ushort(h[3]) << 16);
+          *reinterpret_cast<uint2*>(pr.C + (size_t)tk * pr.ldc + n) = o;
         }
       }
     }
@@ -857,6 +872,10 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   return TLQ_OK;
 }
 
+// One launch per call: the two-token-tile kernel when any problem has M > 8
+// (its problems with M <= 8 take the one-tile path inside it).  Splitting the
+// call into a one-tile and a two-tile launch was measured slower for the INT4
+// decode step: the second launch costs more than the leaner kernel saves.
 template <int BITS>
 tlq_status dispatch_bits(const GemmArgs* a, int count, cudaStream_t s) {
   bool two = false;
