@@ -190,29 +190,75 @@ class Workload:
                 self.tlq.tl_quant_gemm(self.A[M, name], W, s, z, self.C[M, name], self.bits, self.group, stream)
 
 
+class StepGraphs:
+    """CUDA graphs replaying consecutive steps of a workload: a chunk graph of
+    `chunk` steps (a multiple of the rotation phases, so a chunk starts at phase
+    0 and ends at the last phase) and short graphs for the remainders, so any
+    step count is replayed exactly and the weight rotation stays continuous.
+    Several steps per graph keep the per-graph launch gap out of the step time
+    (one graph per step added several microseconds to every decode step)."""
+
+    def __init__(self, torch, run, phases, min_chunk=16):
+        self.torch, self.run, self.phases = torch, run, phases
+        self.chunk = phases * max(1, -(-min_chunk // phases))
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for p in range(phases):  # warm the launch path outside capture
+                run(p)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.main = self._capture(self.chunk, 0)
+        self.rest = {}
+
+    def _capture(self, n, start):
+        g = self.torch.cuda.CUDAGraph()
+        with self.torch.cuda.graph(g):
+            for i in range(n):
+                self.run((start + i) % self.phases)
+        self.torch.cuda.synchronize()
+        return g
+
+    def _tail(self, r, start):
+        if (r, start) not in self.rest:
+            self.rest[r, start] = self._capture(r, start)
+        return self.rest[r, start]
+
+    def prepare(self, warmup, steps):
+        """Capture the remainder graphs both counts need (before any timing)."""
+        rw = warmup % self.chunk
+        if rw:
+            self._tail(rw, (-rw) % self.phases)
+        if steps % self.chunk:
+            self._tail(steps % self.chunk, 0)
+
+    def warm(self, n):
+        """n steps ending at the last phase, so the next step starts the rotation."""
+        r = n % self.chunk
+        if r:
+            self._tail(r, (-r) % self.phases).replay()
+        for _ in range(n // self.chunk):
+            self.main.replay()
+
+    def replay(self, n):
+        """n steps starting at phase 0."""
+        for _ in range(n // self.chunk):
+            self.main.replay()
+        if n % self.chunk:
+            self._tail(n % self.chunk, 0).replay()
+
+
 def capture_steps(torch, wl, phases, separately=False):
-    """One CUDA graph per rotation phase; step i replays graph i % phases."""
-    run = wl.run_step_separately if separately else wl.run_step
-    graphs = []
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for p in range(phases):  # warm the launch path outside capture
-            run(p)
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    for p in range(phases):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            run(p)
-        graphs.append(g)
-    torch.cuda.synchronize()
-    return graphs
+    """Step graphs of a workload (every problem of a step in one batched call, or
+    one tl_quant_gemm call per problem)."""
+    return StepGraphs(torch, wl.run_step_separately if separately else wl.run_step, phases)
 
 
-def time_graphs(torch, graphs, steps, warmup, dist=None):
-    for i in range(warmup):
-        graphs[i % len(graphs)].replay()
+def time_graphs(torch, sg, steps, warmup, dist=None):
+    """Exactly `warmup` untimed steps, then exactly `steps` timed steps between
+    CUDA events on the current stream (barrier + synchronize on both sides)."""
+    sg.prepare(warmup, steps)
+    sg.warm(warmup)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -220,13 +266,27 @@ def time_graphs(torch, graphs, steps, warmup, dist=None):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(steps):
-        graphs[i % len(graphs)].replay()
+    sg.replay(steps)
     e1.record()
     e1.synchronize()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    return e0.elapsed_time(e1)
+
+
+def time_graph_list(torch, graphs, reps, warmup):
+    """Replays of already captured graphs (the per-GEMM breakdown)."""
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        graphs[i % len(graphs)].replay()
+    e1.record()
+    e1.synchronize()
     return e0.elapsed_time(e1)
 
 
@@ -308,7 +368,7 @@ def run_tlq(args, rank, world, dist):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 run24()
-            t = time_graphs(torch, [g], 20, 3)
+            t = time_graph_list(torch, [g], 20, 3)
             us = t * 1e3 / (20 * 24)
             per_gemm["M%d_%s" % (M, name)] = {"us": round(us, 2), "GBps": round(b / (us * 1e-6) / 1e9, 1)}
             del g
@@ -361,13 +421,13 @@ def run_tlq(args, rank, world, dist):
             "l2": "weights/scales/zeros rotated over %d copies (%.0f MB > L2 %.0f MB)" % (
                 ncopy, ncopy * wl4.weight_set_bytes / 1e6, l2 / 1e6),
             "launch": "one tl_quant_gemm_batched call per step (%d persistent decode launch for the 12 "
-                      "problems), replayed from a CUDA graph" % wl4.batched_launches,
+                      "problems); CUDA graphs of %d consecutive steps" % (wl4.batched_launches, graphs.chunk),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm"], 3), "traffic": traffic,
                      "peak_source": peaks["src"],
-                     "kernel": "decode_kernel (%d launches per step; traffic per step)" % wl4.batched_launches},
+                     "kernel": "decode_kernel (%d launch(es) per step; traffic per step)" % wl4.batched_launches},
         "per_gemm": per_gemm,
         "separate_launches": separate,
         "clocks": clocks,
