@@ -724,10 +724,11 @@ uint64_t magic_div40(int d) { return (((uint64_t)1) << 40) / (uint64_t)d + 1; }
 
 // Longest-processing-time-first assignment of the launch's units to `grid`
 // CTAs: units in decreasing cost order, each to the CTA with the smallest
-// load so far (ties: lowest index).  A unit's cost is its k-block count
-// weighted by the token tiles it computes (two tiles cost about 1.7x one,
-// measured).  Returns false when some CTA would hold more than kMaxRounds
-// units.
+// load so far (ties: lowest index).  A unit's cost is its k-block count plus
+// 8 for the unit's fixed work (barrier, reduction, epilogue: about as long
+// as 8 k-blocks, measured), weighted by the token tiles it computes (two
+// tiles cost about 1.7x one, measured).  Returns false when some CTA would
+// hold more than kMaxRounds units.
 bool build_unit_lists(DecodeLaunch& L, int grid) {
   const int units = L.total_units;
   if (units > kMaxListUnits || grid > kMaxListGrid) return false;
@@ -735,7 +736,7 @@ bool build_unit_lists(DecodeLaunch& L, int grid) {
   uint32_t cost[kMaxProblems];
   for (int j = 0; j < L.count; ++j) {
     pord[j] = j;
-    cost[j] = (uint32_t)L.prob[j].nkb * (L.prob[j].M > 8 ? 17u : 10u);
+    cost[j] = (uint32_t)(L.prob[j].nkb + 8) * (L.prob[j].M > 8 ? 17u : 10u);
   }
   std::stable_sort(pord, pord + L.count, [&](int x, int y) { return cost[x] > cost[y]; });
   // binary min-heap of (load, cta)
