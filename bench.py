@@ -146,12 +146,25 @@ class Workload:
             W = tlq.pack_weights(torch.from_numpy(codes).cuda(), bits)
             base[name] = (W, torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda())
         self.copies = [base] + [{k: tuple(t.clone() for t in v) for k, v in base.items()} for _ in range(copies - 1)]
+        # activations and outputs are views into one flat device buffer each (every
+        # segment a multiple of 8 halves, so every view is 16-byte aligned): a step's
+        # inputs and results move in one host<->device copy each
+        keys = [(M, name) for M in Ms for name in shapes]
+        na = sum(M * shapes[name][1] for M, name in keys)
+        nc = sum(M * shapes[name][0] for M, name in keys)
+        self.A_flat = torch.empty(na, dtype=torch.float16, device="cuda")
+        self.C_flat = torch.empty(nc, dtype=torch.float16, device="cuda")
         self.A = {}
         self.C = {}
-        for M in Ms:
-            for name, (N, K) in shapes.items():
-                self.A[M, name] = torch.from_numpy(synth.activations(rng, M, K, a_scale)).cuda()
-                self.C[M, name] = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        oa = oc = 0
+        for M, name in keys:
+            N, K = shapes[name]
+            a = self.A_flat[oa:oa + M * K].view(M, K)
+            a.copy_(torch.from_numpy(synth.activations(rng, M, K, a_scale)))
+            self.A[M, name] = a
+            self.C[M, name] = self.C_flat[oc:oc + M * N].view(M, N)
+            oa += M * K
+            oc += M * N
         torch.cuda.synchronize()
         self.step_bytes = sum(gemm_bytes(M, N, K, bits, self.group) for M in Ms for (N, K) in shapes.values())
         self.step_flops = sum(2 * M * N * K for M in Ms for (N, K) in shapes.values())
@@ -441,19 +454,18 @@ def run_tlq(args, rank, world, dist):
 
 
 def run_e2e(tlq, torch, wl, steps):
-    """Per step: pinned host -> device copy of every activation, the 12 C-ABI
-    calls, device -> pinned host copy of every output."""
-    hostA = {k: v.cpu().pin_memory() for k, v in wl.A.items()}
-    hostC = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in wl.C.items()}
-    h2d = sum(v.numel() * 2 for v in hostA.values())
-    d2h = sum(v.numel() * 2 for v in hostC.values())
+    """Per step: one pinned host -> device copy of the step's activations (all
+    12 problems, one flat buffer), the batched C-ABI call, one device -> pinned
+    host copy of all outputs."""
+    hostA = wl.A_flat.cpu().pin_memory()
+    hostC = torch.empty(wl.C_flat.shape, dtype=wl.C_flat.dtype).pin_memory()
+    h2d = hostA.numel() * 2
+    d2h = hostC.numel() * 2
 
     def one(i):
-        for k, v in hostA.items():
-            wl.A[k].copy_(v, non_blocking=True)
+        wl.A_flat.copy_(hostA, non_blocking=True)
         wl.run_step(i)
-        for k, v in hostC.items():
-            v.copy_(wl.C[k], non_blocking=True)
+        hostC.copy_(wl.C_flat, non_blocking=True)
 
     for i in range(5):
         one(i)
