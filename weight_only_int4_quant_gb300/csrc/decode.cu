@@ -84,9 +84,11 @@ struct DecodeProblem {
 };
 
 // Per-CTA unit lists built on the host (longest-first greedy on estimated
-// unit cost), for launches of up to kMaxListUnits units on up to kMaxListGrid
-// CTAs; larger launches deal units in snake order on the device instead.
-constexpr int kMaxListUnits = 2048;
+// unit cost), up to kMaxPerCta units on each of up to kMaxListGrid CTAs, in
+// fixed per-CTA slots so a CTA reads its whole list in parallel at start-up
+// (no dependent parameter reads); larger launches deal units in snake order
+// on the device instead.
+constexpr int kMaxPerCta = 16;
 constexpr int kMaxListGrid = 256;
 
 struct DecodeLaunch {
@@ -97,9 +99,9 @@ struct DecodeLaunch {
   int gmax;    // largest K/group
   int gpitch;  // row pitch of the scale/zero tiles in halves: gmax rounded up to 8, plus 8
   int nsz;     // scale/zero buffers (3 or 2, by shared memory)
-  int listed;  // 1: CTA b runs units[cta_off[b] .. cta_off[b+1]); 0: snake order
-  uint16_t cta_off[kMaxListGrid + 1];
-  uint16_t units[kMaxListUnits];
+  int listed;  // 1: CTA b runs cta_units[b][0 .. cta_count[b]) (problem | row tile << 4); 0: snake order
+  uint8_t cta_count[kMaxListGrid];
+  uint16_t cta_units[kMaxListGrid][kMaxPerCta];
 };
 
 // FP16 pairs (base + q) of one word: pairs[i] holds positions (i, i + CPW/2).
@@ -520,43 +522,54 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int P = gridDim.x;
   const int b = blockIdx.x;
 
+  // the launch's tensor maps first: their descriptors are fetched while the rest starts
+  if (warp == 0 && lane < L.count) tma_prefetch_desc(&L.wmap[lane]);
   if (tid == 0) {
     for (int i = 0; i < kWarps * kSPW; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
   }
-  // this CTA's units: round r = tid
-  int nrounds;
-  {
-    const int r = tid;
-    int u = -1;
-    if (L.listed) {
-      const int off = L.cta_off[b];
-      if (r < L.cta_off[b + 1] - off) u = L.units[off + r];
-    } else {
-      const int su = r * P + ((r & 1) ? (P - 1 - b) : b);
-      if (r < kMaxRounds && su < L.total_units) u = su;
+  // this CTA's units.  Every thread walks the same rounds, so each parameter
+  // read is a broadcast (per-thread rounds would make 256 divergent,
+  // serialized constant-bank reads); one thread stores the table.
+  int nrounds = 0;
+  if (L.listed) {
+    nrounds = L.cta_count[b];
+    if (tid < kMaxPerCta) {
+      const uint32_t w = L.cta_units[b][tid];  // problem | row tile << 4 (all entries read at once)
+      if (tid < nrounds) {
+        Sched e;
+        e.p = (int)(w & 15u);
+        e.n0 = (int)(w >> 4) * ROWS;
+        e.nkb = L.prob[e.p].nkb;
+        e.pad = 0;
+        tab[tid] = e;
+      }
     }
-    const bool valid = u >= 0;
-    if (valid) {
-      const int p = problem_of(L, u);
-      Sched e;
-      e.p = p;
-      e.n0 = (u - L.prob[p].unit_begin) * ROWS;
-      e.nkb = L.prob[p].nkb;
-      e.pad = 0;
-      tab[r] = e;
+  } else {
+#pragma unroll 1
+    for (int r = 0; r < kMaxRounds; ++r) {
+      const int u = r * P + ((r & 1) ? (P - 1 - b) : b);
+      if (u >= L.total_units) break;
+      if (tid == 0) {
+        const int p = problem_of(L, u);
+        Sched e;
+        e.p = p;
+        e.n0 = (u - L.prob[p].unit_begin) * ROWS;
+        e.nkb = L.prob[p].nkb;
+        e.pad = 0;
+        tab[r] = e;
+      }
+      nrounds = r + 1;
     }
-    nrounds = __syncthreads_count(valid);  // also publishes the barrier inits and the table
   }
+  __syncthreads();  // barrier inits and the table are visible
   if (tid == 0) pdl_launch_dependents();
 
   const uint64_t pol = policy_evict_first();
   Producer prod;
   prod.init(tab, warp, nrounds);
-  if (lane == 0) {
-    tma_prefetch_desc(&L.wmap[0]);
+  if (lane == 0)
     for (int i = 0; i < kSPW; ++i) prod.template issue<ROWS>(L, tab, ring, full, pol);
-  }
   const uint32_t szb_base = smem_u32(szb);
   // scales/zeros of the first nsz - 1 units (weights-side data: before the dependency wait)
   for (int i = 0; i < nsz - 1; ++i) {
@@ -731,7 +744,9 @@ uint64_t magic_div40(int d) { return (((uint64_t)1) << 40) / (uint64_t)d + 1; }
 // hold more than kMaxRounds units.
 bool build_unit_lists(DecodeLaunch& L, int grid) {
   const int units = L.total_units;
-  if (units > kMaxListUnits || grid > kMaxListGrid) return false;
+  if (grid > kMaxListGrid || units > grid * kMaxPerCta) return false;
+  for (int j = 0; j < L.count; ++j)
+    if (L.prob[j].ntiles > 4096) return false;  // an entry holds the row tile in 12 bits
   int pord[kMaxProblems];
   uint32_t cost[kMaxProblems];
   for (int j = 0; j < L.count; ++j) {
@@ -742,23 +757,28 @@ bool build_unit_lists(DecodeLaunch& L, int grid) {
   // binary min-heap of (load, cta)
   uint64_t heap[kMaxListGrid];
   for (int i = 0; i < grid; ++i) heap[i] = (uint64_t)i;  // load 0: already a heap
-  uint16_t cta_of[kMaxListUnits];
-  uint16_t count_of[kMaxListGrid] = {};
+  uint8_t count_of[kMaxListGrid] = {};
   for (int j = 0; j < L.count; ++j) {
     const DecodeProblem& pr = L.prob[pord[j]];
     for (int t = 0; t < pr.ntiles; ++t) {
       const uint64_t top = heap[0];
       const int c = (int)(top & 0xFFFFu);
-      if (++count_of[c] > kMaxRounds) return false;
-      cta_of[pr.unit_begin + t] = (uint16_t)c;
+      if (count_of[c] >= kMaxPerCta) return false;
+      L.cta_units[c][count_of[c]++] = (uint16_t)(pord[j] | (t << 4));  // costliest units first
       uint64_t v = top + ((uint64_t)cost[pord[j]] << 16);
       int i = 0;  // sift down
       for (;;) {
         const int l = 2 * i + 1, r = l + 1;
         int m = i;
         uint64_t mv = v;
-        if (l < grid && heap[l] < mv) { m = l; mv = heap[l]; }
-        if (r < grid && heap[r] < mv) { m = r; mv = heap[r]; }
+        if (l < grid && heap[l] < mv) {
+          m = l;
+          mv = heap[l];
+        }
+        if (r < grid && heap[r] < mv) {
+          m = r;
+          mv = heap[r];
+        }
         if (m == i) break;
         heap[i] = heap[m];
         i = m;
@@ -766,18 +786,7 @@ bool build_unit_lists(DecodeLaunch& L, int grid) {
       heap[i] = v;
     }
   }
-  L.cta_off[0] = 0;
-  for (int c = 0; c < grid; ++c) L.cta_off[c + 1] = (uint16_t)(L.cta_off[c] + count_of[c]);
-  uint16_t fill[kMaxListGrid];
-  for (int c = 0; c < grid; ++c) fill[c] = L.cta_off[c];
-  // each CTA's list in assignment order (costliest units first)
-  for (int j = 0; j < L.count; ++j) {
-    const DecodeProblem& pr = L.prob[pord[j]];
-    for (int t = 0; t < pr.ntiles; ++t) {
-      const int u = pr.unit_begin + t;
-      L.units[fill[cta_of[u]]++] = (uint16_t)u;
-    }
-  }
+  for (int c = 0; c < grid; ++c) L.cta_count[c] = count_of[c];
   return true;
 }
 
