@@ -41,7 +41,9 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreadsP = 10 * 32;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
-constexpr int kPrefetch = 3;          // dequant global-load distance (stages)
+constexpr int kPrefetch = 3;          // scale/zero global-load distance (stages)
+constexpr int kWStages = 4;           // packed-weight TMA ring depth
+constexpr int W_STAGE_MAX = BN * BK * 4 / 8;  // packed bytes of one stage (INT4: 32 bytes per row)
 
 template <int NMT>
 struct PCfg {
@@ -51,6 +53,8 @@ struct PCfg {
 };
 
 static_assert(BN == kDqWarps * 32, "one dequant thread per weight row");
+static_assert(PCfg<1>::STAGES * PCfg<1>::STAGE + kWStages * W_STAGE_MAX + 1024 + 256 <= 232448, "shared memory");
+static_assert(PCfg<2>::STAGES * PCfg<2>::STAGE + kWStages * W_STAGE_MAX + 1024 + 256 <= 232448, "shared memory");
 // split-K slots: ksplit x BM rows x (BN / ksplit + 4) floats, largest at ksplit = 8
 static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::STAGES * PCfg<1>::STAGE, "split-K slots fit in the stages");
 
@@ -117,11 +121,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
 
@@ -186,7 +188,8 @@ __device__ __forceinline__ void store_out(const PrefillParams& p, int m, int n, 
 
 template <int BITS, int EPI, int NMT>
 __global__ void __launch_bounds__(kThreadsP, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap amap, const PrefillParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
+                   const PrefillParams p) {
   constexpr int kStagesP = PCfg<NMT>::STAGES;
   constexpr uint32_t kTmemCols = PCfg<NMT>::TMEM_COLS;
   constexpr int CPW = 32 / BITS;
@@ -197,13 +200,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = smem;                                // [stage][NMT][A_STAGE]
+  constexpr int W_STAGE = BN * BK * BITS / 8;        // packed weights of one stage
   uint8_t* sb = smem + kStagesP * NMT * A_STAGE;     // [stage][B_STAGE]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sb + kStagesP * B_STAGE);
+  uint8_t* sw = sb + kStagesP * B_STAGE;             // [kWStages][BN rows][BK * BITS / 8 bytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sw + kWStages * W_STAGE_MAX);
   uint64_t* full_a = bars;
   uint64_t* full_b = bars + kStagesP;
   uint64_t* empty = bars + 2 * kStagesP;
   uint64_t* accum = bars + 3 * kStagesP;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStagesP + 1);
+  uint64_t* wfull = accum + 1;           // [kWStages] packed tile landed (TMA)
+  uint64_t* wempty = wfull + kWStages;   // [kWStages] the dequant warps read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + kWStages);
   float* red = reinterpret_cast<float*>(smem);  // split-K slots, after the main loop
 
   const int warp = threadIdx.x >> 5;
@@ -222,6 +229,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       mbar_init(&empty[i], 1);
     }
     mbar_init(accum, 1);
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], kDqWarps);
+    }
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -247,6 +258,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       for (int kb = max(0, nkb - kStagesP); kb < nkb; ++kb)
         if (!mbar_wait(&full_a[kb % kStagesP], (kb / kStagesP) & 1, 0x202)) break;
+    } else if (lane == 16) {
+      // ---------------- packed weights: TMA producer (no dependency wait: weights are inputs) ----------------
+      tma_prefetch_desc(&wmap);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int ws = kb % kWStages;
+        if (!mbar_wait(&wempty[ws], ((kb / kWStages) & 1) ^ 1, 0x208)) break;
+        mbar_arrive_expect_tx(&wfull[ws], W_STAGE);
+        tma_load_2d(&wmap, &wfull[ws], sw + ws * W_STAGE, (k0 + kb * BK) * BITS / 32, n0);
+      }
+      for (int kb = max(0, nkb - kWStages); kb < nkb; ++kb)
+        if (!mbar_wait(&wfull[kb % kWStages], (kb / kWStages) & 1, 0x209)) break;
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -278,24 +300,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int r = threadIdx.x;  // weight row inside the tile, 0..255
     const int n = n0 + r;
     const bool row_ok = n < p.N;
-    const int wpr = p.K / CPW;
-    const uint32_t* wrow = p.W + (size_t)(row_ok ? n : 0) * wpr;
     const int G = p.K / p.group;
     const __half* srow = p.S + (size_t)(row_ok ? n : 0) * G;
     const __half* zrow = p.Z + (size_t)(row_ok ? n : 0) * G;
     const bool two_groups = (BITS == 4) && (p.group < BK);  // INT4 with group 32
 
-    // packed words and raw 16-bit scale/zero bits, kPrefetch stages ahead (the
-    // half2 broadcast happens at use, so no load is waited on at issue)
-    uint4 ring[kPrefetch][NV];
+    // raw 16-bit scale/zero bits, kPrefetch stages ahead (the half2 broadcast
+    // happens at use, so no load is waited on at issue); the packed words come
+    // through the TMA ring
     unsigned short sring[kPrefetch][2], zring[kPrefetch][2];
-    auto issue = [&](int kb, uint4 (&dst)[NV], unsigned short (&sd)[2], unsigned short (&zd)[2]) {
+    auto issue = [&](int kb, unsigned short (&sd)[2], unsigned short (&zd)[2]) {
       const int ks = k0 + kb * BK;
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int kv = ks + v * 4 * CPW;
-        dst[v] = (row_ok && kv < p.K) ? ldg_nc_v4(wrow + kv / CPW) : make_uint4(0, 0, 0, 0);
-      }
       const int g0 = ks / p.group;
       const int g1 = two_groups ? min(g0 + 1, G - 1) : g0;
       const unsigned short* sp = reinterpret_cast<const unsigned short*>(srow);
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     };
 #pragma unroll
     for (int j = 0; j < kPrefetch; ++j)
-      if (j < nkb) issue(j, ring[j], sring[j], zring[j]);
+      if (j < nkb) issue(j, sring[j], zring[j]);
 
     bool ok = true;
     for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
@@ -315,13 +330,28 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       for (int j = 0; j < kPrefetch; ++j) {
         const int kb = kb0 + j;
         if (kb < nkb && ok) {
-          uint4 cur[NV];
-#pragma unroll
-          for (int v = 0; v < NV; ++v) cur[v] = ring[j][v];
           const uint32_t s_lo = bcast16(sring[j][0]), s_hi = bcast16(sring[j][1]);
           const uint32_t nzs_lo = hmul2u(bcast16(zring[j][0]), s_lo) ^ 0x80008000u;  // -(z * s)
           const uint32_t nzs_hi = hmul2u(bcast16(zring[j][1]), s_hi) ^ 0x80008000u;
-          if (kb + kPrefetch < nkb) issue(kb + kPrefetch, ring[j], sring[j], zring[j]);
+          if (kb + kPrefetch < nkb) issue(kb + kPrefetch, sring[j], zring[j]);
+          // this stage's packed words: row r of the TMA tile (INT4: two 16-byte
+          // chunks, swapped in rows with bit 2 set by SWIZZLE_32B; INT2: one)
+          const int ws = kb % kWStages;
+          if (!mbar_wait(&wfull[ws], (kb / kWStages) & 1, 0x207)) {
+            ok = false;
+            break;
+          }
+          uint4 cur[NV];
+          {
+            const uint32_t wr = smem_u32(sw + ws * W_STAGE) + (uint32_t)r * (BK * BITS / 8);
+            if constexpr (BITS == 4) {
+              const uint32_t sw32 = (uint32_t)((r >> 2) & 1) << 4;
+              cur[0] = lds128(wr + sw32);
+              cur[1] = lds128(wr + (sw32 ^ 16u));
+            } else {
+              cur[0] = lds128(wr);
+            }
+          }
           const int slot = kb % kStagesP;
           if (!mbar_wait(&empty[slot], ((kb / kStagesP) & 1) ^ 1, 0x205)) {
             ok = false;
@@ -378,7 +408,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&full_b[slot]);
+          if (lane == 0) {
+            mbar_arrive(&full_b[slot]);
+            mbar_arrive(&wempty[ws]);  // its words are consumed
+          }
         }
       }
     }
@@ -541,7 +574,14 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (st != TLQ_OK) return st;
 
-  const size_t smem = 1024 + (size_t)PCfg<NMT>::STAGES * PCfg<NMT>::STAGE + 256;
+  CUtensorMap wmap;
+  const uint64_t wpr = (uint64_t)a.K * BITS / 32;  // words per row
+  st = encode_tiled_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, wpr, (uint64_t)a.N, wpr * 4, BK * BITS / 32, BN,
+                       BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (st != TLQ_OK) return st;
+
+  const size_t smem = 1024 + (size_t)PCfg<NMT>::STAGES * PCfg<NMT>::STAGE + (size_t)kWStages * W_STAGE_MAX + 256;
   auto kern = prefill_kernel<BITS, EPI, NMT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -571,7 +611,7 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   }
   lc.attrs = attrs;
   lc.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, p);
+  cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, wmap, p);
   if (e != cudaSuccess) return cuda_error(e, "prefill: launch");
   if (log_enabled())
     fprintf(stderr,
