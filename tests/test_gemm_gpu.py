@@ -212,6 +212,21 @@ def test_prefill_every_k_split(lib, monkeypatch, bits, ks):
     assert_close(C, ref, "prefill ksplit %s int%d" % (ks, bits))
 
 
+@pytest.mark.parametrize("ks", ["2", "4", "8"])
+@pytest.mark.parametrize("bits", [4, 2])
+def test_prefill_two_token_tiles_with_k_split(lib, monkeypatch, bits, ks):
+    """Two token tiles per CTA and a cluster k split: the partial tiles are reduced once per token tile."""
+    group = synth.DIST[bits]["group"]
+    case = synth.gemm_case(300, 264, 2048, bits, group, seed=17, a_scale=0.5)
+    monkeypatch.setenv("TLQ_PREFILL_NMT", "2")
+    monkeypatch.setenv("TLQ_PREFILL_KSPLIT", ks)
+    Wd, C = run_case(lib, case)
+    C2 = lib.quant_gemm(dev(case["A"]), Wd, dev(case["scales"]), dev(case["zeros"]), bits, group)
+    assert torch.equal(torch.from_numpy(C).cuda().view(torch.int16), C2.view(torch.int16)), "not deterministic"
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(C, ref, "prefill nmt 2 ksplit %s int%d" % (ks, bits))
+
+
 @pytest.mark.parametrize("nmt", ["1", "2"])
 @pytest.mark.parametrize("bits,group,M,N,K", [
     (4, 128, 129, 256, 512),   # second token tile holds one row

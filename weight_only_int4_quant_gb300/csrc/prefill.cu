@@ -57,6 +57,7 @@ static_assert(PCfg<1>::STAGES * PCfg<1>::STAGE + kWStages * W_STAGE_MAX + 1024 +
 static_assert(PCfg<2>::STAGES * PCfg<2>::STAGE + kWStages * W_STAGE_MAX + 1024 + 256 <= 232448, "shared memory");
 // split-K slots: ksplit x BM rows x (BN / ksplit + 4) floats, largest at ksplit = 8
 static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::STAGES * PCfg<1>::STAGE, "split-K slots fit in the stages");
+static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<2>::STAGES * PCfg<2>::STAGE, "split-K slots fit in the stages");
 
 // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16,
 // both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -465,53 +466,58 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
 
   // ---------------- split-K: reduce partial tiles across the cluster ----------------
-  // Rank o owns columns [o * cpr, (o + 1) * cpr).  After a first cluster
-  // barrier (every rank's stage memory is idle), each rank pushes its partial
-  // tile's columns to their owners with remote stores, slot = its own rank;
-  // after a second barrier each owner sums its slots in rank order (fixed,
-  // deterministic) with local loads and writes the outputs.
-  if (NMT == 1 && p.ksplit > 1) {
+  // Rank o owns columns [o * cpr, (o + 1) * cpr).  Once per token tile: after
+  // a cluster barrier (every rank's stage memory is idle, or the previous
+  // round's slots are summed), each rank pushes its partial columns to their
+  // owners with remote stores, slot = its own rank; after a second barrier
+  // each owner sums its slots in rank order (fixed, deterministic) with local
+  // loads and writes the outputs.
+  if (p.ksplit > 1) {
     const int ks = p.ksplit;
     const int cpr = BN / ks;  // 32, 64 or 128: a 32-column TMEM block never straddles two owners
     const int pitch = cpr + 4;  // floats per row of a slot (16-byte aligned, staggered banks)
     const uint32_t red_addr = smem_u32(red);
-    __syncwarp();
-    cluster_sync();
-    if (warp < kDqWarps && acc_ok) {
-      const int q = warp & 3, half = warp >> 2;
-      const int mrow = 32 * q + lane;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col = half * 128 + cc * 32;
-        uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
-        const int owner = col / cpr;
-        const uint32_t dst = map_shared_rank(
-            red_addr + (uint32_t)(((rank * BM + mrow) * pitch + (col - owner * cpr)) * 4), (uint32_t)owner);
+    for (int mt = 0; mt < NMT; ++mt) {
+      __syncwarp();
+      cluster_sync();
+      if (warp < kDqWarps && acc_ok) {
+        const int q = warp & 3, half = warp >> 2;
+        const int mrow = 32 * q + lane;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int col = half * 128 + cc * 32;
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * mt + col), v);
+          const int owner = col / cpr;
+          const uint32_t dst = map_shared_rank(
+              red_addr + (uint32_t)(((rank * BM + mrow) * pitch + (col - owner * cpr)) * 4), (uint32_t)owner);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) st_shared_cluster_v4(dst + 16u * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            st_shared_cluster_v4(dst + 16u * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
       }
-    }
-    __syncwarp();
-    cluster_sync();
-    pdl_wait();
-    const int quads = cpr / 4;
-    for (int it = threadIdx.x; it < BM * quads; it += kThreadsP) {
-      const int mm = it / quads;
-      const int c4 = 4 * (it - mm * quads);
-      float a[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < ks; ++j) {
-        const float4 x = *reinterpret_cast<const float4*>(red + ((size_t)(j * BM + mm) * pitch + c4));
-        a[0] += x.x;
-        a[1] += x.y;
-        a[2] += x.z;
-        a[3] += x.w;
-      }
-      const int m = m0 + mm, n = n0 + rank * cpr + c4;
-      if (m < p.M) {
+      __syncwarp();
+      cluster_sync();
+      if (mt == 0) pdl_wait();
+      const int quads = cpr / 4;
+      for (int it = threadIdx.x; it < BM * quads; it += kThreadsP) {
+        const int mm = it / quads;
+        const int c4 = 4 * (it - mm * quads);
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < ks; ++j) {
+          const float4 x = *reinterpret_cast<const float4*>(red + ((size_t)(j * BM + mm) * pitch + c4));
+          a[0] += x.x;
+          a[1] += x.y;
+          a[2] += x.z;
+          a[3] += x.w;
+        }
+        const int m = m0 + mt * BM + mm, n = n0 + rank * cpr + c4;
+        if (m < p.M) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (n + i < p.N) store_out<EPI>(p, m, n + i, a[i]);
+          for (int i = 0; i < 4; ++i)
+            if (n + i < p.N) store_out<EPI>(p, m, n + i, a[i]);
+        }
       }
     }
   }
@@ -525,6 +531,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
 }
 
+// k split of a grid of `tiles` output tiles: double it while the grid stays
+// within half the SMs and every slice keeps at least 4 stages.
+int ksplit_for(int tiles, int nkb, int sms) {
+  int ks = 1;
+  while (ks < 8 && tiles * ks * 2 <= sms && nkb / (ks * 2) >= 4) ks *= 2;
+  return ks;
+}
+
 template <int BITS, int EPI, int NMT>
 tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   const int sms = device_info().sms;
@@ -533,13 +547,10 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   const int nkb = (a.K + BK - 1) / BK;
   int ks = 1;
   const char* env = getenv("TLQ_PREFILL_KSPLIT");
-  if (NMT == 2) {
-    ks = 1;  // the split-K reduction buffer holds one token tile
-  } else if (env) {
+  if (env) {
     ks = atoi(env);
   } else {
-    const int tiles = ntile * mtile;
-    while (ks < 8 && tiles * ks * 2 <= sms && nkb / (ks * 2) >= 4) ks *= 2;
+    ks = ksplit_for(ntile * mtile, nkb, sms);
   }
   if (ks != 1 && ks != 2 && ks != 4 && ks != 8) return set_error(TLQ_EINVAL, "prefill: k split %d", ks);
   const int per = (nkb + ks - 1) / ks;
@@ -621,16 +632,23 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   return TLQ_OK;
 }
 
-// Two token tiles per CTA when that still gives at least one CTA per SM
-// (TLQ_PREFILL_NMT=1|2 forces the choice; a forced k split implies one tile).
+// Two token tiles per CTA (one dequantized weight tile feeds both) when M
+// has two tiles and that grid fills most SMs, either without a k split or
+// with a 2-way split whose slices keep at least 32 stages (the reduction runs
+// once per token tile; measured slower with shorter slices or wider splits);
+// TLQ_PREFILL_NMT=1|2 forces the choice.
 template <int BITS, int EPI>
 tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
   int nmt = 0;
   if (const char* e = getenv("TLQ_PREFILL_NMT")) nmt = atoi(e);
   if (nmt != 1 && nmt != 2) {
+    const int sms = device_info().sms;
     const int ntile = (a.N + BN - 1) / BN;
     const int mt2 = (a.M + 2 * BM - 1) / (2 * BM);
-    nmt = (getenv("TLQ_PREFILL_KSPLIT") == nullptr && a.M > BM && ntile * mt2 >= device_info().sms) ? 2 : 1;
+    const int nkb = (a.K + BK - 1) / BK;
+    const int ks2 = ksplit_for(ntile * mt2, nkb, sms);
+    const int ctas2 = ntile * mt2 * ks2;
+    nmt = (a.M > BM && 5 * ctas2 >= 3 * sms && (ks2 == 1 || (ks2 == 2 && nkb / ks2 >= 32))) ? 2 : 1;
   }
   return nmt == 2 ? launch_impl<BITS, EPI, 2>(a, s) : launch_impl<BITS, EPI, 1>(a, s);
 }
