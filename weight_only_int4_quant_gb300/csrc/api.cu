@@ -259,17 +259,21 @@ tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void
   if (!aligned16(b->h) || !aligned16(b->qkv_out) || !aligned16(b->o_out) || !aligned16(b->up_out))
     return set_error(TLQ_EINVAL, "tl_loop_block_forward: scratch buffers must be 16-byte aligned");
 
+  // The block's weights are re-read every iteration: when they fit in half
+  // the L2 they are streamed with an evict-last policy so that iterations
+  // after the first read them from L2 ("Model", "Returns", item 4: auto tile
+  // sizing reports loop-block vs L2 residency).
+  const int cpw = 32 / b->bits;
+  size_t wb = 0;
+  for (int i = 0; i < 4; ++i)
+    wb += (size_t)projs[i]->N * (projs[i]->K / cpw) * 4 + (size_t)projs[i]->N * (projs[i]->K / b->group) * 4;
+  const bool keep = L > 1 && wb <= (size_t)device_info().l2_bytes / 2;
   static std::once_flag logged;
   if (log_enabled()) {
     std::call_once(logged, [&] {
-      const int cpw = 32 / b->bits;
-      size_t wb = 0;
-      for (int i = 0; i < 4; ++i)
-        wb += (size_t)projs[i]->N * (projs[i]->K / cpw) * 4 + (size_t)projs[i]->N * (projs[i]->K / b->group) * 4;
       fprintf(stderr, "[tlq] loop block: INT%d group %d, packed weights + scales/zeros %.1f MB, L2 %.1f MB -> %s\n",
               b->bits, b->group, wb / 1e6, device_info().l2_bytes / 1e6,
-              wb <= (size_t)device_info().l2_bytes / 2 ? "L2-resident after the first iteration"
-                                                       : "streamed from HBM every iteration");
+              keep ? "kept in L2 (evict-last) after the first iteration" : "streamed from HBM every iteration");
     });
   }
 
@@ -280,6 +284,7 @@ tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void
     a.bits = b->bits;
     a.group = b->group;
     a.M = M;
+    a.l2_keep = keep ? 1 : 0;
     a.X = nullptr;
     a.ldx = 0;
     // QKV

@@ -301,6 +301,7 @@ struct GemmArgs {
   int ldx;
   int M, N, K, bits, group;
   int epi;
+  int l2_keep = 0;  // 1: stream the weights with an L2 evict-last policy (reused soon, e.g. the loop block)
 };
 
 // Error reporting (thread-local message)

@@ -96,6 +96,7 @@ struct DecodeLaunch {
   DecodeProblem prob[kMaxProblems];
   int count;
   int total_units;
+  int keep_mask;  // bit p: problem p's weights are streamed evict-last (kept in L2)
   int gmax;    // largest K/group
   int gpitch;  // row pitch of the scale/zero tiles in halves: gmax rounded up to 8, plus 8
   int nsz;     // scale/zero buffers (3 or 2, by shared memory)
@@ -187,7 +188,8 @@ struct Producer {
     const int slot = warp * kSPW + (issued % kSPW);
     const Sched e = tab[ri];
     mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
-    tma_load_2d_hint(&L.wmap[e.p], &full[slot], ring + slot * STAGE_BYTES, kb * kWordsPerKBlock, e.n0, pol);
+    tma_load_2d_hint(&L.wmap[e.p], &full[slot], ring + slot * STAGE_BYTES, kb * kWordsPerKBlock, e.n0,
+                     ((L.keep_mask >> e.p) & 1) ? policy_evict_last() : pol);
     ++issued;
     kb += kWarps;
     skip(tab);
@@ -821,6 +823,7 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
     pr.G = g.K / g.group;
     pr.szvec = (pr.G % 8 == 0) && ((reinterpret_cast<uintptr_t>(g.S) | reinterpret_cast<uintptr_t>(g.Z)) % 16 == 0);
     pr.epi = g.epi;
+    if (g.l2_keep) L.keep_mask |= 1 << j;
     pr.ntiles = (g.N + ROWS - 1) / ROWS;
     pr.nkb = (g.K + F::KBLK - 1) / F::KBLK;
     pr.unit_begin = units;

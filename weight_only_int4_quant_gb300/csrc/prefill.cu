@@ -74,6 +74,7 @@ struct PrefillParams {
   int M, N, K, group;
   int kslice;  // k per cluster rank (multiple of BK)
   int ksplit;
+  int l2_keep;  // stream the weights evict-last (kept in L2)
 };
 
 // Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row atoms of
@@ -266,7 +267,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int ws = kb % kWStages;
         if (!mbar_wait(&wempty[ws], ((kb / kWStages) & 1) ^ 1, 0x208)) break;
         mbar_arrive_expect_tx(&wfull[ws], W_STAGE);
-        tma_load_2d(&wmap, &wfull[ws], sw + ws * W_STAGE, (k0 + kb * BK) * BITS / 32, n0);
+        if (p.l2_keep)
+          tma_load_2d_hint(&wmap, &wfull[ws], sw + ws * W_STAGE, (k0 + kb * BK) * BITS / 32, n0, policy_evict_last());
+        else
+          tma_load_2d(&wmap, &wfull[ws], sw + ws * W_STAGE, (k0 + kb * BK) * BITS / 32, n0);
       }
       for (int kb = max(0, nkb - kWStages); kb < nkb; ++kb)
         if (!mbar_wait(&wfull[kb % kWStages], (kb / kWStages) & 1, 0x209)) break;
@@ -575,6 +579,7 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   p.N = a.N;
   p.K = a.K;
   p.group = a.group;
+  p.l2_keep = a.l2_keep;
   p.kslice = per2 * BK;
   p.ksplit = (a.K + p.kslice - 1) / p.kslice;
   if (p.ksplit != ksplit) return set_error(TLQ_EINVAL, "prefill: inconsistent k split");
