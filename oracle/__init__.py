@@ -22,6 +22,10 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   rms_norm_half                    closed forms (constant rows, scale invariance)
   loop_block                       brute force on tiny shapes, closed form
                                    (zero update), split-iteration invariant
+  requant_int4_to_int2             closed forms (a 4-level group, a constant
+                                   group), per-weight error bound, and the
+                                   page's test: error within 2x of direct
+                                   binary32 -> INT2 rounding
 """
 from __future__ import annotations
 
@@ -73,6 +77,7 @@ def _load():
                 "orc_quant_gemm_points": [P, I, P, P, P, I, I, I, I, I, P, P, I, P],
                 "orc_rms_norm_half": [P, I, I, ctypes.c_double, P],
                 "orc_loop_block": [P, I, I, I, P, P, P, P, I, I, I, I, ctypes.c_double],
+                "orc_requant_int4_to_int2": [P, P, P, I, I, I, P, P, P],
             }.items():
                 f = getattr(lib, name)
                 f.restype = ctypes.c_int
@@ -216,3 +221,25 @@ def loop_block(x: np.ndarray, block: dict, bits: int, group: int, L: int, normal
                                 L, 1 if normalize else 0, eps)
     _check(rc, "loop_block")
     return x
+
+
+# ----------------------------------------------------------------------------
+# INT4 -> INT2 group re-quantization: beta-Informed Deployment Features,
+# CTX-TIER, "Details of the shipped kernel" (per group: dequantize, scale =
+# (max - min) / 3, zero = min, round to nearest, four codes per byte).
+# ----------------------------------------------------------------------------
+
+def requant_int4_to_int2(W4: np.ndarray, scales, zeros, K: int, group: int):
+    """INT4 packed words [N][K/8] + FP16 scales/zeros [N][K/group] ->
+    (INT2 words [N][K/16], FP16 scales, FP16 zeros), group unchanged; the
+    binary32 steps are listed in tlq_oracle.c."""
+    W4 = np.ascontiguousarray(W4, dtype=np.uint32)
+    N = W4.shape[0]
+    s4 = _half_bits(scales)
+    z4 = _half_bits(zeros)
+    W2 = np.zeros((N, K // 16), dtype=np.uint32)
+    s2 = np.zeros((N, K // group), dtype=np.uint16)
+    z2 = np.zeros((N, K // group), dtype=np.uint16)
+    _check(_load().orc_requant_int4_to_int2(_ptr(W4), _ptr(s4), _ptr(z4), N, K, group, _ptr(W2), _ptr(s2),
+                                            _ptr(z2)), "requant_int4_to_int2")
+    return W2, s2.view(np.float16), z2.view(np.float16)

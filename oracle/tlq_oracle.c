@@ -282,3 +282,66 @@ int orc_loop_block(float* x, int M, int D, int F, const orc_proj* qkv, const orc
   free(d);
   return rc;
 }
+
+/* ------------------------------------------------------------------ */
+/* INT4 -> INT2 group re-quantization                                  */
+/* ------------------------------------------------------------------ */
+
+/* "beta-Informed Deployment Features", CTX-TIER, "Details of the shipped
+ * kernel": every quantization group of the INT4 weight is dequantized, a new
+ * asymmetric INT2 grid with scale = (max - min) / 3 and zero = min is fitted,
+ * and each weight is rounded to the nearest of the grid's four levels; the
+ * group size stays that of the INT4 weight and the INT2 rows are compact
+ * (K/4 bytes, out of place, as in the page's Phase 2b).
+ *
+ * Readings of this library, all in binary32 and in this order (the GPU takes
+ * every integer decision in the same precision):
+ *   w      = (q4 - z4) * s4                  exact (see orc_dequant)
+ *   lo, hi = min and max of w over the group
+ *   s2     = fp16_RNE((hi - lo) / 3); 1.0 when that is zero
+ *   z2     = fp16_RNE(-lo / s2)              zero = min in this library's
+ *                                            (q - z) * s form
+ *   q2     = clamp(rint(w / s2 + z2), 0, 3)  round to nearest, ties to even
+ * so that (q2 - z2) * s2 is exactly what the INT2 GEMM reads. */
+int orc_requant_int4_to_int2(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, int N, int K,
+                             int group, uint32_t* W2, uint16_t* s2, uint16_t* z2) {
+  if (check_shape(N, K, 4, group) || check_shape(N, K, 2, group) || group % 16) return -1;
+  const int wpr4 = K / 8, wpr2 = K / 16, G = K / group;
+  float* w = (float*)malloc(sizeof(float) * (size_t)group);
+  if (!w) return -2;
+  memset(W2, 0, sizeof(uint32_t) * (size_t)N * wpr2);
+  for (int n = 0; n < N; ++n) {
+    for (int g = 0; g < G; ++g) {
+      const size_t gi = (size_t)n * G + g;
+      const float s = (float)orc_half_to_double(s4[gi]); /* exact: binary16 fits binary32 */
+      const float z = (float)orc_half_to_double(z4[gi]);
+      float lo = INFINITY, hi = -INFINITY;
+      for (int j = 0; j < group; ++j) {
+        const int k = g * group + j;
+        const float q = (float)code_at(W4 + (size_t)n * wpr4, k, 4);
+        const float v = (q - z) * s;
+        w[j] = v;
+        if (v < lo) lo = v;
+        if (v > hi) hi = v;
+      }
+      uint16_t sb = orc_double_to_half((double)((hi - lo) / 3.0f));
+      if (orc_half_to_double(sb) == 0.0) sb = orc_double_to_half(1.0);
+      const float sh = (float)orc_half_to_double(sb);
+      const uint16_t zb = orc_double_to_half((double)(-lo / sh));
+      const float zh = (float)orc_half_to_double(zb);
+      for (int j = 0; j < group; ++j) {
+        const int k = g * group + j;
+        float t = w[j] / sh;
+        t = t + zh;
+        float r = rintf(t);
+        if (r < 0.0f) r = 0.0f;
+        if (r > 3.0f) r = 3.0f;
+        W2[(size_t)n * wpr2 + k / 16] |= (uint32_t)r << (2 * (k % 16));
+      }
+      s2[gi] = sb;
+      z2[gi] = zb;
+    }
+  }
+  free(w);
+  return 0;
+}

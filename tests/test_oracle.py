@@ -356,3 +356,88 @@ def test_loop_block_full_width_stays_finite(bits):
     x = oracle.loop_block(case["x0"], blk, bits, case["group"], L=16, normalize=True)
     assert np.all(np.isfinite(x))
     assert np.max(np.abs(x)) > 10.0
+
+
+# ---------------------------------------------------------------------------
+# INT4 -> INT2 re-quantization (beta-Informed Deployment Features, CTX-TIER,
+# "Details of the shipped kernel")
+# ---------------------------------------------------------------------------
+
+def _int2_dequant(W2, s2, z2, K, group):
+    return oracle.dequant(W2, s2, z2, K, 2, group)
+
+
+def test_requant_four_level_group_is_exact():
+    """A group whose INT4 values sit on a 4-level grid {0, d, 2d, 3d} comes back exactly: codes 0..3,
+    scale d, zero 0 -- the grid the page's scale = (max - min) / 3, zero = min describes."""
+    K, group = 256, 128
+    rng = np.random.default_rng(3)
+    q4 = rng.choice([0, 5, 10, 15], size=(2, K)).astype(np.uint8)
+    q4[:, 0], q4[:, 1] = 0, 15  # each group spans the full range
+    q4[:, 128], q4[:, 129] = 0, 15
+    W4 = oracle.pack(q4, 4)
+    s4 = np.full((2, K // group), 0.0625, dtype=np.float16)
+    z4 = np.zeros((2, K // group), dtype=np.float16)
+    W2, s2, z2 = oracle.requant_int4_to_int2(W4, s4, z4, K, group)
+    assert np.all(s2.astype(np.float64) == 0.3125)  # (15 - 0) * 0.0625 / 3
+    assert np.all(z2.astype(np.float64) == 0.0)
+    np.testing.assert_array_equal(oracle.unpack(W2, K, 2), q4 // 5)
+    np.testing.assert_array_equal(_int2_dequant(W2, s2, z2, K, group), oracle.dequant(W4, s4, z4, K, 4, group))
+
+
+def test_requant_constant_group():
+    """All codes of a group equal: max == min, the scale falls back to 1 and every weight returns exactly."""
+    K, group = 128, 128
+    q4 = np.full((3, K), 7, dtype=np.uint8)
+    W4 = oracle.pack(q4, 4)
+    s4 = np.array([[0.015625], [0.0078125], [0.25]], dtype=np.float16)
+    z4 = np.array([[3.0], [9.5], [7.0]], dtype=np.float16)
+    W2, s2, z2 = oracle.requant_int4_to_int2(W4, s4, z4, K, group)
+    assert np.all(s2.astype(np.float64) == 1.0)
+    np.testing.assert_array_equal(oracle.unpack(W2, K, 2), 0)
+    np.testing.assert_array_equal(_int2_dequant(W2, s2, z2, K, group), oracle.dequant(W4, s4, z4, K, 4, group))
+
+
+def test_requant_error_bound_per_weight():
+    """Every weight lands within half a grid step (plus the FP16 rounding of the zero point) of its INT4
+    value, on the INT4 workload distribution."""
+    rng = synth.rng_for(9)
+    K, group = 512, 128
+    codes, s4, z4 = synth.quant_weights(rng, 64, K, 4, group)
+    W4 = oracle.pack(codes, 4)
+    W2, s2, z2 = oracle.requant_int4_to_int2(W4, s4, z4, K, group)
+    w4 = oracle.dequant(W4, s4, z4, K, 4, group)
+    w2 = _int2_dequant(W2, s2, z2, K, group)
+    sg = np.repeat(s2.astype(np.float64), group, axis=1)
+    zg = np.repeat(np.abs(z2.astype(np.float64)), group, axis=1)
+    bound = sg * (0.5 + zg * 2.0 ** -11) + 1e-12
+    assert np.all(np.abs(w2 - w4) <= bound)
+    # and both ends of each group are represented: codes 0 and 3 occur in every group
+    q2 = oracle.unpack(W2, K, 2).reshape(64, K // group, group)
+    assert np.all(q2.min(axis=2) == 0) and np.all(q2.max(axis=2) == 3)
+
+
+def test_requant_matches_direct_rounding_error():
+    """The page's test: N=64, K=256, group 128 Gaussian weights, INT4 asymmetric rounding, then the
+    re-quantization, against direct binary32 -> INT2 rounding of the same weights: error ratio within 2x
+    (the page measured 1.000).  The INT4 and direct quantizers are written here independently."""
+    rng = np.random.default_rng(2026)
+    N, K, group = 64, 256, 128
+    w = rng.standard_normal((N, K)).astype(np.float32)
+    G = K // group
+    wg = w.reshape(N, G, group).astype(np.float64)
+    lo, hi = wg.min(axis=2), wg.max(axis=2)
+    # INT4 asymmetric round-to-nearest in this library's (q - z) * s form, FP16 scale and zero
+    s4 = ((hi - lo) / 15).astype(np.float16)
+    z4 = (-lo / s4.astype(np.float64)).astype(np.float16)
+    q4 = np.clip(np.rint(wg / s4.astype(np.float64)[..., None] + z4.astype(np.float64)[..., None]), 0, 15)
+    W4 = oracle.pack(q4.reshape(N, K).astype(np.uint8), 4)
+    W2, s2, z2 = oracle.requant_int4_to_int2(W4, s4, z4, K, group)
+    err_rq = np.linalg.norm(_int2_dequant(W2, s2, z2, K, group) - w.astype(np.float64))
+    # direct binary32 -> INT2: scale = (max - min) / 3, zero = min, round to nearest
+    sc = (hi - lo) / 3
+    q2d = np.clip(np.rint((wg - lo[..., None]) / sc[..., None]), 0, 3)
+    err_direct = np.linalg.norm((lo[..., None] + q2d * sc[..., None]).reshape(N, K) - w.astype(np.float64))
+    ratio = err_rq / err_direct
+    assert ratio <= 2.0, ratio
+    assert ratio >= 0.5, ratio
