@@ -407,6 +407,9 @@ def run_tlq(args, rank, world, dist):
     # ---- secondary: loop block ----
     result["loop_block"] = run_loop_block(tlq, torch)
 
+    # ---- secondary: INT4 -> INT2 re-quantization of the loop block (tier switch) ----
+    result["requant"] = run_requant(tlq, torch, peaks, l2)
+
     torch.cuda.synchronize()
     traffic = None
     if NCU_TRAFFIC["kernel_hash"] == kernel_hash() and NCU_TRAFFIC["bytes_per_step"]:
@@ -537,6 +540,49 @@ def run_loop_block(tlq, torch):
     except tlq.TLQError as e:
         out["unavailable"] = str(e)
     return out
+
+
+def run_requant(tlq, torch, peaks, l2):
+    """tl_requant_int4_to_int2 on the four D=2048 loop-block projections
+    (INT4 group 128 -> compact INT2 group 128, new scales/zeros), rotating
+    over enough weight copies that every step's inputs miss L2."""
+    group = 128
+    per_set = sum(N * K // 2 + N * K // 4 + 8 * N * K // group for (N, K) in synth.SHAPES.values())
+    ncopy = max(2, -(-2 * l2 // per_set))
+    sets = []
+    try:
+        for c in range(ncopy):
+            rng = synth.rng_for(500 + c)
+            one = []
+            for name in synth.PROJ_ORDER:
+                N, K = synth.SHAPES[name]
+                codes, s, z = synth.quant_weights(rng, N, K, 4, group)
+                W4 = tlq.pack_weights(torch.from_numpy(codes).cuda(), 4)
+                W2 = torch.empty((N, K // 16), dtype=torch.int32, device="cuda")
+                s2 = torch.empty(s.shape, dtype=torch.float16, device="cuda")
+                one.append((W4, torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda(), W2, s2, torch.empty_like(s2)))
+            sets.append(one)
+
+        def step(i):
+            for (W4, s4, z4, W2, s2, z2) in sets[i % ncopy]:
+                tlq.tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, group)
+
+        for i in range(2 * ncopy):
+            step(i)
+        torch.cuda.synchronize()
+        reps = 8 * ncopy
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                step(i)
+        t = time_graph_list(torch, [g], 5, 3)  # ms for 5 replays
+        us = t * 1e3 / (5 * reps)
+        gbps = per_set / (us * 1e-6) / 1e9
+        return {"us_per_block": round(us, 2), "GBps": round(gbps, 1), "frac_of_hbm": round(gbps / peaks["hbm"], 3),
+                "bytes_per_block": per_set, "launches_per_block": 4,
+                "l2": "%d weight copies rotated (%.0f MB)" % (ncopy, ncopy * per_set / 1e6)}
+    except tlq.TLQError as e:
+        return {"unavailable": str(e)}
 
 
 def cpu_baseline(wl):

@@ -136,6 +136,42 @@ tlq_status tl_pack_weights(const uint8_t* codes, uint32_t* Wpacked, int N, int K
 tlq_status tl_unpack_weights(const uint32_t* Wpacked, uint8_t* codes, int N, int K, int bits,
                              void* stream);
 
+/*
+ * tl_requant_int4_to_int2 -- re-quantize an INT4 weight to INT2, the weight
+ * conversion of the context-length tier switch after which quant_gemm routes
+ * the layer to the INT2 kernel.
+ *
+ * Source: "beta-Informed Deployment Features", CTX-TIER, "Details of the
+ * shipped kernel" (Phase 2 / 2b): per quantization group the INT4 weights are
+ * dequantized, an asymmetric INT2 grid with scale = (max - min) / 3 and
+ * zero = min is fitted, and each weight is rounded to the nearest of its four
+ * levels; the group size is kept; the INT2 rows are compact so the INT4
+ * buffer can be released afterwards.
+ *
+ * In this library's (q - z) * s form, per group of row n (binary32, rounded
+ * to nearest even after every step, in this order):
+ *   w  = (q4 - z4) * s4;  lo, hi = min, max of w over the group
+ *   s2 = fp16((hi - lo) / 3), or 1.0 when that is zero;  z2 = fp16(-lo / s2)
+ *   q2 = clamp(rint(w / s2 + z2), 0, 3)
+ * so (q2 - z2) * s2 is the INT2 GEMM's weight.  Codes, s2 and z2 are
+ * bit-exact and deterministic.
+ *
+ *   W4      uint32 [N][K/8] INT4 weight in the tl_pack_weights format;
+ *           16-byte aligned; read only.
+ *   s4, z4  FP16 [N][K/group] scales / zeros of W4; finite values.
+ *   W2      uint32 [N][K/16] output, compact INT2 rows; 16-byte aligned; must
+ *           not overlap any other argument.
+ *   s2, z2  FP16 [N][K/group] output scales / zeros.  Each may be exactly its
+ *           input (s2 == s4, z2 == z4: converted in place) or overlap nothing.
+ *   N >= 1; K >= 1; group a multiple of 64 dividing K (the INT2 kernel's
+ *   rule); the INT2 weight keeps the INT4 weight's group.
+ *   The caller owns every buffer; W4 may be freed once the stream has passed
+ *   the call.  Returns TLQ_OK, TLQ_EINVAL (null, misaligned, overlapping or
+ *   bad shape) or TLQ_ECUDA.
+ */
+tlq_status tl_requant_int4_to_int2(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, uint32_t* W2,
+                                   uint16_t* s2, uint16_t* z2, int N, int K, int group, void* stream);
+
 /* One quantized projection of the loop block: weights [N][K] in the packed
  * format, FP16 scales/zeros [N][K/group]. */
 typedef struct {

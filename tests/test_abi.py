@@ -89,6 +89,31 @@ def test_pack_and_block_reject_bad_arguments(clib):
     assert clib.tl_selftest_wait_timeout(0, None) == tlq.TLQ_EINVAL
 
 
+def test_requant_rejects_bad_arguments(clib):
+    """Validation of tl_requant_int4_to_int2 happens before any launch; the
+    addresses below are never dereferenced."""
+    import weight_only_int4_quant_gb300 as tlq
+
+    N, K, g = 8, 256, 128
+    W4, s4, z4, W2, s2, z2 = 1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 6 << 20
+
+    def rq(W4=W4, s4=s4, z4=z4, W2=W2, s2=s2, z2=z2, N=N, K=K, g=g):
+        return clib.tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, N, K, g, None)
+
+    assert rq(W4=None) == tlq.TLQ_EINVAL and "null" in tlq.tl_last_error()
+    assert rq(z2=None) == tlq.TLQ_EINVAL
+    assert rq(N=0) == tlq.TLQ_EINVAL
+    assert rq(g=32) == tlq.TLQ_EINVAL and "group" in tlq.tl_last_error()  # INT2 groups are multiples of 64
+    assert rq(g=96) == tlq.TLQ_EINVAL
+    assert rq(K=320) == tlq.TLQ_EINVAL  # K % group
+    assert rq(W4=W4 + 8) == tlq.TLQ_EINVAL and "aligned" in tlq.tl_last_error()
+    assert rq(s2=s2 + 1) == tlq.TLQ_EINVAL
+    assert rq(W2=W4 + 64) == tlq.TLQ_EINVAL and "overlap" in tlq.tl_last_error()
+    assert rq(s2=z4) == tlq.TLQ_EINVAL  # s2 on top of z4
+    assert rq(s2=s4 + 2) == tlq.TLQ_EINVAL  # partial overlap with its own input
+    assert rq(z2=s2 + 4) == tlq.TLQ_EINVAL  # outputs overlap each other
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     import weight_only_int4_quant_gb300 as tlq
 

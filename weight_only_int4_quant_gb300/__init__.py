@@ -19,13 +19,14 @@ __all__ = [
     "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights", "tl_loop_block_forward",
     "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout", "tl_last_error", "tl_version",
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "gemm_descs", "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
+    "tl_requant_int4_to_int2", "requant_int4_to_int2",
 ]
 
 # every symbol include/tlq.h declares
 EXPORTED = (
     "tl_last_error", "tl_version", "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights",
     "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
-    "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched",
+    "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "tl_requant_int4_to_int2",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -92,6 +93,7 @@ def load():
             "tl_selftest_wait_timeout": ([U, P], I),
             "tl_loop_block_forward_static_scratch": ([P, ctypes.POINTER(_Block), I, I, P], I),
             "tl_quant_gemm_batched": ([ctypes.POINTER(_GemmDesc), I, P], I),
+            "tl_requant_int4_to_int2": ([P, P, P, P, P, P, I, I, I, P], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -188,6 +190,18 @@ def tl_unpack_weights(W, codes, bits: int, stream=None) -> None:
                                        N, K, bits, _stream(stream)))
 
 
+def tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, group: int, stream=None) -> None:
+    import torch
+
+    N = W4.shape[0]
+    K = W4.shape[1] * 8
+    i32 = (torch.int32, torch.uint32)
+    _raise_if(load().tl_requant_int4_to_int2(_dev(W4, i32, "W4"), _dev(s4, (torch.float16,), "s4"),
+                                             _dev(z4, (torch.float16,), "z4"), _dev(W2, i32, "W2"),
+                                             _dev(s2, (torch.float16,), "s2"), _dev(z2, (torch.float16,), "z2"),
+                                             N, K, group, _stream(stream)))
+
+
 def tl_loop_block_forward(x, block: "LoopBlock", L: int, stream=None) -> None:
     import torch
 
@@ -241,6 +255,17 @@ def pack_weights(codes, bits: int, stream=None):
     return W
 
 
+def requant_int4_to_int2(W4, s4, z4, group: int, in_place_scales: bool = False, stream=None):
+    """INT4 weight -> (INT2 weight, scales, zeros), same group.  With
+    in_place_scales the INT2 scales/zeros overwrite s4/z4."""
+    import torch
+
+    W2 = torch.empty((W4.shape[0], W4.shape[1] // 2), dtype=torch.int32, device=W4.device)
+    s2, z2 = (s4, z4) if in_place_scales else (torch.empty_like(s4), torch.empty_like(z4))
+    tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, group, stream)
+    return W2, s2, z2
+
+
 def unpack_weights(W, K: int, bits: int, stream=None):
     import torch
 
@@ -270,18 +295,49 @@ class LoopBlock:
         self.qkv_out = torch.empty((max_rows, 3 * D), dtype=torch.float16, device=dev)
         self.o_out = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
         self.up_out = torch.empty((max_rows, F), dtype=torch.float16, device=dev)
+        self.normalize = normalize
+        self._bind()
+
+    def _bind(self):
+        import torch
+
+        cpw = 32 // self.bits
         c = _Block()
         for name in ("qkv", "o", "up", "down"):
-            W, s, z = proj[name]
-            N, K = dims[name]
+            W, s, z = self.proj[name]
             setattr(c, name, _QProj(_dev(W, (torch.int32, torch.uint32), name + ".W"),
                                     _dev(s, (torch.float16,), name + ".s"), _dev(z, (torch.float16,), name + ".z"),
-                                    N, K))
-        c.bits, c.group, c.D = bits, group, D
+                                    W.shape[0], W.shape[1] * cpw))
+        c.bits, c.group, c.D = self.bits, self.group, self.D
         c.h, c.qkv_out, c.o_out, c.up_out = (self.h.data_ptr(), self.qkv_out.data_ptr(), self.o_out.data_ptr(),
                                              self.up_out.data_ptr())
-        c.normalize = 1 if normalize else 0
+        c.normalize = 1 if self.normalize else 0
         self._c = c
+
+    def to_int2(self, stream=None):
+        """The context-length tier switch ("beta-Informed Deployment
+        Features", CTX-TIER, Phase 2 / 2b): re-quantize every INT4 projection
+        to compact INT2 (scales / zeros converted in place), wait for the
+        stream, release the INT4 weights and route later forwards to the INT2
+        kernel.  One way; the group size is kept."""
+        import torch
+
+        if self.bits != 4:
+            raise ValueError("to_int2 needs an INT4 block (bits=%d)" % self.bits)
+        new = {}
+        for name in ("qkv", "o", "up", "down"):
+            W4, s4, z4 = self.proj[name]
+            new[name] = requant_int4_to_int2(W4, s4, z4, self.group, in_place_scales=True, stream=stream)
+        if stream is None:
+            torch.cuda.current_stream().synchronize()
+        elif isinstance(stream, int):
+            torch.cuda.synchronize()
+        else:
+            stream.synchronize()
+        self.proj = new  # the INT4 words go back to the allocator with their last reference
+        self.bits = 2
+        self._bind()
+        return self
 
     def forward(self, x, L: int, stream=None):
         tl_loop_block_forward(x, self, L, stream)

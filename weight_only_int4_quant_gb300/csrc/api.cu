@@ -232,6 +232,30 @@ tlq_status tl_unpack_weights(const uint32_t* Wpacked, uint8_t* codes, int N, int
   return launch_unpack(Wpacked, codes, N, K, bits, static_cast<cudaStream_t>(stream));
 }
 
+tlq_status tl_requant_int4_to_int2(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, uint32_t* W2,
+                                   uint16_t* s2, uint16_t* z2, int N, int K, int group, void* stream) {
+  g_msg[0] = 0;
+  if (!W4 || !s4 || !z4 || !W2 || !s2 || !z2) return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: null pointer");
+  if (N < 1 || K < 1) return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: N=%d K=%d must be >= 1", N, K);
+  if (group < 64 || group % 64 || K % group)
+    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: group=%d must be a multiple of 64 dividing K=%d", group, K);
+  if (!aligned16(W4) || !aligned16(W2))
+    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: W4 and W2 must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(s4) | reinterpret_cast<uintptr_t>(z4) | reinterpret_cast<uintptr_t>(s2) |
+       reinterpret_cast<uintptr_t>(z2)) & 1u)
+    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: scales/zeros must be 2-byte aligned");
+  const size_t b4 = (size_t)N * K / 2, b2 = (size_t)N * K / 4, bg = (size_t)N * (K / group) * 2;
+  if (overlaps(W2, b2, W4, b4) || overlaps(W2, b2, s4, bg) || overlaps(W2, b2, z4, bg) ||
+      overlaps(W2, b2, s2, bg) || overlaps(W2, b2, z2, bg))
+    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: W2 overlaps another argument");
+  if (overlaps(s2, bg, W4, b4) || overlaps(z2, bg, W4, b4) || overlaps(s2, bg, z2, bg))
+    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: s2/z2 overlap W4 or each other");
+  if ((s2 != s4 && (overlaps(s2, bg, s4, bg) || overlaps(s2, bg, z4, bg))) ||
+      (z2 != z4 && (overlaps(z2, bg, z4, bg) || overlaps(z2, bg, s4, bg))))
+    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: s2 / z2 must equal s4 / z4 exactly or not overlap them");
+  return launch_requant(W4, s4, z4, W2, s2, z2, N, K, group, static_cast<cudaStream_t>(stream));
+}
+
 tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void* stream_) {
   g_msg[0] = 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
