@@ -563,9 +563,10 @@ def run_requant(tlq, torch, peaks, l2):
                 one.append((W4, torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda(), W2, s2, torch.empty_like(s2)))
             sets.append(one)
 
-        def step(i):
-            for (W4, s4, z4, W2, s2, z2) in sets[i % ncopy]:
-                tlq.tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, group)
+        descs = [tlq.requant_descs(one) for one in sets]
+
+        def step(i):  # one launch converts the four projections
+            tlq.tl_requant_int4_to_int2_batched(descs[i % ncopy], group)
 
         for i in range(2 * ncopy):
             step(i)
@@ -579,7 +580,7 @@ def run_requant(tlq, torch, peaks, l2):
         us = t * 1e3 / (5 * reps)
         gbps = per_set / (us * 1e-6) / 1e9
         return {"us_per_block": round(us, 2), "GBps": round(gbps, 1), "frac_of_hbm": round(gbps / peaks["hbm"], 3),
-                "bytes_per_block": per_set, "launches_per_block": 4,
+                "bytes_per_block": per_set, "launches_per_block": 1,
                 "l2": "%d weight copies rotated (%.0f MB)" % (ncopy, ncopy * per_set / 1e6)}
     except tlq.TLQError as e:
         return {"unavailable": str(e)}

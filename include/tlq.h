@@ -172,6 +172,30 @@ tlq_status tl_unpack_weights(const uint32_t* Wpacked, uint8_t* codes, int N, int
 tlq_status tl_requant_int4_to_int2(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, uint32_t* W2,
                                    uint16_t* s2, uint16_t* z2, int N, int K, int group, void* stream);
 
+/* One weight of tl_requant_int4_to_int2_batched (device pointers, the same
+ * layouts and rules as tl_requant_int4_to_int2). */
+typedef struct {
+  const uint32_t* W4;
+  const uint16_t* s4;
+  const uint16_t* z4;
+  uint32_t* W2;
+  uint16_t* s2;
+  uint16_t* z2;
+  int N, K;
+} tl_requant_desc;
+
+/*
+ * tl_requant_int4_to_int2_batched -- up to 16 weights of one group size
+ * re-quantized in a single launch (the tier switch converts all projections
+ * of the loop block at once).  Results equal `count` separate
+ * tl_requant_int4_to_int2 calls.
+ *   descs  HOST array of `count` descriptors (0 <= count <= 16; 0 is a no-op).
+ *   No output (W2, s2, z2) may overlap any other buffer of any descriptor,
+ *   except s2 == s4 / z2 == z4 of the same descriptor.  Everything is
+ *   validated before the launch (TLQ_EINVAL names the offending index).
+ */
+tlq_status tl_requant_int4_to_int2_batched(const tl_requant_desc* descs, int count, int group, void* stream);
+
 /* One quantized projection of the loop block: weights [N][K] in the packed
  * format, FP16 scales/zeros [N][K/group]. */
 typedef struct {

@@ -113,6 +113,24 @@ def test_requant_rejects_bad_arguments(clib):
     assert rq(s2=s4 + 2) == tlq.TLQ_EINVAL  # partial overlap with its own input
     assert rq(z2=s2 + 4) == tlq.TLQ_EINVAL  # outputs overlap each other
 
+    # batched: count limits, a bad descriptor by index, overlaps across descriptors
+    D = tlq._RequantDesc
+    ok0 = D(W4, s4, z4, W2, s2, z2, N, K)
+    arr = (D * 17)(*([ok0] * 17))
+    assert clib.tl_requant_int4_to_int2_batched(arr, 17, g, None) == tlq.TLQ_EINVAL
+    assert clib.tl_requant_int4_to_int2_batched(None, 2, g, None) == tlq.TLQ_EINVAL
+    assert clib.tl_requant_int4_to_int2_batched(arr, 1, 100, None) == tlq.TLQ_EINVAL
+    bad = (D * 2)(ok0, D(7 << 20, 8 << 20, 9 << 20, 10 << 20, 11 << 20, 12 << 20, N, 200))
+    assert clib.tl_requant_int4_to_int2_batched(bad, 2, g, None) == tlq.TLQ_EINVAL
+    assert "[1]" in tlq.tl_last_error()
+    # problem 1 writes its W2 over problem 0's W4
+    cross = (D * 2)(ok0, D(7 << 20, 8 << 20, 9 << 20, W4 + 256, 11 << 20, 12 << 20, N, K))
+    assert clib.tl_requant_int4_to_int2_batched(cross, 2, g, None) == tlq.TLQ_EINVAL
+    assert "overlap" in tlq.tl_last_error()
+    # problem 1 converts its scales in place of problem 0's scales
+    cross2 = (D * 2)(ok0, D(7 << 20, s4, 9 << 20, 10 << 20, s4, 12 << 20, N, K))
+    assert clib.tl_requant_int4_to_int2_batched(cross2, 2, g, None) == tlq.TLQ_EINVAL
+
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     import weight_only_int4_quant_gb300 as tlq

@@ -99,6 +99,32 @@ def test_requant_full_size_loop_block_weights(lib, proj):
     assert_same(run_gpu(lib, W4, s4, z4, 128), ref, proj)
 
 
+@pytest.mark.parametrize("group", [64, 128, 192, 2048])
+def test_requant_batched_equals_oracle(lib, group):
+    """Several weights of one group size in one launch (the grid strides over
+    all of them): every output against the oracle; one weight converts its
+    scales and zeros in place."""
+    rng = np.random.default_rng(group)
+    shapes = [(40, 2 * 3 * group), (8, 4 * group), (129, 2 * group), (1, group), (16, 6 * group)]
+    host, probs = [], []
+    for i, (N, K) in enumerate(shapes):
+        codes, s4, z4 = weights(rng, N, K, group, ["workload", "signed", "narrow", "degenerate", "extreme"][i])
+        W4 = oracle.pack(codes, 4)
+        with np.errstate(over="ignore"):
+            host.append(oracle.requant_int4_to_int2(W4, s4, z4, K, group))
+        W4d, s4d, z4d = dev(W4.view(np.int32)), dev(s4), dev(z4)
+        W2 = torch.empty((N, K // 16), dtype=torch.int32, device="cuda")
+        if i == 2:
+            probs.append((W4d, s4d, z4d, W2, s4d, z4d))
+        else:
+            probs.append((W4d, s4d, z4d, W2, torch.empty_like(s4d), torch.empty_like(z4d)))
+    lib.tl_requant_int4_to_int2_batched(probs, group)
+    torch.cuda.synchronize()
+    for i, (p, ref) in enumerate(zip(probs, host)):
+        got = (p[3].cpu().numpy().view(np.uint32), p[4].cpu().numpy(), p[5].cpu().numpy())
+        assert_same(got, ref, "problem %d g%d" % (i, group))
+
+
 def test_requant_deterministic(lib):
     codes, s4, z4 = synth.quant_weights(synth.rng_for(3), 512, 2048, 4, 128)
     W4 = oracle.pack(codes, 4)

@@ -19,7 +19,7 @@ __all__ = [
     "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights", "tl_loop_block_forward",
     "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout", "tl_last_error", "tl_version",
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "gemm_descs", "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
-    "tl_requant_int4_to_int2", "requant_int4_to_int2",
+    "tl_requant_int4_to_int2", "tl_requant_int4_to_int2_batched", "requant_int4_to_int2",
 ]
 
 # every symbol include/tlq.h declares
@@ -27,6 +27,7 @@ EXPORTED = (
     "tl_last_error", "tl_version", "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights",
     "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "tl_requant_int4_to_int2",
+    "tl_requant_int4_to_int2_batched",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -48,6 +49,11 @@ class _GemmDesc(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("Wpacked", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("zeros", ctypes.c_void_p), ("C", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
                 ("K", ctypes.c_int), ("bits", ctypes.c_int), ("group", ctypes.c_int)]
+
+
+class _RequantDesc(ctypes.Structure):
+    _fields_ = [("W4", ctypes.c_void_p), ("s4", ctypes.c_void_p), ("z4", ctypes.c_void_p), ("W2", ctypes.c_void_p),
+                ("s2", ctypes.c_void_p), ("z2", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int)]
 
 
 class _Block(ctypes.Structure):
@@ -94,6 +100,7 @@ def load():
             "tl_loop_block_forward_static_scratch": ([P, ctypes.POINTER(_Block), I, I, P], I),
             "tl_quant_gemm_batched": ([ctypes.POINTER(_GemmDesc), I, P], I),
             "tl_requant_int4_to_int2": ([P, P, P, P, P, P, I, I, I, P], I),
+            "tl_requant_int4_to_int2_batched": ([ctypes.POINTER(_RequantDesc), I, I, P], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -200,6 +207,25 @@ def tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, group: int, stream=None) -> 
                                              _dev(z4, (torch.float16,), "z4"), _dev(W2, i32, "W2"),
                                              _dev(s2, (torch.float16,), "s2"), _dev(z2, (torch.float16,), "z2"),
                                              N, K, group, _stream(stream)))
+
+
+def requant_descs(problems):
+    """(W4, s4, z4, W2, s2, z2) tensor tuples -> a ctypes descriptor array."""
+    import torch
+
+    i32 = (torch.int32, torch.uint32)
+    arr = (_RequantDesc * len(problems))()
+    for i, (W4, s4, z4, W2, s2, z2) in enumerate(problems):
+        arr[i] = _RequantDesc(_dev(W4, i32, "W4"), _dev(s4, (torch.float16,), "s4"), _dev(z4, (torch.float16,), "z4"),
+                              _dev(W2, i32, "W2"), _dev(s2, (torch.float16,), "s2"), _dev(z2, (torch.float16,), "z2"),
+                              W4.shape[0], W4.shape[1] * 8)
+    return arr
+
+
+def tl_requant_int4_to_int2_batched(descs, group: int, stream=None) -> None:
+    if not isinstance(descs, ctypes.Array):
+        descs = requant_descs(descs)
+    _raise_if(load().tl_requant_int4_to_int2_batched(descs, len(descs), group, _stream(stream)))
 
 
 def tl_loop_block_forward(x, block: "LoopBlock", L: int, stream=None) -> None:
@@ -324,10 +350,13 @@ class LoopBlock:
 
         if self.bits != 4:
             raise ValueError("to_int2 needs an INT4 block (bits=%d)" % self.bits)
-        new = {}
+        new, probs = {}, []
         for name in ("qkv", "o", "up", "down"):
             W4, s4, z4 = self.proj[name]
-            new[name] = requant_int4_to_int2(W4, s4, z4, self.group, in_place_scales=True, stream=stream)
+            W2 = torch.empty((W4.shape[0], W4.shape[1] // 2), dtype=torch.int32, device=W4.device)
+            new[name] = (W2, s4, z4)
+            probs.append((W4, s4, z4, W2, s4, z4))
+        tl_requant_int4_to_int2_batched(probs, self.group, stream)  # one launch for the block
         if stream is None:
             torch.cuda.current_stream().synchronize()
         elif isinstance(stream, int):

@@ -232,28 +232,87 @@ tlq_status tl_unpack_weights(const uint32_t* Wpacked, uint8_t* codes, int N, int
   return launch_unpack(Wpacked, codes, N, K, bits, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// Validation of one re-quantization problem against itself.
+tlq_status check_requant(const tl_requant_desc& d, int group, const char* who, int idx) {
+  if (!d.W4 || !d.s4 || !d.z4 || !d.W2 || !d.s2 || !d.z2) return set_error(TLQ_EINVAL, "%s[%d]: null pointer", who, idx);
+  if (d.N < 1 || d.K < 1) return set_error(TLQ_EINVAL, "%s[%d]: N=%d K=%d must be >= 1", who, idx, d.N, d.K);
+  if (d.K % group) return set_error(TLQ_EINVAL, "%s[%d]: group=%d does not divide K=%d", who, idx, group, d.K);
+  if (!aligned16(d.W4) || !aligned16(d.W2))
+    return set_error(TLQ_EINVAL, "%s[%d]: W4 and W2 must be 16-byte aligned", who, idx);
+  if ((reinterpret_cast<uintptr_t>(d.s4) | reinterpret_cast<uintptr_t>(d.z4) | reinterpret_cast<uintptr_t>(d.s2) |
+       reinterpret_cast<uintptr_t>(d.z2)) & 1u)
+    return set_error(TLQ_EINVAL, "%s[%d]: scales/zeros must be 2-byte aligned", who, idx);
+  return TLQ_OK;
+}
+
+struct RqRegion {
+  const void* p;
+  size_t n;
+  int prob;
+  int kind;  // 0 W4, 1 s4, 2 z4, 3 W2, 4 s2, 5 z2
+};
+
+// Outputs (W2, s2, z2) may overlap nothing, except that s2 / z2 may be
+// exactly the s4 / z4 of the same problem.  Inputs may overlap each other.
+tlq_status check_requant_overlaps(const tl_requant_desc* d, int count, int group, const char* who) {
+  RqRegion r[6 * kMaxRequantProblems];
+  int n = 0;
+  for (int i = 0; i < count; ++i) {
+    const size_t b4 = (size_t)d[i].N * d[i].K / 2, b2 = (size_t)d[i].N * d[i].K / 4;
+    const size_t bg = (size_t)d[i].N * (d[i].K / group) * 2;
+    r[n++] = {d[i].W4, b4, i, 0};
+    r[n++] = {d[i].s4, bg, i, 1};
+    r[n++] = {d[i].z4, bg, i, 2};
+    r[n++] = {d[i].W2, b2, i, 3};
+    r[n++] = {d[i].s2, bg, i, 4};
+    r[n++] = {d[i].z2, bg, i, 5};
+  }
+  for (int a = 0; a < n; ++a) {
+    if (r[a].kind < 3) continue;  // every pair with at least one output
+    for (int b = 0; b < n; ++b) {
+      if (b == a || (r[b].kind >= 3 && b < a)) continue;
+      if (!overlaps(r[a].p, r[a].n, r[b].p, r[b].n)) continue;
+      const bool same_prob = r[a].prob == r[b].prob;
+      if (same_prob && r[a].p == r[b].p && r[a].n == r[b].n && r[a].kind - r[b].kind == 3 && r[b].kind >= 1)
+        continue;  // s2 == s4 or z2 == z4: converted in place
+      static const char* names[6] = {"W4", "s4", "z4", "W2", "s2", "z2"};
+      return set_error(TLQ_EINVAL, "%s: %s of problem %d overlaps %s of problem %d", who, names[r[a].kind], r[a].prob,
+                       names[r[b].kind], r[b].prob);
+    }
+  }
+  return TLQ_OK;
+}
+
+tlq_status requant(const tl_requant_desc* d, int count, int group, void* stream, const char* who) {
+  if (count < 0 || count > kMaxRequantProblems)
+    return set_error(TLQ_EINVAL, "%s: count=%d (0..%d)", who, count, kMaxRequantProblems);
+  if (count > 0 && !d) return set_error(TLQ_EINVAL, "%s: null descriptor array", who);
+  if (group < 64 || group % 64)
+    return set_error(TLQ_EINVAL, "%s: group=%d must be a multiple of 64 (the INT2 kernels' rule)", who, group);
+  for (int i = 0; i < count; ++i) {
+    tlq_status st = check_requant(d[i], group, who, i);
+    if (st != TLQ_OK) return st;
+  }
+  tlq_status st = check_requant_overlaps(d, count, group, who);
+  if (st != TLQ_OK) return st;
+  if (count == 0) return TLQ_OK;
+  RequantArgs a[kMaxRequantProblems];
+  for (int i = 0; i < count; ++i) a[i] = RequantArgs{d[i].W4, d[i].s4, d[i].z4, d[i].W2, d[i].s2, d[i].z2, d[i].N, d[i].K};
+  return launch_requant(a, count, group, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
 tlq_status tl_requant_int4_to_int2(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, uint32_t* W2,
                                    uint16_t* s2, uint16_t* z2, int N, int K, int group, void* stream) {
   g_msg[0] = 0;
-  if (!W4 || !s4 || !z4 || !W2 || !s2 || !z2) return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: null pointer");
-  if (N < 1 || K < 1) return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: N=%d K=%d must be >= 1", N, K);
-  if (group < 64 || group % 64 || K % group)
-    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: group=%d must be a multiple of 64 dividing K=%d", group, K);
-  if (!aligned16(W4) || !aligned16(W2))
-    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: W4 and W2 must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(s4) | reinterpret_cast<uintptr_t>(z4) | reinterpret_cast<uintptr_t>(s2) |
-       reinterpret_cast<uintptr_t>(z2)) & 1u)
-    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: scales/zeros must be 2-byte aligned");
-  const size_t b4 = (size_t)N * K / 2, b2 = (size_t)N * K / 4, bg = (size_t)N * (K / group) * 2;
-  if (overlaps(W2, b2, W4, b4) || overlaps(W2, b2, s4, bg) || overlaps(W2, b2, z4, bg) ||
-      overlaps(W2, b2, s2, bg) || overlaps(W2, b2, z2, bg))
-    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: W2 overlaps another argument");
-  if (overlaps(s2, bg, W4, b4) || overlaps(z2, bg, W4, b4) || overlaps(s2, bg, z2, bg))
-    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: s2/z2 overlap W4 or each other");
-  if ((s2 != s4 && (overlaps(s2, bg, s4, bg) || overlaps(s2, bg, z4, bg))) ||
-      (z2 != z4 && (overlaps(z2, bg, z4, bg) || overlaps(z2, bg, s4, bg))))
-    return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: s2 / z2 must equal s4 / z4 exactly or not overlap them");
-  return launch_requant(W4, s4, z4, W2, s2, z2, N, K, group, static_cast<cudaStream_t>(stream));
+  const tl_requant_desc d = {W4, s4, z4, W2, s2, z2, N, K};
+  return requant(&d, 1, group, stream, "tl_requant_int4_to_int2");
+}
+
+tlq_status tl_requant_int4_to_int2_batched(const tl_requant_desc* descs, int count, int group, void* stream) {
+  g_msg[0] = 0;
+  return requant(descs, count, group, stream, "tl_requant_int4_to_int2_batched");
 }
 
 tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void* stream_) {

@@ -333,8 +333,19 @@ tlq_status launch_decode(const GemmArgs* a, int count, cudaStream_t stream);
 tlq_status launch_prefill(const GemmArgs& a, cudaStream_t stream);
 tlq_status launch_pack(const uint8_t* codes, uint32_t* W, int N, int K, int bits, cudaStream_t stream);
 tlq_status launch_unpack(const uint32_t* W, uint8_t* codes, int N, int K, int bits, cudaStream_t stream);
-tlq_status launch_requant(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, uint32_t* W2, uint16_t* s2,
-                          uint16_t* z2, int N, int K, int group, cudaStream_t stream);
+// INT4 -> INT2 re-quantization of up to kMaxRequantProblems weights sharing
+// one group size, in one persistent launch.
+constexpr int kMaxRequantProblems = 16;
+struct RequantArgs {
+  const uint32_t* W4;
+  const uint16_t* s4;
+  const uint16_t* z4;
+  uint32_t* W2;
+  uint16_t* s2;
+  uint16_t* z2;
+  int N, K;
+};
+tlq_status launch_requant(const RequantArgs* a, int count, int group, cudaStream_t stream);
 tlq_status launch_rmsnorm(const float* x, __half* h, int M, int D, int normalize, cudaStream_t stream);
 tlq_status launch_timeout_probe(uint32_t limit_us, cudaStream_t stream);
 

@@ -9,22 +9,27 @@
 // Every floating-point step is binary32 with round-to-nearest-even, in that
 // order, so the codes, s2 and z2 are bit-identical to a scalar evaluation.
 //
-// Two facts make the kernel a byte-SIMD stream instead of a per-weight divide:
-//  * inside a group, w depends on the 4-bit code only, and c -> w(c) is
-//    monotone (each rounded step is monotone; the direction is the sign of
-//    s4).  So min/max of w over the group are w(cmin) and w(cmax), and
-//  * q2(c) = f(w(c)) is monotone in c as well, so it is fixed by three integer
-//    thresholds C_j = #{c in 0..15 : q2(c) < j}: q2 >= j iff c' >= C_j, with
-//    c' = c (s4 > 0) or 15 - c (s4 < 0).  The 16 values q2(c) are evaluated
-//    with the exact scalar formula, spread over the lanes of the group.
+// Inside a group w depends on the 4-bit code only, so the kernel evaluates the
+// exact scalar formula for the 16 codes once per group and then maps codes
+// with a table, not a divide per weight:
+//  * c -> w(c) is monotone (each rounded step is monotone; the direction is
+//    the sign of s4), so min/max of w over the group are w(cmin) and w(cmax)
+//    of the smallest and largest code present;
+//  * the table q2(c), c = 0..15, is held in four registers as byte pools of
+//    two byte permutes (see rq_pack16), which translate four codes each.
 // The one exception to monotonicity is s4 = +-0: every w is a zero whose sign
 // follows (c - z4), and the scalar min/max keep the group's first weight; the
 // kernel then takes the first code of the group.
 //
-// Layout: the [N][K] codes are viewed as N*K/group consecutive groups (K is a
-// multiple of group).  A group of `group` codes is T = group/32 chunks of 32
-// codes (16 bytes of INT4 in, 8 bytes of INT2 out); P lanes (a power of two,
-// P >= T up to 32) work on one group, lane l on chunks l, l+P, ...
+// Layout: the [N][K] codes of a weight are N*K/group consecutive groups (K is
+// a multiple of group); the groups of all weights of one launch are numbered
+// one after the other.  One thread converts one group: T = group/32 chunks of
+// 32 codes (16 bytes of INT4 in, 8 bytes of INT2 out each), so a group's
+// per-group work (min/max reduction, two divides for s2 / z2, sixteen for the
+// code map) is done once, without shuffles.  The grid is persistent (the
+// resident CTAs of every SM, one launch for all weights): each thread strides
+// over the groups and, for group sizes up to 128, loads its next group's
+// words before it converts the current one.
 #include "common.cuh"
 
 namespace tlq {
@@ -47,84 +52,130 @@ __device__ __forceinline__ uint32_t rq_code(float w, float sh, float zh) {
   return static_cast<uint32_t>(r);
 }
 
-// Byte-wise min / max accumulation of the 8 codes of one INT4 word.
-__device__ __forceinline__ void rq_minmax(uint32_t x, uint32_t& mn, uint32_t& mx) {
-  const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
-  mn = __vminu4(mn, __vminu4(lo, hi));
-  mx = __vmaxu4(mx, __vmaxu4(lo, hi));
+// Byte-wise compare of two vectors of bytes 0..15: 0xFF where a >= b, else 0.
+// (a | 0x80) - b keeps every byte in 0x71..0x8F (no borrow between bytes) and
+// sets its bit 7 exactly when a >= b; a byte permute in sign mode widens it.
+__device__ __forceinline__ uint32_t rq_ge_mask(uint32_t a, uint32_t b) {
+  uint32_t m;
+  // prmt selector nibbles 8..B: bytes 0..3 of the source, each replaced by
+  // copies of its sign bit (PTX "prmt", default mode)
+  asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(m) : "r"((a | 0x80808080u) - b));
+  return m;
 }
 
-// The 8 codes of one INT4 word -> 16 bits of INT2 codes (code j at bits 2j).
-// b1..b3 hold (0x80 - C_j) in every byte: adding one to a byte of codes 0..15
-// sets its bit 7 exactly when the code is >= C_j, with no carry out of the
-// byte.  The three tests form a thermometer (C1 <= C2 <= C3), so q2's bit 1
-// is test 2 and its bit 0 the parity of the three.
-__device__ __forceinline__ uint32_t rq_pack8(uint32_t x, uint32_t flip, uint32_t b1, uint32_t b2, uint32_t b3) {
-  const uint32_t lo = (x & 0x0F0F0F0Fu) ^ flip;          // codes 0, 2, 4, 6 (byte i = code 2i)
-  const uint32_t hi = ((x >> 4) & 0x0F0F0F0Fu) ^ flip;   // codes 1, 3, 5, 7
-  const uint32_t l1 = lo + b1, l2 = lo + b2, l3 = lo + b3;
-  const uint32_t h1 = hi + b1, h2 = hi + b2, h3 = hi + b3;
-  const uint32_t L0 = (l1 ^ l2 ^ l3) & 0x80808080u, L1 = l2 & 0x80808080u;
-  const uint32_t H0 = (h1 ^ h2 ^ h3) & 0x80808080u, H1 = h2 & 0x80808080u;
-  // byte i: bits 0..3 = q2(code 2i) | q2(code 2i+1) << 2
-  uint32_t n = (L0 >> 7) | (L1 >> 6) | (H0 >> 5) | (H1 >> 4);
-  n = (n | (n >> 4)) & 0x00FF00FFu;
-  return (n | (n >> 8)) & 0x0000FFFFu;
+// Byte-wise min and max of two vectors of bytes 0..15.
+__device__ __forceinline__ void rq_minmax2(uint32_t a, uint32_t b, uint32_t& mn, uint32_t& mx) {
+  const uint32_t m = rq_ge_mask(a, b);
+  mx = b ^ ((a ^ b) & m);
+  mn = a ^ ((a ^ b) & m);
+}
+__device__ __forceinline__ uint32_t rq_min(uint32_t a, uint32_t b) { return a ^ ((a ^ b) & rq_ge_mask(a, b)); }
+__device__ __forceinline__ uint32_t rq_max(uint32_t a, uint32_t b) { return b ^ ((a ^ b) & rq_ge_mask(a, b)); }
+
+// Byte-wise min and max over the 32 codes of one chunk (4 INT4 words).
+__device__ __forceinline__ void rq_chunk_minmax(const uint4& v, uint32_t& mn, uint32_t& mx) {
+  uint32_t n0, x0, n1, x1, n2, x2, n3, x3;
+  rq_minmax2(v.x & 0x0F0F0F0Fu, (v.x >> 4) & 0x0F0F0F0Fu, n0, x0);
+  rq_minmax2(v.y & 0x0F0F0F0Fu, (v.y >> 4) & 0x0F0F0F0Fu, n1, x1);
+  rq_minmax2(v.z & 0x0F0F0F0Fu, (v.z >> 4) & 0x0F0F0F0Fu, n2, x2);
+  rq_minmax2(v.w & 0x0F0F0F0Fu, (v.w >> 4) & 0x0F0F0F0Fu, n3, x3);
+  mn = rq_min(rq_min(n0, n1), rq_min(n2, n3));
+  mx = rq_max(rq_max(x0, x1), rq_max(x2, x3));
 }
 
-// ONE: every lane holds at most one chunk (T <= 32), kept in registers
-// between the two passes; otherwise lanes loop and re-read their chunks.
-template <bool ONE>
-__global__ void __launch_bounds__(kRqThreads) requant_kernel(const uint4* __restrict__ W4,
-                                                             const uint16_t* s4, const uint16_t* z4,
-                                                             uint2* __restrict__ W2, uint16_t* s2, uint16_t* z2,
-                                                             long long ngroups, int T, int lg2P) {
-  const int P = 1 << lg2P;
-  const long long t = static_cast<long long>(blockIdx.x) * kRqThreads + threadIdx.x;
-  const long long gi = t >> lg2P;
-  if (gi >= ngroups) return;  // whole P-lane sets leave together (P divides 32)
-  const int l = static_cast<int>(t & (P - 1));
-  const int lane = threadIdx.x & 31;
-  const int leader = lane & ~(P - 1);
-  const unsigned mask = P == 32 ? 0xffffffffu : (((1u << P) - 1u) << leader);
-  const uint4* src = W4 + gi * T;
+// Byte permute (PTX prmt, default mode): byte i of the result is byte
+// (sel_i & 7) of {lo, hi} (lo = bytes 0..3), or copies of that byte's bit 7
+// when sel_i & 8.  sel_i is nibble i of `sel`, so the low 16 bits of an INT4
+// word select with its first four codes.
+__device__ __forceinline__ uint32_t rq_prmt(uint32_t lo, uint32_t hi, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(sel));
+  return r;
+}
 
-  // Lane 0 of the set reads s4 / z4 (and later writes s2 / z2, which may
-  // alias them); the others receive the values by shuffle.
-  uint32_t sz = 0, first = 0;
-  uint4 v = make_uint4(0, 0, 0, 0);
-  uint32_t mn = 0x0F0F0F0Fu, mx = 0u;
-  if (ONE) {
-    if (l < T) {
-      v = __ldg(src + l);
-      rq_minmax(v.x, mn, mx);
-      rq_minmax(v.y, mn, mx);
-      rq_minmax(v.z, mn, mx);
-      rq_minmax(v.w, mn, mx);
+// Code table as byte pools.  For code c < 8: byte c of pool A holds bit 0 of
+// q2(c) in bit 0, byte c of pool B bit 1 of q2(c) in bit 1.  For c >= 8 the
+// selector nibble has bit 3 set, the permute copies bit 7 of byte c - 8, and
+// that bit holds bit 0 (pool A) or bit 1 (pool B) of q2(c).  So for every
+// code, (A & 1) | (B & 2) of its result byte is q2(c).
+struct RqPools {
+  uint32_t a0, a1, b0, b1;
+};
+
+// Four codes (the low 16 bits of sel) -> bytes q2(c_i), i = 0..3.
+__device__ __forceinline__ uint32_t rq_lookup4(const RqPools& t, uint32_t sel) {
+  return (rq_prmt(t.a0, t.a1, sel) & 0x01010101u) | (rq_prmt(t.b0, t.b1, sel) & 0x02020202u);
+}
+
+// Bytes q_0..q_3 (each 0..3) -> q_0 | q_1 << 2 | q_2 << 4 | q_3 << 6 in the
+// top byte: the multiplier moves byte i (bit 8i) up by 24 - 6i; the other
+// products land above bit 31 or sum to less than 2^24 below bit 24.
+__device__ __forceinline__ uint32_t rq_compact4(uint32_t r) { return r * 0x01041040u; }
+
+// Two INT4 words (16 codes) -> one INT2 word, code j at bits 2j.
+__device__ __forceinline__ uint32_t rq_pack16(uint32_t x0, uint32_t x1, const RqPools& t) {
+  const uint32_t m0 = rq_compact4(rq_lookup4(t, x0)), m1 = rq_compact4(rq_lookup4(t, x0 >> 16));
+  const uint32_t m2 = rq_compact4(rq_lookup4(t, x1)), m3 = rq_compact4(rq_lookup4(t, x1 >> 16));
+  return __byte_perm(__byte_perm(m0, m1, 0x0073), __byte_perm(m2, m3, 0x0073), 0x5410);
+}
+
+// One weight of a launch; gstart = number of groups of the weights before it.
+struct RqProblem {
+  const uint4* W4;
+  const uint16_t* s4;
+  const uint16_t* z4;
+  uint2* W2;
+  uint16_t* s2;
+  uint16_t* z2;
+  long long gstart;
+};
+
+struct RqLaunch {
+  RqProblem p[kMaxRequantProblems];
+  int count;
+  long long ngroups;  // all weights
+  int T;  // chunks of 32 codes per group
+};
+
+// The problem holding group g, at or after problem p (groups are visited in
+// increasing order by each thread).
+__device__ __forceinline__ int rq_advance(const RqLaunch& L, int p, long long g) {
+#pragma unroll 1
+  while (p + 1 < L.count && g >= L.p[p + 1].gstart) ++p;
+  return p;
+}
+
+// Converts one group held in v[0..TC) (TC > 0) or re-read from src (TC == 0,
+// T chunks).  sz = s4 | z4 << 16.
+template <int TC>
+__device__ __forceinline__ void rq_group(const uint4* v, const uint4* __restrict__ src, int T, uint32_t sz,
+                                         uint2* __restrict__ dst, uint16_t* s2, uint16_t* z2) {
+  const int nch = TC > 0 ? TC : T;
+  uint32_t mn = 0x0F0F0F0Fu, mx = 0u, first;
+  if (TC > 0) {
+#pragma unroll
+    for (int i = 0; i < (TC > 0 ? TC : 1); ++i) {
+      uint32_t a, b;
+      rq_chunk_minmax(v[i], a, b);
+      mn = rq_min(mn, a);
+      mx = rq_max(mx, b);
     }
+    first = v[0].x & 15u;
   } else {
-    for (int ch = l; ch < T; ch += P) {
-      const uint4 u = __ldg(src + ch);
-      if (ch == 0) v = u;
-      rq_minmax(u.x, mn, mx);
-      rq_minmax(u.y, mn, mx);
-      rq_minmax(u.z, mn, mx);
-      rq_minmax(u.w, mn, mx);
+    first = __ldg(reinterpret_cast<const uint32_t*>(src)) & 15u;
+#pragma unroll 1
+    for (int i = 0; i < nch; ++i) {
+      uint32_t a, b;
+      rq_chunk_minmax(__ldg(src + i), a, b);
+      mn = rq_min(mn, a);
+      mx = rq_max(mx, b);
     }
   }
-  if (l == 0) {
-    sz = static_cast<uint32_t>(s4[gi]) | (static_cast<uint32_t>(z4[gi]) << 16);
-    first = v.x & 15u;
-  }
-  // cmin in byte 0, 15 - cmax in byte 1: one byte-wise min reduction.
-  uint32_t cmn = min(min(mn & 0xFFu, (mn >> 8) & 0xFFu), min((mn >> 16) & 0xFFu, mn >> 24));
-  uint32_t cmx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
-  uint32_t red = cmn | ((15u - cmx) << 8);
-  for (int o = P >> 1; o > 0; o >>= 1) red = __vminu4(red, __shfl_xor_sync(mask, red, o));
-  cmn = red & 0xFFu;
-  cmx = 15u - ((red >> 8) & 0xFFu);
-  sz = __shfl_sync(mask, sz, leader);
-  first = __shfl_sync(mask, first, leader);
+  mn = rq_min(mn, mn >> 16);
+  mn = rq_min(mn, mn >> 8);
+  mx = rq_max(mx, mx >> 16);
+  mx = rq_max(mx, mx >> 8);
+  const uint32_t cmn = mn & 0xFFu, cmx = mx & 0xFFu;
 
   const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(sz & 0xFFFFu)));
   const float z = __half2float(__ushort_as_half(static_cast<unsigned short>(sz >> 16)));
@@ -142,55 +193,117 @@ __global__ void __launch_bounds__(kRqThreads) requant_kernel(const uint4* __rest
   const __half zb = __float2half_rn(__fdiv_rn(-lo, sh));
   const float zh = __half2float(zb);
 
-  // Threshold counts C_j = #{c : q2(c) < j}, one byte each, summed over lanes.
-  uint32_t cnt = 0;
-  for (uint32_t c = static_cast<uint32_t>(l); c < 16u; c += static_cast<uint32_t>(P)) {
+  // The code table: q2(c) for c = 0..15 with the scalar formula.
+  RqPools t = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (uint32_t c = 0; c < 16u; ++c) {
     const uint32_t q = rq_code(rq_dequant(c, z, s), sh, zh);
-    cnt += (q < 1u ? 1u : 0u) | (q < 2u ? 0x100u : 0u) | (q < 3u ? 0x10000u : 0u);
-  }
-  for (int o = P >> 1; o > 0; o >>= 1) cnt += __shfl_xor_sync(mask, cnt, o);
-  const uint32_t b1 = (0x80u - (cnt & 0xFFu)) * 0x01010101u;
-  const uint32_t b2 = (0x80u - ((cnt >> 8) & 0xFFu)) * 0x01010101u;
-  const uint32_t b3 = (0x80u - ((cnt >> 16) & 0xFFu)) * 0x01010101u;
-  const uint32_t flip = s < 0.0f ? 0x0F0F0F0Fu : 0u;
-
-  uint2* dst = W2 + gi * T;
-  if (ONE) {
-    if (l < T)
-      dst[l] = make_uint2(rq_pack8(v.x, flip, b1, b2, b3) | (rq_pack8(v.y, flip, b1, b2, b3) << 16),
-                          rq_pack8(v.z, flip, b1, b2, b3) | (rq_pack8(v.w, flip, b1, b2, b3) << 16));
-  } else {
-    for (int ch = l; ch < T; ch += P) {
-      const uint4 u = __ldg(src + ch);
-      dst[ch] = make_uint2(rq_pack8(u.x, flip, b1, b2, b3) | (rq_pack8(u.y, flip, b1, b2, b3) << 16),
-                           rq_pack8(u.z, flip, b1, b2, b3) | (rq_pack8(u.w, flip, b1, b2, b3) << 16));
+    const uint32_t sft = 8u * (c & 3u) + (c < 8u ? 0u : 7u);
+    const uint32_t qa = (q & 1u) << sft, qb = (c < 8u ? (q & 2u) : (q >> 1)) << sft;
+    if ((c & 7u) < 4u) {
+      t.a0 |= qa;
+      t.b0 |= qb;
+    } else {
+      t.a1 |= qa;
+      t.b1 |= qb;
     }
   }
-  if (l == 0) {
-    s2[gi] = __half_as_ushort(sb);
-    z2[gi] = __half_as_ushort(zb);
+
+  if (TC > 0) {
+#pragma unroll
+    for (int i = 0; i < (TC > 0 ? TC : 1); ++i)
+      dst[i] = make_uint2(rq_pack16(v[i].x, v[i].y, t), rq_pack16(v[i].z, v[i].w, t));
+  } else {
+#pragma unroll 1
+    for (int i = 0; i < nch; ++i) {
+      const uint4 u = __ldg(src + i);
+      dst[i] = make_uint2(rq_pack16(u.x, u.y, t), rq_pack16(u.z, u.w, t));
+    }
+  }
+  *s2 = __half_as_ushort(sb);
+  *z2 = __half_as_ushort(zb);
+}
+
+// TC = chunks per group known at compile time (2: group 64, 4: group 128),
+// with the next group prefetched; 0 = any group size, chunks re-read.
+template <int TC>
+__global__ void __launch_bounds__(kRqThreads, 3) requant_kernel(const __grid_constant__ RqLaunch L) {
+  const long long stride = static_cast<long long>(gridDim.x) * kRqThreads;
+  long long g = static_cast<long long>(blockIdx.x) * kRqThreads + threadIdx.x;
+  if (g >= L.ngroups) return;
+  const int T = TC > 0 ? TC : L.T;
+  int p = rq_advance(L, 0, g);
+  constexpr int NV = TC > 0 ? TC : 1;
+  uint4 vn[NV];
+  uint32_t szn = 0;
+  int pn = p;
+  if (TC > 0) {
+    const long long gl = g - L.p[p].gstart;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) vn[i] = __ldg(L.p[p].W4 + gl * T + i);
+    szn = static_cast<uint32_t>(L.p[p].s4[gl]) | (static_cast<uint32_t>(L.p[p].z4[gl]) << 16);
+  }
+#pragma unroll 1
+  for (; g < L.ngroups; g += stride) {
+    const RqProblem& pr = L.p[p];
+    const long long gi = g - pr.gstart;
+    uint4 v[NV];
+    uint32_t sz;
+    if (TC > 0) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = vn[i];
+      sz = szn;
+      const long long gn = g + stride;
+      if (gn < L.ngroups) {  // the next group's words are in flight during this one
+        pn = rq_advance(L, p, gn);
+        const long long gl = gn - L.p[pn].gstart;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) vn[i] = __ldg(L.p[pn].W4 + gl * T + i);
+        szn = static_cast<uint32_t>(L.p[pn].s4[gl]) | (static_cast<uint32_t>(L.p[pn].z4[gl]) << 16);
+      }
+    } else {
+      sz = static_cast<uint32_t>(pr.s4[gi]) | (static_cast<uint32_t>(pr.z4[gi]) << 16);
+    }
+    // s4 / z4 of this group were read above, before s2 / z2 (which may alias
+    // them) are written.
+    rq_group<TC>(v, pr.W4 + gi * T, T, sz, pr.W2 + gi * T, pr.s2 + gi, pr.z2 + gi);
+    if (TC > 0) p = pn;
+    else if (g + stride < L.ngroups) p = rq_advance(L, p, g + stride);
   }
 }
 
 }  // namespace
 
-tlq_status launch_requant(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, uint32_t* W2, uint16_t* s2,
-                          uint16_t* z2, int N, int K, int group, cudaStream_t stream) {
-  const long long ngroups = static_cast<long long>(N) * (K / group);
-  const int T = group / 32;
-  int lg2P = 0;
-  while ((1 << lg2P) < T && lg2P < 5) ++lg2P;
-  const long long threads = ngroups << lg2P;
-  const long long blocks = (threads + kRqThreads - 1) / kRqThreads;
-  if (blocks > 0x7fffffffLL) return set_error(TLQ_EINVAL, "tl_requant_int4_to_int2: N*K too large");
-  const uint4* src = reinterpret_cast<const uint4*>(W4);
-  uint2* dst = reinterpret_cast<uint2*>(W2);
-  if (T <= 32)
-    requant_kernel<true><<<static_cast<unsigned>(blocks), kRqThreads, 0, stream>>>(src, s4, z4, dst, s2, z2, ngroups,
-                                                                                   T, lg2P);
+tlq_status launch_requant(const RequantArgs* a, int count, int group, cudaStream_t stream) {
+  RqLaunch L = {};
+  long long g = 0;
+  for (int i = 0; i < count; ++i) {
+    L.p[i] = RqProblem{reinterpret_cast<const uint4*>(a[i].W4), a[i].s4, a[i].z4, reinterpret_cast<uint2*>(a[i].W2),
+                       a[i].s2, a[i].z2, g};
+    g += static_cast<long long>(a[i].N) * (a[i].K / group);
+  }
+  L.count = count;
+  L.ngroups = g;
+  L.T = group / 32;
+  if (g == 0) return TLQ_OK;
+  const int kind = L.T == 4 ? 2 : (L.T == 2 ? 1 : 0);
+  // persistent: the resident CTAs of every SM, fewer when there is less work
+  static int occ[3] = {0, 0, 0};
+  int& o = occ[kind];
+  if (o == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &o, kind == 2 ? requant_kernel<4> : (kind == 1 ? requant_kernel<2> : requant_kernel<0>), kRqThreads, 0);
+    if (e != cudaSuccess || o < 1) o = 1;
+  }
+  const long long want = (g + kRqThreads - 1) / kRqThreads;
+  const long long cap = static_cast<long long>(device_info().sms) * o;
+  const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
+  if (kind == 2)
+    requant_kernel<4><<<blocks, kRqThreads, 0, stream>>>(L);
+  else if (kind == 1)
+    requant_kernel<2><<<blocks, kRqThreads, 0, stream>>>(L);
   else
-    requant_kernel<false><<<static_cast<unsigned>(blocks), kRqThreads, 0, stream>>>(src, s4, z4, dst, s2, z2, ngroups,
-                                                                                    T, lg2P);
+    requant_kernel<0><<<blocks, kRqThreads, 0, stream>>>(L);
   return cuda_error(cudaGetLastError(), "requant: launch");
 }
 
