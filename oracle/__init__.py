@@ -22,6 +22,13 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   rms_norm_half                    closed forms (constant rows, scale invariance)
   loop_block                       brute force on tiny shapes, closed form
                                    (zero update), split-iteration invariant
+  swiglu                           closed forms (g = 0, u = 0, large |g|),
+                                   the identity silu(g) - silu(-g) = g,
+                                   agreement with scipy's logistic function
+  loop_block_swiglu                closed form (zero gate or zero up: no
+                                   update), reduction to the bilinear block
+                                   g * u when the gate output is large,
+                                   split-iteration invariant
   requant_int4_to_int2             closed forms (a 4-level group, a constant
                                    group), per-weight error bound, and the
                                    page's test: error within 2x of direct
@@ -78,6 +85,8 @@ def _load():
                 "orc_rms_norm_half": [P, I, I, ctypes.c_double, P],
                 "orc_loop_block": [P, I, I, I, P, P, P, P, I, I, I, I, ctypes.c_double],
                 "orc_requant_int4_to_int2": [P, P, P, I, I, I, P, P, P],
+                "orc_swiglu": [P, P, P, ctypes.c_size_t],
+                "orc_loop_block_swiglu": [P, I, I, I, P, P, P, P, P, I, I, I, I, ctypes.c_double],
             }.items():
                 f = getattr(lib, name)
                 f.restype = ctypes.c_int
@@ -220,6 +229,45 @@ def loop_block(x: np.ndarray, block: dict, bits: int, group: int, L: int, normal
     rc = _load().orc_loop_block(_ptr(x), M, D, F, *[ctypes.byref(p) for p in projs], bits, group,
                                 L, 1 if normalize else 0, eps)
     _check(rc, "loop_block")
+    return x
+
+
+# ----------------------------------------------------------------------------
+# SwiGLU feed-forward of the five-weight loop block: "Model", ffn_dim (the
+# width of the gate and up projections); beta-Informed Deployment Features,
+# CTX-TIER, Phase 2b (attn_qkv, attn_out, mlp_gate, mlp_up, mlp_down).
+# ----------------------------------------------------------------------------
+
+def swiglu(g, u) -> np.ndarray:
+    """fp16(silu(g) * u) element-wise for FP16 arrays g, u (binary64 inside)."""
+    g = _half_bits(g)
+    u = _half_bits(u)
+    assert g.shape == u.shape
+    out = np.empty(g.shape, dtype=np.uint16)
+    _check(_load().orc_swiglu(_ptr(g), _ptr(u), _ptr(out), g.size), "swiglu")
+    return out.view(np.float16)
+
+
+def loop_block_swiglu(x: np.ndarray, block: dict, bits: int, group: int, L: int, normalize: bool = True,
+                      eps: float = EPS) -> np.ndarray:
+    """The five-weight SwiGLU block L times on a copy of x (FP32 [M][D]).
+
+    ``block`` maps "qkv", "o", "gate", "up", "down" to (W packed, scales,
+    zeros)."""
+    x = np.array(x, dtype=np.float32, order="C", copy=True)
+    M, D = x.shape
+    F = block["up"][0].shape[0]
+    keep = []
+    projs = []
+    for name in ("qkv", "o", "gate", "up", "down"):
+        W, s, z = block[name]
+        W = np.ascontiguousarray(W, dtype=np.uint32)
+        s, z = _half_bits(s), _half_bits(z)
+        keep += [W, s, z]
+        projs.append(_Proj(_ptr(W), _ptr(s), _ptr(z)))
+    rc = _load().orc_loop_block_swiglu(_ptr(x), M, D, F, *[ctypes.byref(p) for p in projs], bits, group,
+                                       L, 1 if normalize else 0, eps)
+    _check(rc, "loop_block_swiglu")
     return x
 
 

@@ -32,6 +32,10 @@
  *    norm); qkv = Q(h); o = Q(qkv[:, :D]); u = relu(Q(o)); x += float(Q(u)),
  *    every GEMM output rounded to FP16, the residual add done in FP32.
  *    relu(v) = v if v > 0 else +0.
+ *  - SwiGLU loop block (five weights: qkv, o, gate, up, down): as above up
+ *    to o, then g = Q_gate(o), u = Q_up(o) (FP16 GEMM outputs) and
+ *    a = fp16_RNE(silu(g) * u) with silu(g) = g / (1 + exp(-g)) evaluated in
+ *    binary64 on the FP16 values; x += float(Q_down(a)).
  */
 #include <math.h>
 #include <stdint.h>
@@ -279,6 +283,69 @@ int orc_loop_block(float* x, int M, int D, int F, const orc_proj* qkv, const orc
   free(q);
   free(ob);
   free(u);
+  free(d);
+  return rc;
+}
+
+/* ------------------------------------------------------------------ */
+/* SwiGLU: the gated feed-forward of the five-weight loop block         */
+/* ------------------------------------------------------------------ */
+
+/* "Model", ffn_dim: "For SwiGLU this is the width of the gate and up
+ * projections"; the five loop-block weights attn_qkv, attn_out, mlp_gate,
+ * mlp_up, mlp_down ("beta-Informed Deployment Features", CTX-TIER, Phase 2b).
+ * out[i] = fp16_RNE( g * u / (1 + exp(-g)) ) in binary64, g and u FP16. */
+int orc_swiglu(const uint16_t* g, const uint16_t* u, uint16_t* out, size_t n) {
+  for (size_t i = 0; i < n; ++i) {
+    const double gv = orc_half_to_double(g[i]);
+    const double uv = orc_half_to_double(u[i]);
+    const double silu = gv / (1.0 + exp(-gv));
+    out[i] = orc_double_to_half(silu * uv);
+  }
+  return 0;
+}
+
+/* x[M][D] (FP32, updated in place) <- L applications of the SwiGLU block
+ * {qkv: [3D x D], o: [D x D], gate: [F x D], up: [F x D], down: [D x F]}. */
+int orc_loop_block_swiglu(float* x, int M, int D, int F, const orc_proj* qkv, const orc_proj* o,
+                          const orc_proj* gate, const orc_proj* up, const orc_proj* down, int bits,
+                          int group, int L, int normalize, double eps) {
+  if (M < 0 || D <= 0 || F <= 0 || L < 0) return -1;
+  if (check_shape(3 * D, D, bits, group) || check_shape(F, D, bits, group) || check_shape(D, F, bits, group))
+    return -1;
+  size_t nh = (size_t)M * D, nq = (size_t)M * 3 * D, nu = (size_t)M * F;
+  uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (nh ? nh : 1));
+  uint16_t* q = (uint16_t*)malloc(sizeof(uint16_t) * (nq ? nq : 1));
+  uint16_t* ob = (uint16_t*)malloc(sizeof(uint16_t) * (nh ? nh : 1));
+  uint16_t* gb = (uint16_t*)malloc(sizeof(uint16_t) * (nu ? nu : 1));
+  uint16_t* ub = (uint16_t*)malloc(sizeof(uint16_t) * (nu ? nu : 1));
+  uint16_t* ab = (uint16_t*)malloc(sizeof(uint16_t) * (nu ? nu : 1));
+  uint16_t* d = (uint16_t*)malloc(sizeof(uint16_t) * (nh ? nh : 1));
+  int rc = 0;
+  if (!h || !q || !ob || !gb || !ub || !ab || !d) rc = -2;
+  for (int l = 0; l < L && rc == 0; ++l) {
+    if (normalize) {
+      orc_rms_norm_half(x, M, D, eps, h);
+    } else {
+      for (size_t i = 0; i < nh; ++i) h[i] = orc_double_to_half((double)x[i]);
+    }
+    rc |= orc_quant_gemm(h, D, qkv->W, qkv->scales, qkv->zeros, q, 3 * D, M, 3 * D, D, bits, group);
+    rc |= orc_quant_gemm(q, 3 * D, o->W, o->scales, o->zeros, ob, D, M, D, D, bits, group);
+    rc |= orc_quant_gemm(ob, D, gate->W, gate->scales, gate->zeros, gb, F, M, F, D, bits, group);
+    rc |= orc_quant_gemm(ob, D, up->W, up->scales, up->zeros, ub, F, M, F, D, bits, group);
+    rc |= orc_swiglu(gb, ub, ab, nu);
+    rc |= orc_quant_gemm(ab, F, down->W, down->scales, down->zeros, d, D, M, D, F, bits, group);
+    for (size_t i = 0; i < nh; ++i) {
+      float dv = (float)orc_half_to_double(d[i]);
+      x[i] = x[i] + dv;
+    }
+  }
+  free(h);
+  free(q);
+  free(ob);
+  free(gb);
+  free(ub);
+  free(ab);
   free(d);
   return rc;
 }

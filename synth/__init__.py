@@ -76,3 +76,18 @@ def block_case(M: int, bits: int, group: int | None = None, seed: int = 0, D: in
         proj[name] = quant_weights(rng, N, K, bits, group)
     return dict(x0=x0, proj=proj, M=M, D=D, F=F, bits=bits,
                 group=DIST[bits]["group"] if group is None else group)
+
+
+def swiglu_block_case(M: int, bits: int, group: int | None = None, seed: int = 0, D: int = D_MODEL,
+                      F: int = FFN) -> dict:
+    """One five-weight SwiGLU loop-block problem: x0 and the shared
+    projections qkv, o, gate, up, down (same value distributions)."""
+    rng = rng_for(seed)
+    x0 = rng.standard_normal((M, D)).astype(np.float32)
+    shapes = {"qkv": (3 * D, D), "o": (D, D), "gate": (F, D), "up": (F, D), "down": (D, F)}
+    proj = {}
+    for name in ("qkv", "o", "gate", "up", "down"):
+        N, K = shapes[name]
+        proj[name] = quant_weights(rng, N, K, bits, group)
+    return dict(x0=x0, proj=proj, M=M, D=D, F=F, bits=bits,
+                group=DIST[bits]["group"] if group is None else group)

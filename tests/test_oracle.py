@@ -363,6 +363,118 @@ def test_loop_block_full_width_stays_finite(bits):
 # "Details of the shipped kernel")
 # ---------------------------------------------------------------------------
 
+# ---------------------------------------------------------------------------
+# SwiGLU feed-forward and the five-weight block
+# ---------------------------------------------------------------------------
+
+def _ulp16(v):
+    """Spacing of binary16 at |v| (subnormal spacing 2^-24 below 2^-14)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return 2.0 ** (e - 10)
+
+
+def test_swiglu_closed_forms():
+    """g = 0 or u = 0 give 0; g >= 20 gives fp16(g * u) (the gate is fully open); g <= -30 gives 0
+    (fully closed)."""
+    rng = np.random.default_rng(1)
+    u = rng.uniform(-100, 100, 256).astype(np.float16)
+    assert np.all(oracle.swiglu(np.zeros(256, np.float16), u).astype(np.float64) == 0.0)
+    g = rng.uniform(-100, 100, 256).astype(np.float16)
+    assert np.all(oracle.swiglu(g, np.zeros(256, np.float16)).astype(np.float64) == 0.0)
+    # powers of two for u keep g * u exact in FP16: the open gate returns it unchanged
+    gp = rng.uniform(20, 60, 256).astype(np.float16)
+    up = (2.0 ** rng.integers(-6, 6, 256)).astype(np.float16) * rng.choice([-1, 1], 256).astype(np.float16)
+    np.testing.assert_array_equal(oracle.swiglu(gp, up), (gp.astype(np.float64) * up).astype(np.float16))
+    gn = rng.uniform(-60, -30, 256).astype(np.float16)
+    assert np.all(oracle.swiglu(gn, u).astype(np.float64) == 0.0)
+
+
+def test_swiglu_odd_part_identity():
+    """silu(g) - silu(-g) = g exactly, so fp16(silu(g) u) - fp16(silu(-g) u) is g u within the two
+    roundings: a wrong sign in the exponent or a dropped factor breaks it."""
+    rng = np.random.default_rng(2)
+    g = rng.uniform(-8, 8, 4096).astype(np.float16)
+    u = rng.uniform(-4, 4, 4096).astype(np.float16)
+    ap = oracle.swiglu(g, u).astype(np.float64)
+    am = oracle.swiglu(-g, u).astype(np.float64)
+    exact = g.astype(np.float64) * u.astype(np.float64)
+    assert np.all(np.abs((ap - am) - exact) <= 0.5 * _ulp16(ap) + 0.5 * _ulp16(am) + 1e-12)
+
+
+def test_swiglu_against_scipy_logistic():
+    """silu(g) = g * expit(g) with scipy's logistic function, rounded once to FP16: equal except
+    where binary64 rounding lands on the other side of an FP16 tie (none expected here)."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(3)
+    g = (rng.standard_normal(20000) * 4).astype(np.float16)
+    u = (rng.standard_normal(20000) * 2).astype(np.float16)
+    ref = (g.astype(np.float64) * special.expit(g.astype(np.float64)) * u.astype(np.float64)).astype(np.float16)
+    got = oracle.swiglu(g, u)
+    diff = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    assert np.all(diff <= _ulp16(ref))
+    assert np.count_nonzero(diff) <= 2
+
+
+def _tiny_swiglu_block(bits, seed, D=64, F=128, M=2):
+    case = synth.swiglu_block_case(M, bits, group=32 if bits == 4 else 64, seed=seed, D=D, F=F)
+    blk = {k: (oracle.pack(c, bits), s, z) for k, (c, s, z) in case["proj"].items()}
+    return case, blk
+
+
+def _exact_swiglu_block_once(x, case):
+    """One un-normalized SwiGLU block application with exact sums and the (separately pinned)
+    element-wise swiglu."""
+    g = case["group"]
+    x = x.astype(np.float32)
+    h = np.array([[rne_half_bits(Fraction(float(v))) for v in row] for row in x], np.uint16).view(np.float16)
+
+    def q(a, name):
+        codes, s, z = case["proj"][name]
+        return _exact_gemm_bits(a, codes, s, z, g).view(np.float16)
+
+    D = case["D"]
+    qkv = q(h, "qkv")
+    o = q(np.ascontiguousarray(qkv[:, :D]), "o")
+    a = oracle.swiglu(q(o, "gate"), q(o, "up"))
+    d = q(np.ascontiguousarray(a), "down")
+    return (x + d.astype(np.float32)).astype(np.float32)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_swiglu_block_brute_force(bits):
+    case, blk = _tiny_swiglu_block(bits, seed=21)
+    x1 = oracle.loop_block_swiglu(case["x0"], blk, bits, case["group"], L=1, normalize=False)
+    ref = _exact_swiglu_block_once(case["x0"], case)
+    assert np.array_equal(x1.view(np.uint32), ref.view(np.uint32))
+    x2 = oracle.loop_block_swiglu(case["x0"], blk, bits, case["group"], L=2, normalize=False)
+    assert np.array_equal(x2.view(np.uint32), _exact_swiglu_block_once(ref, case).view(np.uint32))
+
+
+@pytest.mark.parametrize("which", ["gate", "up"])
+def test_swiglu_block_zero_update(which):
+    """A gate or an up projection with q == z gives g = 0 or u = 0, so the feed-forward adds exactly
+    zero and x is unchanged."""
+    case, blk = _tiny_swiglu_block(4, seed=22)
+    W, s, z = blk[which]
+    N, KW = W.shape
+    blk[which] = (oracle.pack(np.full((N, KW * 8), 9, np.uint8), 4), s, np.full_like(z, 9.0))
+    for norm in (True, False):
+        x = oracle.loop_block_swiglu(case["x0"], blk, 4, case["group"], L=3, normalize=norm)
+        assert np.array_equal(x.view(np.uint32), case["x0"].view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_swiglu_block_split_invariant(bits):
+    case, blk = _tiny_swiglu_block(bits, seed=23, M=3)
+    g = case["group"]
+    full = oracle.loop_block_swiglu(case["x0"], blk, bits, g, L=5)
+    mid = oracle.loop_block_swiglu(case["x0"], blk, bits, g, L=2)
+    rest = oracle.loop_block_swiglu(mid, blk, bits, g, L=3)
+    assert np.array_equal(full.view(np.uint32), rest.view(np.uint32))
+    assert not np.array_equal(full.view(np.uint32), case["x0"].view(np.uint32))
+
+
 def _int2_dequant(W2, s2, z2, K, group):
     return oracle.dequant(W2, s2, z2, K, 2, group)
 
