@@ -500,43 +500,57 @@ def run_prefill(tlq, torch, peaks):
 
 
 def run_loop_block(tlq, torch):
+    """The shared-weight block applied L times from one CUDA graph: the ReLU
+    block (four weights) and the pages' five-weight SwiGLU block."""
     out = {}
+    D, F = synth.D_MODEL, synth.FFN
+    shapes = {"relu": [(3 * D, D), (D, D), (F, D), (D, F)],
+              "swiglu": [(3 * D, D), (D, D), (2 * F, D), (D, F)]}
     try:
-        for bits in (4, 2):
-            for M in (1, 128):
-                case = synth.block_case(M, bits, seed=3)
-                proj = {}
-                for name, (codes, s, z) in case["proj"].items():
-                    proj[name] = (tlq.pack_weights(torch.from_numpy(codes).cuda(), bits),
-                                  torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda())
-                blk = tlq.LoopBlock(proj, bits, case["group"], M)
-                x0 = torch.from_numpy(case["x0"]).cuda()
-                for L in (4, 8, 16):
-                    x = x0.clone()
-                    blk.forward(x, L)  # warm
-                    torch.cuda.synchronize()
-                    g = torch.cuda.CUDAGraph()
-                    with torch.cuda.graph(g):
-                        blk.forward(x, L)
-                    for _ in range(3):
-                        g.replay()
-                    torch.cuda.synchronize()
-                    reps = 20
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record()
-                    for _ in range(reps):
-                        g.replay()
-                    e1.record()
-                    e1.synchronize()
-                    ms = e0.elapsed_time(e1) / reps
-                    wbytes = sum(N * K * bits // 8 + 4 * N * K // case["group"]
-                                 for (N, K) in [(6144, 2048), (2048, 2048), (8192, 2048), (2048, 8192)])
-                    out["int%d_M%d_L%d" % (bits, M, L)] = {
-                        "ms": round(ms, 4), "us_per_iter": round(ms * 1e3 / L, 2),
-                        "eff_GBps": round(L * wbytes / (ms * 1e-3) / 1e9, 1),
-                        "TFLOPs": round(L * 2 * M * 50331648 / (ms * 1e-3) / 1e12, 2)}
-                del blk, proj
+        for kind in ("relu", "swiglu"):
+            for bits in (4, 2):
+                for M in (1, 128):
+                    if kind == "relu":
+                        case = synth.block_case(M, bits, seed=3)
+                    else:
+                        case = synth.swiglu_block_case(M, bits, seed=3)
+                    proj = {}
+                    for name, (codes, s, z) in case["proj"].items():
+                        proj[name] = (tlq.pack_weights(torch.from_numpy(codes).cuda(), bits),
+                                      torch.from_numpy(s).cuda(), torch.from_numpy(z).cuda())
+                    if kind == "relu":
+                        blk = tlq.LoopBlock(proj, bits, case["group"], M)
+                    else:
+                        blk = tlq.SwiGLUBlock(proj, bits, case["group"], M)
+                    x0 = torch.from_numpy(case["x0"]).cuda()
+                    wbytes = sum(N * K * bits // 8 + 4 * N * K // case["group"] for (N, K) in shapes[kind])
+                    macs = sum(N * K for (N, K) in shapes[kind])
+                    for L in (4, 8, 16):
+                        x = x0.clone()
+                        blk.forward(x, L)  # warm
+                        torch.cuda.synchronize()
+                        g = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(g):
+                            blk.forward(x, L)
+                        for _ in range(3):
+                            g.replay()
+                        torch.cuda.synchronize()
+                        reps = 20
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        for _ in range(reps):
+                            g.replay()
+                        e1.record()
+                        e1.synchronize()
+                        ms = e0.elapsed_time(e1) / reps
+                        key = ("" if kind == "relu" else "swiglu_") + "int%d_M%d_L%d" % (bits, M, L)
+                        out[key] = {
+                            "ms": round(ms, 4), "us_per_iter": round(ms * 1e3 / L, 2),
+                            "eff_GBps": round(L * wbytes / (ms * 1e-3) / 1e9, 1),
+                            "TFLOPs": round(L * 2 * M * macs / (ms * 1e-3) / 1e12, 2)}
+                        del g
+                    del blk, proj
     except tlq.TLQError as e:
         out["unavailable"] = str(e)
     return out

@@ -196,6 +196,38 @@ typedef struct {
  */
 tlq_status tl_requant_int4_to_int2_batched(const tl_requant_desc* descs, int count, int group, void* stream);
 
+/*
+ * tl_quant_gemm_swiglu -- the SwiGLU feed-forward's gate and up projections as
+ * one GEMM with the gate*up product in its epilogue.
+ *
+ *   C[m][i] = fp16( silu(g) * u ),  g = fp16(acc[m][2i]),  u = fp16(acc[m][2i+1]),
+ *   silu(g) = g / (1 + exp(-g)),  acc = A . dequant(Wgu)^T in FP32.
+ *
+ * Source: "Model", ffn_dim -- "For SwiGLU this is the width of the gate and up
+ * projections"; the loop block's mlp_gate / mlp_up weights ("beta-Informed
+ * Deployment Features", CTX-TIER, Phase 2b).  g and u are rounded to FP16 like
+ * any GEMM output of the block; the product is formed in FP32 (the pages fix
+ * neither).
+ *   Wgu     packed weights [N2][K] whose rows alternate gate and up: row 2i is
+ *           gate row i, row 2i+1 up row i (tl_interleave_rows builds it from
+ *           the two packed weights; scales and zeros are interleaved the same
+ *           way).  N2 = 2F, a multiple of 16.
+ *   C       FP16 [M][N2/2], row stride N2/2; must not overlap A.
+ *   Other arguments and errors as tl_quant_gemm.
+ */
+tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales,
+                                const uint16_t* zeros, uint16_t* C, int M, int N2, int K, int bits, int group,
+                                void* stream);
+
+/*
+ * tl_interleave_rows -- out row 2i = row i of a, out row 2i+1 = row i of b
+ * (device buffers of `rows` rows of `row_bytes` bytes; out holds 2*rows).
+ * Lays out the gate and up weights (packed words, scales, zeros) for
+ * tl_quant_gemm_swiglu.  out must not overlap a or b.  Asynchronous on
+ * `stream`.  Returns TLQ_OK, TLQ_EINVAL or TLQ_ECUDA.
+ */
+tlq_status tl_interleave_rows(const void* a, const void* b, void* out, int rows, size_t row_bytes, void* stream);
+
 /* One quantized projection of the loop block: weights [N][K] in the packed
  * format, FP16 scales/zeros [N][K/group]. */
 typedef struct {
@@ -229,6 +261,31 @@ typedef struct {
 } tl_block;
 
 /*
+ * The five-weight SwiGLU loop block (attn_qkv, attn_out, mlp_gate, mlp_up,
+ * mlp_down -- "beta-Informed Deployment Features", CTX-TIER, Phase 2b;
+ * "Model", ffn_dim):
+ *   h = norm(x); qkv = Q(h); o = Q(qkv[:, :D]);
+ *   a = fp16(silu(Q_gate(o)) * Q_up(o)); x += float(Q_down(a))
+ * with every GEMM output rounded to FP16 and the residual add in FP32.
+ *   qkv     : N = 3*D, K = D          o    : N = D, K = D
+ *   gate_up : N = 2*F, K = D, rows interleaved (see tl_quant_gemm_swiglu)
+ *   down    : N = D, K = F
+ * Scratch (caller-owned device FP16, at least M rows): h [M][D],
+ * qkv_out [M][3D], o_out [M][D], act_out [M][F].  normalize as tl_block.
+ */
+typedef struct {
+  tl_qproj qkv, o, gate_up, down;
+  int bits;
+  int group;
+  int D;
+  uint16_t* h;
+  uint16_t* qkv_out;
+  uint16_t* o_out;
+  uint16_t* act_out;
+  int normalize;
+} tl_swiglu_block;
+
+/*
  * tl_loop_block_forward -- apply the shared block L times to the FP32
  * residual stream x[M][D] in place:
  *
@@ -250,6 +307,14 @@ typedef struct {
  * whether the block's packed weights fit in L2 and the kernel choice.
  */
 tlq_status tl_loop_block_forward(float* x, const tl_block* block, int L, int M, void* stream);
+
+/*
+ * tl_swiglu_block_forward -- the five-weight SwiGLU loop block applied L times
+ * to the FP32 residual x [M][D] in place (same rules, errors and L2 policy as
+ * tl_loop_block_forward; the gate/up GEMM runs with the SwiGLU epilogue, so a
+ * block iteration is five launches like the ReLU block).
+ */
+tlq_status tl_swiglu_block_forward(float* x, const tl_swiglu_block* block, int L, int M, void* stream);
 
 /*
  * tl_loop_block_forward_static_scratch -- tl_loop_block_forward for callers

@@ -132,6 +132,36 @@ def test_requant_rejects_bad_arguments(clib):
     assert clib.tl_requant_int4_to_int2_batched(cross2, 2, g, None) == tlq.TLQ_EINVAL
 
 
+def test_swiglu_entry_points_reject_bad_arguments(clib):
+    """Host-side validation of the SwiGLU GEMM, the row interleave and the
+    SwiGLU block; nothing is launched (the addresses are never dereferenced)."""
+    import weight_only_int4_quant_gb300 as tlq
+
+    A, W, S, Z, C = 1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20
+    ok = dict(A=A, W=W, S=S, Z=Z, C=C, M=4, N2=64, K=256, bits=4, group=128)
+
+    def sw(**kw):
+        a = dict(ok, **kw)
+        return clib.tl_quant_gemm_swiglu(a["A"], a["W"], a["S"], a["Z"], a["C"], a["M"], a["N2"], a["K"],
+                                         a["bits"], a["group"], None)
+
+    assert sw(N2=24) == tlq.TLQ_EINVAL and "16" in tlq.tl_last_error()
+    assert sw(A=None) == tlq.TLQ_EINVAL
+    assert sw(bits=3) == tlq.TLQ_EINVAL
+    assert sw(C=A + 64) == tlq.TLQ_EINVAL and "overlap" in tlq.tl_last_error()
+    assert clib.tl_interleave_rows(None, W, C, 4, 64, None) == tlq.TLQ_EINVAL
+    assert clib.tl_interleave_rows(A, W, C, 0, 64, None) == tlq.TLQ_EINVAL
+    assert clib.tl_interleave_rows(A, W, A + 64, 4, 64, None) == tlq.TLQ_EINVAL  # out over a
+    assert clib.tl_swiglu_block_forward(None, None, 1, 1, None) == tlq.TLQ_EINVAL
+    blk = tlq._SwigluBlock()
+    blk.D = 64
+    assert clib.tl_swiglu_block_forward(16, ctypes.byref(blk), 1, 1, None) == tlq.TLQ_EINVAL
+    blk.qkv.N, blk.qkv.K, blk.o.N, blk.o.K = 192, 64, 64, 64
+    blk.gate_up.N, blk.gate_up.K, blk.down.N, blk.down.K = 120, 64, 64, 60  # 2F not a multiple of 16
+    assert clib.tl_swiglu_block_forward(16, ctypes.byref(blk), 1, 1, None) == tlq.TLQ_EINVAL
+    assert "gate_up" in tlq.tl_last_error()
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     import weight_only_int4_quant_gb300 as tlq
 

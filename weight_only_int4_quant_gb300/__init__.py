@@ -20,6 +20,8 @@ __all__ = [
     "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout", "tl_last_error", "tl_version",
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "gemm_descs", "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
     "tl_requant_int4_to_int2", "tl_requant_int4_to_int2_batched", "requant_int4_to_int2",
+    "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward", "quant_gemm_swiglu",
+    "interleave_rows", "SwiGLUBlock",
 ]
 
 # every symbol include/tlq.h declares
@@ -27,7 +29,7 @@ EXPORTED = (
     "tl_last_error", "tl_version", "tl_quant_gemm", "tl_pack_weights", "tl_unpack_weights",
     "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "tl_requant_int4_to_int2",
-    "tl_requant_int4_to_int2_batched",
+    "tl_requant_int4_to_int2_batched", "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -61,6 +63,13 @@ class _Block(ctypes.Structure):
                 ("bits", ctypes.c_int), ("group", ctypes.c_int), ("D", ctypes.c_int),
                 ("h", ctypes.c_void_p), ("qkv_out", ctypes.c_void_p), ("o_out", ctypes.c_void_p),
                 ("up_out", ctypes.c_void_p), ("normalize", ctypes.c_int)]
+
+
+class _SwigluBlock(ctypes.Structure):
+    _fields_ = [("qkv", _QProj), ("o", _QProj), ("gate_up", _QProj), ("down", _QProj),
+                ("bits", ctypes.c_int), ("group", ctypes.c_int), ("D", ctypes.c_int),
+                ("h", ctypes.c_void_p), ("qkv_out", ctypes.c_void_p), ("o_out", ctypes.c_void_p),
+                ("act_out", ctypes.c_void_p), ("normalize", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -101,6 +110,9 @@ def load():
             "tl_quant_gemm_batched": ([ctypes.POINTER(_GemmDesc), I, P], I),
             "tl_requant_int4_to_int2": ([P, P, P, P, P, P, I, I, I, P], I),
             "tl_requant_int4_to_int2_batched": ([ctypes.POINTER(_RequantDesc), I, I, P], I),
+            "tl_quant_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P], I),
+            "tl_interleave_rows": ([P, P, P, I, ctypes.c_size_t, P], I),
+            "tl_swiglu_block_forward": ([P, ctypes.POINTER(_SwigluBlock), I, I, P], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -209,6 +221,32 @@ def tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, group: int, stream=None) -> 
                                              N, K, group, _stream(stream)))
 
 
+def tl_quant_gemm_swiglu(A, Wgu, scales, zeros, C, bits: int, group: int, stream=None) -> None:
+    import torch
+
+    M, K = A.shape
+    N2 = Wgu.shape[0]
+    if tuple(C.shape) != (M, N2 // 2):
+        raise ValueError("C must be [M, N2/2] = [%d, %d]" % (M, N2 // 2))
+    _raise_if(load().tl_quant_gemm_swiglu(_dev(A, (torch.float16,), "A"), _dev(Wgu, (torch.int32, torch.uint32), "Wgu"),
+                                          _dev(scales, (torch.float16,), "scales"),
+                                          _dev(zeros, (torch.float16,), "zeros"), _dev(C, (torch.float16,), "C"),
+                                          M, N2, K, bits, group, _stream(stream)))
+
+
+def tl_interleave_rows(a, b, out, stream=None) -> None:
+    """out[2i] = a[i], out[2i+1] = b[i] (row-major device tensors)."""
+    for t, name in ((a, "a"), (b, "b"), (out, "out")):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if a.shape != b.shape or a.dtype != b.dtype or out.dtype != a.dtype or out.shape[0] != 2 * a.shape[0] \
+            or tuple(out.shape[1:]) != tuple(a.shape[1:]):
+        raise ValueError("interleave_rows: a, b [rows, ...] and out [2 rows, ...] of one dtype")
+    rows = a.shape[0]
+    _raise_if(load().tl_interleave_rows(a.data_ptr(), b.data_ptr(), out.data_ptr(), rows,
+                                        a.numel() * a.element_size() // rows, _stream(stream)))
+
+
 def requant_descs(problems):
     """(W4, s4, z4, W2, s2, z2) tensor tuples -> a ctypes descriptor array."""
     import torch
@@ -279,6 +317,22 @@ def pack_weights(codes, bits: int, stream=None):
     W = torch.empty((N, K * bits // 32), dtype=torch.int32, device=codes.device)
     tl_pack_weights(codes, W, bits, stream)
     return W
+
+
+def quant_gemm_swiglu(A, Wgu, scales, zeros, bits: int, group: int, stream=None):
+    import torch
+
+    C = torch.empty((A.shape[0], Wgu.shape[0] // 2), dtype=torch.float16, device=A.device)
+    tl_quant_gemm_swiglu(A, Wgu, scales, zeros, C, bits, group, stream)
+    return C
+
+
+def interleave_rows(a, b, stream=None):
+    import torch
+
+    out = torch.empty((2 * a.shape[0],) + tuple(a.shape[1:]), dtype=a.dtype, device=a.device)
+    tl_interleave_rows(a, b, out, stream)
+    return out
 
 
 def requant_int4_to_int2(W4, s4, z4, group: int, in_place_scales: bool = False, stream=None):
@@ -371,3 +425,84 @@ class LoopBlock:
     def forward(self, x, L: int, stream=None):
         tl_loop_block_forward(x, self, L, stream)
         return x
+
+
+class SwiGLUBlock:
+    """The five-weight SwiGLU loop block (attn_qkv, attn_out, mlp_gate,
+    mlp_up, mlp_down).
+
+    ``proj`` maps "qkv", "o", "gate", "up", "down" to (W packed int32,
+    scales, zeros) CUDA tensors.  The gate and up weights are interleaved row
+    by row into one [2F, ...] weight for the fused GEMM (tl_interleave_rows);
+    scratch for up to ``max_rows`` rows is allocated here."""
+
+    def __init__(self, proj: dict, bits: int, group: int, max_rows: int, normalize: bool = True, stream=None):
+        import torch
+
+        self.bits, self.group, self.max_rows, self.normalize = bits, group, max_rows, normalize
+        gate, up = proj["gate"], proj["up"]
+        gate_up = tuple(interleave_rows(g, u, stream) for g, u in zip(gate, up))
+        self.proj = {"qkv": proj["qkv"], "o": proj["o"], "gate_up": gate_up, "down": proj["down"]}
+        cpw = 32 // bits
+        D = proj["o"][0].shape[0]
+        F = gate[0].shape[0]
+        self.D, self.F = D, F
+        dev = proj["o"][0].device
+        self.h = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
+        self.qkv_out = torch.empty((max_rows, 3 * D), dtype=torch.float16, device=dev)
+        self.o_out = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
+        self.act_out = torch.empty((max_rows, F), dtype=torch.float16, device=dev)
+        self._bind()
+
+    def _bind(self):
+        import torch
+
+        cpw = 32 // self.bits
+        c = _SwigluBlock()
+        for name in ("qkv", "o", "gate_up", "down"):
+            W, s, z = self.proj[name]
+            setattr(c, name, _QProj(_dev(W, (torch.int32, torch.uint32), name + ".W"),
+                                    _dev(s, (torch.float16,), name + ".s"), _dev(z, (torch.float16,), name + ".z"),
+                                    W.shape[0], W.shape[1] * cpw))
+        c.bits, c.group, c.D = self.bits, self.group, self.D
+        c.h, c.qkv_out, c.o_out, c.act_out = (self.h.data_ptr(), self.qkv_out.data_ptr(), self.o_out.data_ptr(),
+                                              self.act_out.data_ptr())
+        c.normalize = 1 if self.normalize else 0
+        self._c = c
+
+    def forward(self, x, L: int, stream=None):
+        import torch
+
+        M = x.shape[0]
+        if M > self.max_rows:
+            raise ValueError("x has %d rows, the block's scratch holds %d" % (M, self.max_rows))
+        _raise_if(load().tl_swiglu_block_forward(_dev(x, (torch.float32,), "x"), ctypes.byref(self._c), L, M,
+                                                 _stream(stream)))
+        return x
+
+    def to_int2(self, stream=None):
+        """The context-length tier switch for the five weights (the fused
+        gate/up weight re-quantizes row by row like the two it holds): one
+        launch, scales / zeros in place, INT4 words released after the
+        stream has passed the conversion."""
+        import torch
+
+        if self.bits != 4:
+            raise ValueError("to_int2 needs an INT4 block (bits=%d)" % self.bits)
+        new, probs = {}, []
+        for name in ("qkv", "o", "gate_up", "down"):
+            W4, s4, z4 = self.proj[name]
+            W2 = torch.empty((W4.shape[0], W4.shape[1] // 2), dtype=torch.int32, device=W4.device)
+            new[name] = (W2, s4, z4)
+            probs.append((W4, s4, z4, W2, s4, z4))
+        tl_requant_int4_to_int2_batched(probs, self.group, stream)
+        if stream is None:
+            torch.cuda.current_stream().synchronize()
+        elif isinstance(stream, int):
+            torch.cuda.synchronize()
+        else:
+            stream.synchronize()
+        self.proj = new
+        self.bits = 2
+        self._bind()
+        return self

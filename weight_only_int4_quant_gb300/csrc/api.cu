@@ -167,6 +167,36 @@ tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint1
   return run_gemm(plain_args(A, Wpacked, scales, zeros, C, M, N, K, bits, group), static_cast<cudaStream_t>(stream));
 }
 
+tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales, const uint16_t* zeros,
+                                uint16_t* C, int M, int N2, int K, int bits, int group, void* stream) {
+  g_msg[0] = 0;
+  tlq_status st = check_gemm_call(A, Wgu, scales, zeros, C, M, N2, K, bits, group, "tl_quant_gemm_swiglu");
+  if (st != TLQ_OK) return st;
+  if (N2 % 16) return set_error(TLQ_EINVAL, "tl_quant_gemm_swiglu: N2=%d must be a multiple of 16", N2);
+  if (overlaps(A, (size_t)M * K * 2, C, (size_t)M * (N2 / 2) * 2))
+    return set_error(TLQ_EINVAL, "tl_quant_gemm_swiglu: A and C overlap");
+  GemmArgs a = plain_args(A, Wgu, scales, zeros, C, M, N2, K, bits, group);
+  a.ldc = N2 / 2;
+  a.epi = kEpiSwiglu;
+  return run_gemm(a, static_cast<cudaStream_t>(stream));
+}
+
+tlq_status tl_interleave_rows(const void* a, const void* b, void* out, int rows, size_t row_bytes, void* stream) {
+  g_msg[0] = 0;
+  if (!a || !b || !out) return set_error(TLQ_EINVAL, "tl_interleave_rows: null pointer");
+  if (rows < 1 || row_bytes < 1)
+    return set_error(TLQ_EINVAL, "tl_interleave_rows: rows=%d row_bytes=%zu must be >= 1", rows, row_bytes);
+  const size_t n = (size_t)rows * row_bytes;
+  if (overlaps(out, 2 * n, a, n) || overlaps(out, 2 * n, b, n))
+    return set_error(TLQ_EINVAL, "tl_interleave_rows: out overlaps an input");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpy2DAsync(out, 2 * row_bytes, a, row_bytes, row_bytes, (size_t)rows, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy2DAsync(static_cast<char*>(out) + row_bytes, 2 * row_bytes, b, row_bytes, row_bytes, (size_t)rows,
+                          cudaMemcpyDeviceToDevice, s);
+  return cuda_error(e, "tl_interleave_rows: copy");
+}
+
 tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_) {
   g_msg[0] = 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -315,112 +345,109 @@ tlq_status tl_requant_int4_to_int2_batched(const tl_requant_desc* descs, int cou
   return requant(descs, count, group, stream, "tl_requant_int4_to_int2_batched");
 }
 
-tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void* stream_) {
-  g_msg[0] = 0;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (!x || !b) return set_error(TLQ_EINVAL, "tl_loop_block_forward: null x or block");
-  if (L < 0) return set_error(TLQ_EINVAL, "tl_loop_block_forward: L=%d (must be >= 0)", L);
-  if (M < 1) return set_error(TLQ_EINVAL, "tl_loop_block_forward: M=%d (must be >= 1)", M);
-  const int D = b->D, F = b->up.N;
-  if (D < 1 || D % 8) return set_error(TLQ_EINVAL, "tl_loop_block_forward: D=%d must be a positive multiple of 8", D);
-  if (b->qkv.N != 3 * D || b->qkv.K != D) return set_error(TLQ_EINVAL, "tl_loop_block_forward: qkv must be [3D x D]");
-  if (b->o.N != D || b->o.K != D) return set_error(TLQ_EINVAL, "tl_loop_block_forward: o must be [D x D]");
-  if (b->up.K != D || F < 1) return set_error(TLQ_EINVAL, "tl_loop_block_forward: up must be [F x D]");
-  if (b->down.N != D || b->down.K != F) return set_error(TLQ_EINVAL, "tl_loop_block_forward: down must be [D x F]");
-  if (!b->h || !b->qkv_out || !b->o_out || !b->up_out)
-    return set_error(TLQ_EINVAL, "tl_loop_block_forward: null scratch buffer");
-  const tl_qproj* projs[4] = {&b->qkv, &b->o, &b->up, &b->down};
-  const char* names[4] = {"qkv", "o", "up", "down"};
+namespace {
+// One loop block for the driver: the ReLU block (ff = up, [F x D]) or the
+// SwiGLU block (ff = interleaved gate/up, [2F x D]).
+struct BlockSpec {
+  const tl_qproj* proj[4];  // qkv, o, ff, down
+  int bits, group, D, F;
+  bool swiglu;
+  uint16_t *h, *qkv_out, *o_out, *act_out;
+  int normalize;
+  const char* who;
+};
+
+tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_t stream) {
+  const char* who = b.who;
+  if (L < 0) return set_error(TLQ_EINVAL, "%s: L=%d (must be >= 0)", who, L);
+  if (M < 1) return set_error(TLQ_EINVAL, "%s: M=%d (must be >= 1)", who, M);
+  const int D = b.D, F = b.F;
+  if (D < 1 || D % 8) return set_error(TLQ_EINVAL, "%s: D=%d must be a positive multiple of 8", who, D);
+  const char* ffname = b.swiglu ? "gate_up" : "up";
+  if (b.proj[0]->N != 3 * D || b.proj[0]->K != D) return set_error(TLQ_EINVAL, "%s: qkv must be [3D x D]", who);
+  if (b.proj[1]->N != D || b.proj[1]->K != D) return set_error(TLQ_EINVAL, "%s: o must be [D x D]", who);
+  if (b.proj[2]->K != D || F < 1) return set_error(TLQ_EINVAL, "%s: %s must have K = D", who, ffname);
+  if (b.swiglu && (b.proj[2]->N % 16))
+    return set_error(TLQ_EINVAL, "%s: gate_up N=%d must be 2F with F a multiple of 8", who, b.proj[2]->N);
+  if (b.proj[3]->N != D || b.proj[3]->K != F) return set_error(TLQ_EINVAL, "%s: down must be [D x F]", who);
+  if (!b.h || !b.qkv_out || !b.o_out || !b.act_out) return set_error(TLQ_EINVAL, "%s: null scratch buffer", who);
+  const char* names[4] = {"qkv", "o", ffname, "down"};
   for (int i = 0; i < 4; ++i) {
-    const tl_qproj* p = projs[i];
-    if (!p->W || !p->s || !p->z) return set_error(TLQ_EINVAL, "tl_loop_block_forward: %s has a null pointer", names[i]);
-    if (!aligned16(p->W)) return set_error(TLQ_EINVAL, "tl_loop_block_forward: %s weights not 16-byte aligned", names[i]);
-    tlq_status st = check_gemm_shape(M, p->N, p->K, b->bits, b->group, names[i]);
+    const tl_qproj* p = b.proj[i];
+    if (!p->W || !p->s || !p->z) return set_error(TLQ_EINVAL, "%s: %s has a null pointer", who, names[i]);
+    if (!aligned16(p->W)) return set_error(TLQ_EINVAL, "%s: %s weights not 16-byte aligned", who, names[i]);
+    tlq_status st = check_gemm_shape(M, p->N, p->K, b.bits, b.group, names[i]);
     if (st != TLQ_OK) return st;
-    if (p->N % 8) return set_error(TLQ_EINVAL, "tl_loop_block_forward: %s N=%d must be a multiple of 8", names[i], p->N);
+    if (p->N % 8) return set_error(TLQ_EINVAL, "%s: %s N=%d must be a multiple of 8", who, names[i], p->N);
   }
-  if (!aligned16(b->h) || !aligned16(b->qkv_out) || !aligned16(b->o_out) || !aligned16(b->up_out))
-    return set_error(TLQ_EINVAL, "tl_loop_block_forward: scratch buffers must be 16-byte aligned");
+  if (!aligned16(b.h) || !aligned16(b.qkv_out) || !aligned16(b.o_out) || !aligned16(b.act_out))
+    return set_error(TLQ_EINVAL, "%s: scratch buffers must be 16-byte aligned", who);
 
   // The block's weights are re-read every iteration: when they fit in half
   // the L2 they are streamed with an evict-last policy so that iterations
   // after the first read them from L2 ("Model", "Returns", item 4: auto tile
   // sizing reports loop-block vs L2 residency).
-  const int cpw = 32 / b->bits;
+  const int cpw = 32 / b.bits;
   size_t wb = 0;
   for (int i = 0; i < 4; ++i)
-    wb += (size_t)projs[i]->N * (projs[i]->K / cpw) * 4 + (size_t)projs[i]->N * (projs[i]->K / b->group) * 4;
+    wb += (size_t)b.proj[i]->N * (b.proj[i]->K / cpw) * 4 + (size_t)b.proj[i]->N * (b.proj[i]->K / b.group) * 4;
   const bool keep = L > 1 && wb <= (size_t)device_info().l2_bytes / 2;
   static std::once_flag logged;
   if (log_enabled()) {
     std::call_once(logged, [&] {
       fprintf(stderr, "[tlq] loop block: INT%d group %d, packed weights + scales/zeros %.1f MB, L2 %.1f MB -> %s\n",
-              b->bits, b->group, wb / 1e6, device_info().l2_bytes / 1e6,
+              b.bits, b.group, wb / 1e6, device_info().l2_bytes / 1e6,
               keep ? "kept in L2 (evict-last) after the first iteration" : "streamed from HBM every iteration");
     });
   }
 
-  for (int l = 0; l < L; ++l) {
-    tlq_status st = launch_rmsnorm(x, reinterpret_cast<__half*>(b->h), M, D, b->normalize, stream);
-    if (st != TLQ_OK) return st;
+  auto gemm = [&](const tl_qproj* p, const uint16_t* A, int lda, uint16_t* C, int ldc, int epi) {
     GemmArgs a;
-    a.bits = b->bits;
-    a.group = b->group;
+    a.bits = b.bits;
+    a.group = b.group;
     a.M = M;
     a.l2_keep = keep ? 1 : 0;
-    a.X = nullptr;
-    a.ldx = 0;
-    // QKV
-    a.A = reinterpret_cast<const __half*>(b->h);
-    a.lda = D;
-    a.W = b->qkv.W;
-    a.S = reinterpret_cast<const __half*>(b->qkv.s);
-    a.Z = reinterpret_cast<const __half*>(b->qkv.z);
-    a.C = reinterpret_cast<__half*>(b->qkv_out);
-    a.ldc = 3 * D;
-    a.N = 3 * D;
-    a.K = D;
-    a.epi = kEpiStore;
-    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
-    // O on qkv[:, :D]
-    a.A = reinterpret_cast<const __half*>(b->qkv_out);
-    a.lda = 3 * D;
-    a.W = b->o.W;
-    a.S = reinterpret_cast<const __half*>(b->o.s);
-    a.Z = reinterpret_cast<const __half*>(b->o.z);
-    a.C = reinterpret_cast<__half*>(b->o_out);
-    a.ldc = D;
-    a.N = D;
-    a.K = D;
-    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
-    // UP + relu
-    a.A = reinterpret_cast<const __half*>(b->o_out);
-    a.lda = D;
-    a.W = b->up.W;
-    a.S = reinterpret_cast<const __half*>(b->up.s);
-    a.Z = reinterpret_cast<const __half*>(b->up.z);
-    a.C = reinterpret_cast<__half*>(b->up_out);
-    a.ldc = F;
-    a.N = F;
-    a.K = D;
-    a.epi = kEpiRelu;
-    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
-    // DOWN + FP32 residual add
-    a.A = reinterpret_cast<const __half*>(b->up_out);
-    a.lda = F;
-    a.W = b->down.W;
-    a.S = reinterpret_cast<const __half*>(b->down.s);
-    a.Z = reinterpret_cast<const __half*>(b->down.z);
-    a.C = nullptr;
-    a.ldc = 0;
-    a.X = x;
-    a.ldx = D;
-    a.N = D;
-    a.K = F;
-    a.epi = kEpiResidual;
-    if ((st = run_gemm(a, stream)) != TLQ_OK) return st;
+    a.A = reinterpret_cast<const __half*>(A);
+    a.lda = lda;
+    a.W = p->W;
+    a.S = reinterpret_cast<const __half*>(p->s);
+    a.Z = reinterpret_cast<const __half*>(p->z);
+    a.C = reinterpret_cast<__half*>(C);
+    a.ldc = ldc;
+    a.X = epi == kEpiResidual ? x : nullptr;
+    a.ldx = epi == kEpiResidual ? D : 0;
+    a.N = p->N;
+    a.K = p->K;
+    a.epi = epi;
+    return run_gemm(a, stream);
+  };
+  for (int l = 0; l < L; ++l) {
+    tlq_status st = launch_rmsnorm(x, reinterpret_cast<__half*>(b.h), M, D, b.normalize, stream);
+    if (st != TLQ_OK) return st;
+    if ((st = gemm(b.proj[0], b.h, D, b.qkv_out, 3 * D, kEpiStore)) != TLQ_OK) return st;  // QKV
+    if ((st = gemm(b.proj[1], b.qkv_out, 3 * D, b.o_out, D, kEpiStore)) != TLQ_OK) return st;  // O on qkv[:, :D]
+    // UP + ReLU, or the fused gate/up GEMM + SwiGLU
+    if ((st = gemm(b.proj[2], b.o_out, D, b.act_out, F, b.swiglu ? kEpiSwiglu : kEpiRelu)) != TLQ_OK) return st;
+    if ((st = gemm(b.proj[3], b.act_out, F, nullptr, 0, kEpiResidual)) != TLQ_OK) return st;  // DOWN + FP32 residual
   }
   return TLQ_OK;
+}
+}  // namespace
+
+tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void* stream) {
+  g_msg[0] = 0;
+  if (!x || !b) return set_error(TLQ_EINVAL, "tl_loop_block_forward: null x or block");
+  const BlockSpec s = {{&b->qkv, &b->o, &b->up, &b->down}, b->bits, b->group, b->D, b->up.N, false,
+                       b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, "tl_loop_block_forward"};
+  return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
+}
+
+tlq_status tl_swiglu_block_forward(float* x, const tl_swiglu_block* b, int L, int M, void* stream) {
+  g_msg[0] = 0;
+  if (!x || !b) return set_error(TLQ_EINVAL, "tl_swiglu_block_forward: null x or block");
+  const BlockSpec s = {{&b->qkv, &b->o, &b->gate_up, &b->down}, b->bits, b->group, b->D, b->gate_up.N / 2, true,
+                       b->h, b->qkv_out, b->o_out, b->act_out, b->normalize, "tl_swiglu_block_forward"};
+  return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
 }
 
 tlq_status tl_check_status(void* stream) {

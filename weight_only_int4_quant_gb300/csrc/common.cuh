@@ -279,11 +279,24 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   return v;
 }
 
-// Epilogue kinds shared by the GEMM kernels.
-enum Epilogue : int { kEpiStore = 0, kEpiRelu = 1, kEpiResidual = 2 };
+// Epilogue kinds shared by the GEMM kernels.  kEpiSwiglu: the weight rows are
+// (gate, up) pairs, rows 2i and 2i+1; output column i (row stride ldc) is
+// swiglu_half(fp16(acc[2i]), fp16(acc[2i+1])).
+enum Epilogue : int { kEpiStore = 0, kEpiRelu = 1, kEpiResidual = 2, kEpiSwiglu = 3 };
 
 __device__ __forceinline__ __half relu_half(__half v) {
   return (__half2float(v) > 0.f) ? v : __float2half_rn(0.f);
+}
+
+// fp16(silu(g) * u), silu(g) = g / (1 + exp(-g)), on the FP16 GEMM outputs
+// ("Model", ffn_dim: the gate and up projections of SwiGLU).  FP32 with the
+// hardware exponential and the approximate divide: silu's relative error is
+// about 2^-20, far below FP16's 2^-11, and it keeps the decode kernel's
+// register budget (an IEEE divide here spills).  For g below about -87 the
+// divide returns 0 (silu's limit).
+__device__ __forceinline__ __half swiglu_half(__half g, __half u) {
+  const float gf = __half2float(g);
+  return __float2half_rn(__fdividef(gf, 1.0f + __expf(-gf)) * __half2float(u));
 }
 
 // ---------------------------------------------------------------------------

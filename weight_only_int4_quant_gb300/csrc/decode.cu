@@ -712,6 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           float* xp = pr.X + (size_t)tk * pr.ldx + n;
 #pragma unroll
           for (int j = 0; j < 4; ++j) xp[j] = xp[j] + __half2float(h[j]);
+        } else if (epi == kEpiSwiglu) {  // rows (n, n+1), (n+2, n+3) are (gate, up) pairs
+          const uint32_t o = (uint32_t)__half_as_ushort(swiglu_half(h[0], h[1])) |
+                             ((uint32_t)__half_as_ushort(swiglu_half(h[2], h[3])) << 16);
+          *reinterpret_cast<uint32_t*>(pr.C + (size_t)tk * pr.ldc + n / 2) = o;
         } else {
           if (epi == kEpiRelu) {
 #pragma unroll

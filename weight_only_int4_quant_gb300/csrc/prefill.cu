@@ -443,6 +443,25 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (n0 + col + i < p.N) store_out<EPI>(p, m, n0 + col + i, __uint_as_float(v[i]));
+            } else if constexpr (EPI == kEpiSwiglu) {
+              // 32 rows = 16 (gate, up) pairs -> 16 outputs at column (n0 + col) / 2
+#pragma unroll
+              for (int c16 = 0; c16 < 2; ++c16) {
+                const int nb = n0 + col + c16 * 16;
+                if (nb < p.N) {  // N is a multiple of 16
+                  uint32_t h[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const int j = c16 * 16 + 4 * i;
+                    const __half a0 = swiglu_half(__float2half_rn(__uint_as_float(v[j])),
+                                                  __float2half_rn(__uint_as_float(v[j + 1])));
+                    const __half a1 = swiglu_half(__float2half_rn(__uint_as_float(v[j + 2])),
+                                                  __float2half_rn(__uint_as_float(v[j + 3])));
+                    h[i] = (uint32_t)__half_as_ushort(a0) | ((uint32_t)__half_as_ushort(a1) << 16);
+                  }
+                  *reinterpret_cast<uint4*>(p.C + (size_t)m * p.ldc + nb / 2) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+              }
             } else {
 #pragma unroll
               for (int c8 = 0; c8 < 4; ++c8) {
@@ -518,9 +537,18 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
         const int m = m0 + mt * BM + mm, n = n0 + rank * cpr + c4;
         if (m < p.M) {
+          if constexpr (EPI == kEpiSwiglu) {
+            if (n < p.N) {  // N is a multiple of 16: the quad is whole
+              const __half a0 = swiglu_half(__float2half_rn(a[0]), __float2half_rn(a[1]));
+              const __half a1 = swiglu_half(__float2half_rn(a[2]), __float2half_rn(a[3]));
+              *reinterpret_cast<uint32_t*>(p.C + (size_t)m * p.ldc + n / 2) =
+                  (uint32_t)__half_as_ushort(a0) | ((uint32_t)__half_as_ushort(a1) << 16);
+            }
+          } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (n + i < p.N) store_out<EPI>(p, m, n + i, a[i]);
+            for (int i = 0; i < 4; ++i)
+              if (n + i < p.N) store_out<EPI>(p, m, n + i, a[i]);
+          }
         }
       }
     }
@@ -663,6 +691,7 @@ tlq_status dispatch_epi(const GemmArgs& a, cudaStream_t s) {
   switch (a.epi) {
     case kEpiStore: return launch_pick<BITS, kEpiStore>(a, s);
     case kEpiRelu: return launch_pick<BITS, kEpiRelu>(a, s);
+    case kEpiSwiglu: return launch_pick<BITS, kEpiSwiglu>(a, s);
     default: return launch_pick<BITS, kEpiResidual>(a, s);
   }
 }
