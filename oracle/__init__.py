@@ -16,6 +16,8 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   pack / unpack                    hand-written words, byte-layout restatement,
                                    round trip
   dequant                          exact rational arithmetic on every group
+  dequant_half                     exact rational value rounded by an
+                                   independent RNE search, closed forms
   quant_gemm                       exact rational sum rounded once (brute force),
                                    closed forms, torch binary64 matmul
   quant_gemm_points                equality with quant_gemm
@@ -80,6 +82,7 @@ def _load():
                 "orc_pack": [P, P, I, I, I],
                 "orc_unpack": [P, P, I, I, I],
                 "orc_dequant": [P, P, P, I, I, I, I, P],
+                "orc_dequant_half": [P, P, P, I, I, I, I, P],
                 "orc_quant_gemm": [P, I, P, P, P, P, I, I, I, I, I, I],
                 "orc_quant_gemm_points": [P, I, P, P, P, I, I, I, I, I, P, P, I, P],
                 "orc_rms_norm_half": [P, I, I, ctypes.c_double, P],
@@ -160,6 +163,17 @@ def dequant(W: np.ndarray, scales, zeros, K: int, bits: int, group: int) -> np.n
     out = np.empty((N, K), dtype=np.float64)
     _check(_load().orc_dequant(_ptr(W), _ptr(s), _ptr(z), N, K, bits, group, _ptr(out)), "dequant")
     return out
+
+
+def dequant_half(W: np.ndarray, scales, zeros, K: int, bits: int, group: int) -> np.ndarray:
+    """FP16 body of a packed weight: fp16_RNE((q - z) * s) per weight, +0 for
+    exact zeros ("Model", "VRAM cost": the FP16 body cache)."""
+    W = np.ascontiguousarray(W, dtype=np.uint32)
+    s, z = _half_bits(scales), _half_bits(zeros)
+    N = W.shape[0]
+    out = np.empty((N, K), dtype=np.uint16)
+    _check(_load().orc_dequant_half(_ptr(W), _ptr(s), _ptr(z), N, K, bits, group, _ptr(out)), "dequant_half")
+    return out.view(np.float16)
 
 
 def quant_gemm(A, W: np.ndarray, scales, zeros, bits: int, group: int, K: int | None = None) -> np.ndarray:

@@ -159,6 +159,27 @@ int orc_dequant(const uint32_t* W, const uint16_t* scales, const uint16_t* zeros
   return 0;
 }
 
+/* The FP16 "body" of a quantized weight: each weight dequantized exactly
+ * and rounded once to FP16 (RNE); an exact zero is stored as +0.  This is the
+ * dense copy the runtime's dequant-to-FP16 cache keeps ("Model", section
+ * "VRAM cost", the FP16 body cache option), here as a comparison point for
+ * the quantized GEMM. */
+int orc_dequant_half(const uint32_t* W, const uint16_t* scales, const uint16_t* zeros,
+                     int N, int K, int bits, int group, uint16_t* out) {
+  if (check_shape(N, K, bits, group)) return -1;
+  int wpr = K * bits / 32;
+  int G = K / group;
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k) {
+      double q = (double)code_at(W + (size_t)n * wpr, k, bits);
+      double sc = orc_half_to_double(scales[(size_t)n * G + k / group]);
+      double z = orc_half_to_double(zeros[(size_t)n * G + k / group]);
+      double w = (q - z) * sc; /* exact in binary64 */
+      out[(size_t)n * K + k] = w == 0.0 ? (uint16_t)0 : orc_double_to_half(w);
+    }
+  return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* The quantized GEMM                                                   */
 /* ------------------------------------------------------------------ */

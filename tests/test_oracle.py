@@ -156,6 +156,43 @@ def test_dequant_exact(bits, group):
             assert Fraction(w[n, k]) == exact
 
 
+def _body_weights(rng, N, K, bits, group):
+    """Codes with scales and zeros that stress the rounding: signed, tiny (subnormal), huge, and
+    zero points that are tiny next to the codes."""
+    G = K // group
+    codes = rng.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    s = rng.choice([1.0, -1.0], (N, G)) * rng.choice([3e-7, 1e-4, 0.0123, 0.7, 300.0, 30000.0], (N, G))
+    z = rng.choice([6e-8, 1e-5, 0.37, 7.3, -11.0, 2000.0], (N, G)) * rng.uniform(0.5, 1.5, (N, G))
+    return codes, s.astype(np.float16), z.astype(np.float16)
+
+
+@pytest.mark.parametrize("bits,group", [(4, 32), (2, 64)])
+def test_dequant_half_is_exact_value_rounded_once(bits, group):
+    """Every FP16 body weight is the exact rational (q - z) * s rounded by the independent RNE search
+    (overflow to inf), with +0 for an exact zero."""
+    rng = np.random.default_rng(bits)
+    N, K = 24, 256
+    codes, s, z = _body_weights(rng, N, K, bits, group)
+    W = oracle.pack(codes, bits)
+    with np.errstate(over="ignore"):
+        body = oracle.dequant_half(W, s, z, K, bits, group).view(np.uint16)
+    for n in range(N):
+        for k in range(K):
+            g = k // group
+            exact = (Fraction(int(codes[n, k])) - half_frac(z[n, g])) * half_frac(s[n, g])
+            want = 0 if exact == 0 else rne_half_bits(exact)
+            assert body[n, k] == want, (n, k, exact)
+
+
+def test_dequant_half_zero_is_positive():
+    """q == z gives +0 whatever the sign of the scale."""
+    codes = np.full((2, 64), 5, np.uint8)
+    W = oracle.pack(codes, 4)
+    s = np.array([[0.25, -0.25], [-3.0, 7.0]], np.float16)
+    z = np.full((2, 2), 5.0, np.float16)
+    assert np.all(oracle.dequant_half(W, s, z, 64, 4, 32).view(np.uint16) == 0)
+
+
 def test_dequant_special_cases():
     # s = 1, z = 0: w = q (plain integer codes)
     codes = np.arange(16, dtype=np.uint8).reshape(1, 16).repeat(2, 0)
