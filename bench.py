@@ -407,6 +407,9 @@ def run_tlq(args, rank, world, dist):
     # ---- secondary: loop block ----
     result["loop_block"] = run_loop_block(tlq, torch)
 
+    # ---- secondary: FP16 body cache (dequant kernel + a plain FP16 GEMM) ----
+    result["fp16_body"] = run_fp16_body(tlq, torch, peaks, l2)
+
     # ---- secondary: INT4 -> INT2 re-quantization of the loop block (tier switch) ----
     result["requant"] = run_requant(tlq, torch, peaks, l2)
 
@@ -551,6 +554,80 @@ def run_loop_block(tlq, torch):
                             "TFLOPs": round(L * 2 * M * macs / (ms * 1e-3) / 1e12, 2)}
                         del g
                     del blk, proj
+    except tlq.TLQError as e:
+        out["unavailable"] = str(e)
+    return out
+
+
+def run_fp16_body(tlq, torch, peaks, l2):
+    """The FP16 body cache as a comparison point: tl_dequant_fp16 on the four
+    D=2048 projections (INT4 group 128, rotating copies so every launch reads
+    HBM), then the step's GEMMs as plain FP16 GEMMs on the bodies (cuBLAS
+    through torch.matmul, FP32 accumulation) against the quantized kernels at
+    the same M."""
+    group = 128
+    out = {}
+    try:
+        per_set = sum(N * K // 2 + 4 * N * K // group + 2 * N * K for (N, K) in synth.SHAPES.values())
+        ncopy = max(2, -(-2 * l2 // per_set))
+        sets = []
+        for c in range(ncopy):
+            rng = synth.rng_for(700 + c)
+            one = []
+            for name in synth.PROJ_ORDER:
+                N, K = synth.SHAPES[name]
+                codes, s, z = synth.quant_weights(rng, N, K, 4, group)
+                one.append((tlq.pack_weights(torch.from_numpy(codes).cuda(), 4), torch.from_numpy(s).cuda(),
+                            torch.from_numpy(z).cuda(), torch.empty((N, K), dtype=torch.float16, device="cuda")))
+            sets.append(one)
+
+        def deq(i):
+            for (W, s, z, body) in sets[i % ncopy]:
+                tlq.tl_dequant_fp16(W, s, z, body, 4, group)
+
+        for i in range(ncopy):
+            deq(i)
+        torch.cuda.synchronize()
+        reps = 4 * ncopy
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                deq(i)
+        t = time_graph_list(torch, [g], 5, 2)
+        us = t * 1e3 / (5 * reps)
+        gbps = per_set / (us * 1e-6) / 1e9
+        out["dequant"] = {"us_per_block": round(us, 2), "GBps": round(gbps, 1), "frac_of_hbm": round(gbps / peaks["hbm"], 3),
+                          "bytes_per_block": per_set, "launches_per_block": 4}
+        del g
+        # GEMMs: quantized path vs dense FP16 on the bodies (copy 0), one graph per M
+        for M in (1, 16, 128, 512, 2048):
+            A = {K: torch.randn((M, K), device="cuda").half() for K in {k for (_, k) in synth.SHAPES.values()}}
+            Cq = [torch.empty((M, N), dtype=torch.float16, device="cuda") for (N, _) in synth.SHAPES.values()]
+            q = sets[0]
+
+            def run_quant():
+                for (W, s, z, _), (N, K), C in zip(q, synth.SHAPES.values(), Cq):
+                    tlq.tl_quant_gemm(A[K], W, s, z, C, 4, group)
+
+            def run_dense():
+                for (_, _, _, body), (N, K), C in zip(q, synth.SHAPES.values(), Cq):
+                    torch.matmul(A[K], body.t(), out=C)
+
+            row = {}
+            for name, fn in (("quant", run_quant), ("dense_fp16", run_dense)):
+                fn()
+                torch.cuda.synchronize()
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    fn()
+                n = 20 if M >= 512 else 100
+                ms = time_graph_list(torch, [gr], n, 3) / n
+                flops = 2 * M * sum(N * K for (N, K) in synth.SHAPES.values())
+                row[name] = {"us": round(ms * 1e3, 2), "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 1)}
+                del gr
+            row["quant_speedup"] = round(row["dense_fp16"]["us"] / row["quant"]["us"], 2)
+            out["gemm_M%d" % M] = row
+            del A, Cq
     except tlq.TLQError as e:
         out["unavailable"] = str(e)
     return out

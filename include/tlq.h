@@ -220,6 +220,24 @@ tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const ui
                                 void* stream);
 
 /*
+ * tl_dequant_fp16 -- the FP16 body of a quantized weight: out[n][k] =
+ * fp16_RNE((q - z) * s), each weight rounded once from its exact value, +0
+ * for an exact zero.  Bit-exact and deterministic.
+ *
+ * Source: "Model", section "VRAM cost": the opt-in FP16 body cache (a dense
+ * FP16 copy of the loop-block weights, about 3x their quantized memory).
+ * This library offers it as a comparison point for the quantized GEMM: a
+ * plain FP16 GEMM on the body.
+ *   Wpacked, scales, zeros  as tl_quant_gemm (16-byte aligned Wpacked).
+ *   out     FP16 [N][K], row-major, 16-byte aligned, caller-owned; must not
+ *           overlap the inputs.
+ *   bits, group, N, K: the rules of tl_quant_gemm (N need not be a multiple
+ *   of 8).  Returns TLQ_OK, TLQ_EINVAL or TLQ_ECUDA.
+ */
+tlq_status tl_dequant_fp16(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t* zeros, uint16_t* out,
+                           int N, int K, int bits, int group, void* stream);
+
+/*
  * tl_interleave_rows -- out row 2i = row i of a, out row 2i+1 = row i of b
  * (device buffers of `rows` rows of `row_bytes` bytes; out holds 2*rows).
  * Lays out the gate and up weights (packed words, scales, zeros) for

@@ -162,6 +162,19 @@ def test_swiglu_entry_points_reject_bad_arguments(clib):
     assert "gate_up" in tlq.tl_last_error()
 
 
+def test_dequant_fp16_rejects_bad_arguments(clib):
+    import weight_only_int4_quant_gb300 as tlq
+
+    W, S, Z, O = 1 << 20, 2 << 20, 3 << 20, 4 << 20
+    assert clib.tl_dequant_fp16(None, S, Z, O, 8, 256, 4, 128, None) == tlq.TLQ_EINVAL
+    assert clib.tl_dequant_fp16(W, S, Z, O, 8, 256, 3, 128, None) == tlq.TLQ_EINVAL
+    assert clib.tl_dequant_fp16(W, S, Z, O, 8, 256, 2, 32, None) == tlq.TLQ_EINVAL
+    assert clib.tl_dequant_fp16(W, S, Z, O, 8, 200, 4, 128, None) == tlq.TLQ_EINVAL
+    assert clib.tl_dequant_fp16(W, S, Z, O + 8, 8, 256, 4, 128, None) == tlq.TLQ_EINVAL
+    assert clib.tl_dequant_fp16(W, S, Z, W + 16, 8, 256, 4, 128, None) == tlq.TLQ_EINVAL
+    assert "overlap" in tlq.tl_last_error()
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     import weight_only_int4_quant_gb300 as tlq
 

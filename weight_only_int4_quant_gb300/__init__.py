@@ -21,7 +21,7 @@ __all__ = [
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "gemm_descs", "quant_gemm", "pack_weights", "unpack_weights", "LoopBlock",
     "tl_requant_int4_to_int2", "tl_requant_int4_to_int2_batched", "requant_int4_to_int2",
     "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward", "quant_gemm_swiglu",
-    "interleave_rows", "SwiGLUBlock",
+    "interleave_rows", "SwiGLUBlock", "tl_dequant_fp16", "dequant_fp16",
 ]
 
 # every symbol include/tlq.h declares
@@ -30,6 +30,7 @@ EXPORTED = (
     "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "tl_requant_int4_to_int2",
     "tl_requant_int4_to_int2_batched", "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward",
+    "tl_dequant_fp16",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -112,6 +113,7 @@ def load():
             "tl_requant_int4_to_int2_batched": ([ctypes.POINTER(_RequantDesc), I, I, P], I),
             "tl_quant_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P], I),
             "tl_interleave_rows": ([P, P, P, I, ctypes.c_size_t, P], I),
+            "tl_dequant_fp16": ([P, P, P, P, I, I, I, I, P], I),
             "tl_swiglu_block_forward": ([P, ctypes.POINTER(_SwigluBlock), I, I, P], I),
         }
         for name, (args, res) in sigs.items():
@@ -232,6 +234,26 @@ def tl_quant_gemm_swiglu(A, Wgu, scales, zeros, C, bits: int, group: int, stream
                                           _dev(scales, (torch.float16,), "scales"),
                                           _dev(zeros, (torch.float16,), "zeros"), _dev(C, (torch.float16,), "C"),
                                           M, N2, K, bits, group, _stream(stream)))
+
+
+def tl_dequant_fp16(W, scales, zeros, out, bits: int, group: int, stream=None) -> None:
+    import torch
+
+    N, K = out.shape
+    if W.shape[0] != N or W.shape[1] * (32 // bits) != K:
+        raise ValueError("W [%d, %d] does not hold [%d, %d] INT%d weights" % (W.shape[0], W.shape[1], N, K, bits))
+    _raise_if(load().tl_dequant_fp16(_dev(W, (torch.int32, torch.uint32), "W"), _dev(scales, (torch.float16,), "scales"),
+                                     _dev(zeros, (torch.float16,), "zeros"), _dev(out, (torch.float16,), "out"),
+                                     N, K, bits, group, _stream(stream)))
+
+
+def dequant_fp16(W, scales, zeros, bits: int, group: int, stream=None):
+    """The FP16 body [N, K] of a packed weight (one rounding per weight)."""
+    import torch
+
+    out = torch.empty((W.shape[0], W.shape[1] * (32 // bits)), dtype=torch.float16, device=W.device)
+    tl_dequant_fp16(W, scales, zeros, out, bits, group, stream)
+    return out
 
 
 def tl_interleave_rows(a, b, out, stream=None) -> None:

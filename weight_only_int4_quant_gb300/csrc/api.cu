@@ -181,6 +181,20 @@ tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const ui
   return run_gemm(a, static_cast<cudaStream_t>(stream));
 }
 
+tlq_status tl_dequant_fp16(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t* zeros, uint16_t* out, int N,
+                           int K, int bits, int group, void* stream) {
+  g_msg[0] = 0;
+  if (!Wpacked || !scales || !zeros || !out) return set_error(TLQ_EINVAL, "tl_dequant_fp16: null pointer");
+  tlq_status st = check_gemm_shape(1, N, K, bits, group, "tl_dequant_fp16");
+  if (st != TLQ_OK) return st;
+  if (!aligned16(Wpacked) || !aligned16(out))
+    return set_error(TLQ_EINVAL, "tl_dequant_fp16: Wpacked and out must be 16-byte aligned");
+  const size_t ob = (size_t)N * K * 2, wb = (size_t)N * K * bits / 8, gb = (size_t)N * (K / group) * 2;
+  if (overlaps(out, ob, Wpacked, wb) || overlaps(out, ob, scales, gb) || overlaps(out, ob, zeros, gb))
+    return set_error(TLQ_EINVAL, "tl_dequant_fp16: out overlaps an input");
+  return launch_body(Wpacked, scales, zeros, out, N, K, bits, group, static_cast<cudaStream_t>(stream));
+}
+
 tlq_status tl_interleave_rows(const void* a, const void* b, void* out, int rows, size_t row_bytes, void* stream) {
   g_msg[0] = 0;
   if (!a || !b || !out) return set_error(TLQ_EINVAL, "tl_interleave_rows: null pointer");

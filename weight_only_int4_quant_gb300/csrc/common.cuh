@@ -359,6 +359,8 @@ struct RequantArgs {
   int N, K;
 };
 tlq_status launch_requant(const RequantArgs* a, int count, int group, cudaStream_t stream);
+tlq_status launch_body(const uint32_t* W, const uint16_t* s, const uint16_t* z, uint16_t* out, int N, int K, int bits,
+                       int group, cudaStream_t stream);
 tlq_status launch_rmsnorm(const float* x, __half* h, int M, int D, int normalize, cudaStream_t stream);
 tlq_status launch_timeout_probe(uint32_t limit_us, cudaStream_t stream);
 
