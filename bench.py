@@ -407,6 +407,9 @@ def run_tlq(args, rank, world, dist):
     # ---- secondary: loop block ----
     result["loop_block"] = run_loop_block(tlq, torch)
 
+    # ---- secondary: chunked prefill of the loop block ----
+    result["chunked_prefill"] = run_chunked_prefill(tlq, torch)
+
     # ---- secondary: FP16 body cache (dequant kernel + a plain FP16 GEMM) ----
     result["fp16_body"] = run_fp16_body(tlq, torch, peaks, l2)
 
@@ -554,6 +557,41 @@ def run_loop_block(tlq, torch):
                             "TFLOPs": round(L * 2 * M * macs / (ms * 1e-3) / 1e12, 2)}
                         del g
                     del blk, proj
+    except tlq.TLQError as e:
+        out["unavailable"] = str(e)
+    return out
+
+
+def run_chunked_prefill(tlq, torch, S=1024, L=4):
+    """Chunked prefill of an S-token prompt through the D=2048 SwiGLU block
+    (INT4, L iterations): time and scratch memory per chunk size against
+    single-shot, each run captured in one CUDA graph (the launch count grows
+    with the number of chunks)."""
+    out = {"prompt_tokens": S, "L": L}
+    try:
+        case = synth.swiglu_block_case(S, 4, seed=9)
+        proj = {name: (tlq.pack_weights(torch.from_numpy(c).cuda(), 4), torch.from_numpy(s).cuda(),
+                       torch.from_numpy(z).cuda()) for name, (c, s, z) in case["proj"].items()}
+        x0 = torch.from_numpy(case["x0"]).cuda()
+        D, F = case["D"], case["F"]
+        base = None
+        for chunk in (0, 512, 256, 128, 64):
+            rows = S if chunk == 0 else chunk
+            blk = tlq.SwiGLUBlock(proj, 4, case["group"], rows)
+            x = x0.clone()
+            blk.forward(x, L, chunk=chunk)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                blk.forward(x, L, chunk=chunk)
+            ms = time_graph_list(torch, [g], 10, 2) / 10
+            nchunks = 1 if chunk == 0 else -(-S // chunk)
+            if base is None:
+                base = ms
+            out["single" if chunk == 0 else "chunk%d" % chunk] = {
+                "ms": round(ms, 3), "overhead_pct": round(100.0 * (ms / base - 1.0), 1),
+                "launches": nchunks * L * 5, "scratch_MB": round(2 * rows * (5 * D + F) / 1e6, 2)}
+            del g, blk
     except tlq.TLQError as e:
         out["unavailable"] = str(e)
     return out

@@ -335,6 +335,27 @@ tlq_status tl_loop_block_forward(float* x, const tl_block* block, int L, int M, 
 tlq_status tl_swiglu_block_forward(float* x, const tl_swiglu_block* block, int L, int M, void* stream);
 
 /*
+ * tl_loop_block_forward_chunked / tl_swiglu_block_forward_chunked -- chunked
+ * prefill: the M rows of x are split into chunks of `chunk` rows and each
+ * chunk runs through all L iterations before the next one starts, so the
+ * scratch buffers need only min(chunk, M) rows.
+ *
+ * Source: "Model", section "Chunked prefill": prompts longer than
+ * prefill_chunk are split into chunks that each run through all blocks and
+ * loop iterations in turn; the buffer VRAM shrinks with the chunk while the
+ * launch count grows with the number of chunks.  The block's rows are
+ * independent (no attention on this path), so every chunk is the block on a
+ * row slice; results match single-shot within the GEMM tolerance (the kernel
+ * choice and summation order depend on the row count: M <= 16 takes the
+ * decode kernel).
+ *   chunk <= 0 or chunk >= M: single shot.  Other arguments and errors as the
+ *   unchunked calls; scratch rows must cover min(chunk, M).
+ */
+tlq_status tl_loop_block_forward_chunked(float* x, const tl_block* block, int L, int M, int chunk, void* stream);
+tlq_status tl_swiglu_block_forward_chunked(float* x, const tl_swiglu_block* block, int L, int M, int chunk,
+                                           void* stream);
+
+/*
  * tl_loop_block_forward_static_scratch -- tl_loop_block_forward for callers
  * that cannot allocate device memory or provide scratch buffers (a serving
  * runtime that forbids allocation after start-up, a plugin interface that only

@@ -22,6 +22,7 @@ __all__ = [
     "tl_requant_int4_to_int2", "tl_requant_int4_to_int2_batched", "requant_int4_to_int2",
     "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward", "quant_gemm_swiglu",
     "interleave_rows", "SwiGLUBlock", "tl_dequant_fp16", "dequant_fp16",
+    "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
 ]
 
 # every symbol include/tlq.h declares
@@ -30,7 +31,7 @@ EXPORTED = (
     "tl_loop_block_forward", "tl_check_status", "tl_reset_status", "tl_selftest_wait_timeout",
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "tl_requant_int4_to_int2",
     "tl_requant_int4_to_int2_batched", "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward",
-    "tl_dequant_fp16",
+    "tl_dequant_fp16", "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -114,6 +115,8 @@ def load():
             "tl_quant_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P], I),
             "tl_interleave_rows": ([P, P, P, I, ctypes.c_size_t, P], I),
             "tl_dequant_fp16": ([P, P, P, P, I, I, I, I, P], I),
+            "tl_loop_block_forward_chunked": ([P, ctypes.POINTER(_Block), I, I, I, P], I),
+            "tl_swiglu_block_forward_chunked": ([P, ctypes.POINTER(_SwigluBlock), I, I, I, P], I),
             "tl_swiglu_block_forward": ([P, ctypes.POINTER(_SwigluBlock), I, I, P], I),
         }
         for name, (args, res) in sigs.items():
@@ -298,6 +301,28 @@ def tl_loop_block_forward(x, block: "LoopBlock", L: int, stream=None) -> None:
                                            _stream(stream)))
 
 
+def _rows_for(block, M, chunk):
+    rows = M if chunk <= 0 or chunk >= M else chunk
+    if rows > block.max_rows:
+        raise ValueError("%d rows per pass, the block's scratch holds %d" % (rows, block.max_rows))
+
+
+def tl_loop_block_forward_chunked(x, block: "LoopBlock", L: int, chunk: int, stream=None) -> None:
+    import torch
+
+    _rows_for(block, x.shape[0], chunk)
+    _raise_if(load().tl_loop_block_forward_chunked(_dev(x, (torch.float32,), "x"), ctypes.byref(block._c), L,
+                                                   x.shape[0], chunk, _stream(stream)))
+
+
+def tl_swiglu_block_forward_chunked(x, block: "SwiGLUBlock", L: int, chunk: int, stream=None) -> None:
+    import torch
+
+    _rows_for(block, x.shape[0], chunk)
+    _raise_if(load().tl_swiglu_block_forward_chunked(_dev(x, (torch.float32,), "x"), ctypes.byref(block._c), L,
+                                                     x.shape[0], chunk, _stream(stream)))
+
+
 def tl_loop_block_forward_static_scratch(x, block: "LoopBlock", L: int, stream=None) -> None:
     """tl_loop_block_forward with the intermediates in the library's static
     device scratch (no caller buffers, no allocation); the block's own scratch
@@ -444,8 +469,12 @@ class LoopBlock:
         self._bind()
         return self
 
-    def forward(self, x, L: int, stream=None):
-        tl_loop_block_forward(x, self, L, stream)
+    def forward(self, x, L: int, stream=None, chunk: int = 0):
+        """L iterations on x in place; chunk > 0 runs chunked prefill."""
+        if chunk > 0:
+            tl_loop_block_forward_chunked(x, self, L, chunk, stream)
+        else:
+            tl_loop_block_forward(x, self, L, stream)
         return x
 
 
@@ -492,10 +521,14 @@ class SwiGLUBlock:
         c.normalize = 1 if self.normalize else 0
         self._c = c
 
-    def forward(self, x, L: int, stream=None):
+    def forward(self, x, L: int, stream=None, chunk: int = 0):
+        """L iterations on x in place; chunk > 0 runs chunked prefill."""
         import torch
 
         M = x.shape[0]
+        if chunk > 0:
+            tl_swiglu_block_forward_chunked(x, self, L, chunk, stream)
+            return x
         if M > self.max_rows:
             raise ValueError("x has %d rows, the block's scratch holds %d" % (M, self.max_rows))
         _raise_if(load().tl_swiglu_block_forward(_dev(x, (torch.float32,), "x"), ctypes.byref(self._c), L, M,

@@ -456,6 +456,37 @@ tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void
   return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// Chunk-first prefill: rows [r0, r0 + chunk) run through all L iterations,
+// then the next chunk, with scratch for `chunk` rows only.
+tlq_status block_forward_chunked(float* x, const BlockSpec& s, int L, int M, int chunk, cudaStream_t stream) {
+  if (M < 1) return set_error(TLQ_EINVAL, "%s: M=%d (must be >= 1)", s.who, M);
+  if (chunk <= 0 || chunk > M) chunk = M;
+  for (int r0 = 0; r0 < M; r0 += chunk) {
+    const int rows = M - r0 < chunk ? M - r0 : chunk;
+    tlq_status st = block_forward(x + (size_t)r0 * s.D, s, L, rows, stream);
+    if (st != TLQ_OK) return st;
+  }
+  return TLQ_OK;
+}
+}  // namespace
+
+tlq_status tl_loop_block_forward_chunked(float* x, const tl_block* b, int L, int M, int chunk, void* stream) {
+  g_msg[0] = 0;
+  if (!x || !b) return set_error(TLQ_EINVAL, "tl_loop_block_forward_chunked: null x or block");
+  const BlockSpec s = {{&b->qkv, &b->o, &b->up, &b->down}, b->bits, b->group, b->D, b->up.N, false,
+                       b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, "tl_loop_block_forward_chunked"};
+  return block_forward_chunked(x, s, L, M, chunk, static_cast<cudaStream_t>(stream));
+}
+
+tlq_status tl_swiglu_block_forward_chunked(float* x, const tl_swiglu_block* b, int L, int M, int chunk, void* stream) {
+  g_msg[0] = 0;
+  if (!x || !b) return set_error(TLQ_EINVAL, "tl_swiglu_block_forward_chunked: null x or block");
+  const BlockSpec s = {{&b->qkv, &b->o, &b->gate_up, &b->down}, b->bits, b->group, b->D, b->gate_up.N / 2, true,
+                       b->h, b->qkv_out, b->o_out, b->act_out, b->normalize, "tl_swiglu_block_forward_chunked"};
+  return block_forward_chunked(x, s, L, M, chunk, static_cast<cudaStream_t>(stream));
+}
+
 tlq_status tl_swiglu_block_forward(float* x, const tl_swiglu_block* b, int L, int M, void* stream) {
   g_msg[0] = 0;
   if (!x || !b) return set_error(TLQ_EINVAL, "tl_swiglu_block_forward: null x or block");
