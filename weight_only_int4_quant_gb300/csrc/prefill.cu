@@ -75,7 +75,14 @@ struct PrefillParams {
   int kslice;  // k per cluster rank (multiple of BK)
   int ksplit;
   int l2_keep;  // stream the weights evict-last (kept in L2)
+  int szvec;    // K/group % 8 == 0 and 16-byte aligned scale/zero arrays: 8 groups per 16-byte load
 };
+
+// Half i (0..7) of a 16-byte vector, as the low 16 bits.
+__device__ __forceinline__ uint32_t pick16(const uint4& v, int i) {
+  const uint32_t w = (i & 4) ? ((i & 2) ? v.w : v.z) : ((i & 2) ? v.y : v.x);
+  return (i & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
 
 // Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row atoms of
 // 1024 bytes (stride byte offset 1024), descriptor version 1.
@@ -310,9 +317,30 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const __half* zrow = p.Z + (size_t)(row_ok ? n : 0) * G;
     const bool two_groups = (BITS == 4) && (p.group < BK);  // INT4 with group 32
 
-    // raw 16-bit scale/zero bits, kPrefetch stages ahead (the half2 broadcast
-    // happens at use, so no load is waited on at issue); the packed words come
-    // through the TMA ring
+    // Scales/zeros.  Vector path (szvec): each thread holds its row's values
+    // for a window of 8 groups in one 16-byte load per array, and the next
+    // window in flight: one load pair per 8 groups instead of scattered 2-byte
+    // loads every stage (those each touch 32 sectors per warp and crowd the
+    // L1 that the dequantized tiles go through).  Otherwise: raw 16-bit bits,
+    // kPrefetch stages ahead (the half2 broadcast happens at use, so no load
+    // is waited on at issue).  The packed words come through the TMA ring.
+    const bool szvec = p.szvec != 0;
+    uint4 sv = make_uint4(0, 0, 0, 0), zv = sv, svn = sv, zvn = sv;
+    int win = 0;
+    auto load_win = [&](int w, uint4& s4, uint4& z4) {
+      if (row_ok && 8 * w < G) {
+        s4 = __ldg(reinterpret_cast<const uint4*>(srow) + w);
+        z4 = __ldg(reinterpret_cast<const uint4*>(zrow) + w);
+      } else {
+        s4 = make_uint4(0, 0, 0, 0);
+        z4 = s4;
+      }
+    };
+    if (szvec) {
+      win = (k0 / p.group) >> 3;
+      load_win(win, sv, zv);
+      load_win(win + 1, svn, zvn);
+    }
     unsigned short sring[kPrefetch][2], zring[kPrefetch][2];
     auto issue = [&](int kb, unsigned short (&sd)[2], unsigned short (&zd)[2]) {
       const int ks = k0 + kb * BK;
@@ -327,7 +355,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     };
 #pragma unroll
     for (int j = 0; j < kPrefetch; ++j)
-      if (j < nkb) issue(j, sring[j], zring[j]);
+      if (!szvec && j < nkb) issue(j, sring[j], zring[j]);
 
     bool ok = true;
     for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
@@ -335,10 +363,31 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       for (int j = 0; j < kPrefetch; ++j) {
         const int kb = kb0 + j;
         if (kb < nkb && ok) {
-          const uint32_t s_lo = bcast16(sring[j][0]), s_hi = bcast16(sring[j][1]);
-          const uint32_t nzs_lo = hmul2u(bcast16(zring[j][0]), s_lo) ^ 0x80008000u;  // -(z * s)
-          const uint32_t nzs_hi = hmul2u(bcast16(zring[j][1]), s_hi) ^ 0x80008000u;
-          if (kb + kPrefetch < nkb) issue(kb + kPrefetch, sring[j], zring[j]);
+          uint32_t s_lo, s_hi, z_lo, z_hi;
+          if (szvec) {
+            const int g0 = (k0 + kb * BK) / p.group;
+            if ((g0 >> 3) > win) {  // a stage spans at most two groups: the window moves by one
+              sv = svn;
+              zv = zvn;
+              ++win;
+              load_win(win + 1, svn, zvn);
+            }
+            // with two groups per stage g0 is even, so g0 + 1 stays in the window
+            s_lo = pick16(sv, g0 & 7);
+            z_lo = pick16(zv, g0 & 7);
+            s_hi = two_groups ? pick16(sv, (g0 + 1) & 7) : s_lo;
+            z_hi = two_groups ? pick16(zv, (g0 + 1) & 7) : z_lo;
+          } else {
+            s_lo = sring[j][0];
+            s_hi = sring[j][1];
+            z_lo = zring[j][0];
+            z_hi = zring[j][1];
+            if (kb + kPrefetch < nkb) issue(kb + kPrefetch, sring[j], zring[j]);
+          }
+          s_lo = bcast16((unsigned short)s_lo);
+          s_hi = bcast16((unsigned short)s_hi);
+          const uint32_t nzs_lo = hmul2u(bcast16((unsigned short)z_lo), s_lo) ^ 0x80008000u;  // -(z * s)
+          const uint32_t nzs_hi = hmul2u(bcast16((unsigned short)z_hi), s_hi) ^ 0x80008000u;
           // this stage's packed words: row r of the TMA tile (INT4: two 16-byte
           // chunks, swapped in rows with bit 2 set by SWIZZLE_32B; INT2: one)
           const int ws = kb % kWStages;
@@ -608,6 +657,8 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   p.K = a.K;
   p.group = a.group;
   p.l2_keep = a.l2_keep;
+  p.szvec = ((a.K / a.group) % 8 == 0 && (reinterpret_cast<uintptr_t>(a.S) & 15) == 0 &&
+             (reinterpret_cast<uintptr_t>(a.Z) & 15) == 0) ? 1 : 0;
   p.kslice = per2 * BK;
   p.ksplit = (a.K + p.kslice - 1) / p.kslice;
   if (p.ksplit != ksplit) return set_error(TLQ_EINVAL, "prefill: inconsistent k split");
