@@ -323,7 +323,7 @@ def kernel_hash():
 # dram bytes (read + write) per launch of the decode kernel for the headline
 # step, from the ncu capture summarised in profiles/ (None until captured for
 # the current kernel source).
-NCU_TRAFFIC = {"kernel_hash": "502021166b4bac36", "bytes_per_step": 82782720}  # profiles/decode_kernel_int4_decode_step.md
+NCU_TRAFFIC = {"kernel_hash": "39b90f8262af834c", "bytes_per_step": 82625280}  # profiles/decode_kernel_int4_decode_step.md
 
 
 def run_tlq(args, rank, world, dist):

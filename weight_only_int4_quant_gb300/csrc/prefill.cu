@@ -42,22 +42,30 @@ constexpr int kThreadsP = 10 * 32;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int kPrefetch = 3;          // scale/zero global-load distance (stages)
-constexpr int kWStages = 4;           // packed-weight TMA ring depth
 constexpr int W_STAGE_MAX = BN * BK * 4 / 8;  // packed bytes of one stage (INT4: 32 bytes per row)
 
+// Ring depths, each with its own full/empty barriers: activations (SA, TMA),
+// dequantized weights (SB, written by the dequantizing warps) and packed
+// weights (SW, TMA).  Measured on GB300: with two token tiles a 2-deep B ring
+// that frees shared memory for a 4-deep A ring is about 4% faster than 3/3;
+// with one token tile 4/4/4 is best (6/2/6 was 5% slower).
 template <int NMT>
 struct PCfg {
-  static constexpr int STAGES = NMT == 1 ? 4 : 3;
-  static constexpr int STAGE = NMT * A_STAGE + B_STAGE;
+  static constexpr int SA = 4;
+  static constexpr int SB = NMT == 1 ? 4 : 2;
+  static constexpr int SW = 4;
+  static constexpr int RING = SA * NMT * A_STAGE + SB * B_STAGE;  // A and B rings (also the split-K slots)
+  static constexpr int SMEM = 1024 + RING + SW * W_STAGE_MAX + 256;
   static constexpr uint32_t TMEM_COLS = 256u * NMT;
 };
 
 static_assert(BN == kDqWarps * 32, "one dequant thread per weight row");
-static_assert(PCfg<1>::STAGES * PCfg<1>::STAGE + kWStages * W_STAGE_MAX + 1024 + 256 <= 232448, "shared memory");
-static_assert(PCfg<2>::STAGES * PCfg<2>::STAGE + kWStages * W_STAGE_MAX + 1024 + 256 <= 232448, "shared memory");
+static_assert(PCfg<1>::SMEM <= 232448 && PCfg<2>::SMEM <= 232448, "shared memory");
+static_assert((2 * PCfg<1>::SA + 2 * PCfg<1>::SB + 1 + 2 * PCfg<1>::SW) * 8 + 4 <= 256, "barriers fit");
+static_assert((2 * PCfg<2>::SA + 2 * PCfg<2>::SB + 1 + 2 * PCfg<2>::SW) * 8 + 4 <= 256, "barriers fit");
 // split-K slots: ksplit x BM rows x (BN / ksplit + 4) floats, largest at ksplit = 8
-static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::STAGES * PCfg<1>::STAGE, "split-K slots fit in the stages");
-static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<2>::STAGES * PCfg<2>::STAGE, "split-K slots fit in the stages");
+static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::RING, "split-K slots fit in the rings");
+static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<2>::RING, "split-K slots fit in the rings");
 
 // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16,
 // both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -199,7 +207,7 @@ template <int BITS, int EPI, int NMT>
 __global__ void __launch_bounds__(kThreadsP, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
                    const PrefillParams p) {
-  constexpr int kStagesP = PCfg<NMT>::STAGES;
+  constexpr int SA = PCfg<NMT>::SA, SB = PCfg<NMT>::SB, SW = PCfg<NMT>::SW;
   constexpr uint32_t kTmemCols = PCfg<NMT>::TMEM_COLS;
   constexpr int CPW = 32 / BITS;
   constexpr int WPS = BK / CPW;                 // packed words per row per stage (8 or 4)
@@ -208,18 +216,19 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sa = smem;                                // [stage][NMT][A_STAGE]
+  uint8_t* sa = smem;                                // [SA][NMT][A_STAGE]
   constexpr int W_STAGE = BN * BK * BITS / 8;        // packed weights of one stage
-  uint8_t* sb = smem + kStagesP * NMT * A_STAGE;     // [stage][B_STAGE]
-  uint8_t* sw = sb + kStagesP * B_STAGE;             // [kWStages][BN rows][BK * BITS / 8 bytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sw + kWStages * W_STAGE_MAX);
-  uint64_t* full_a = bars;
-  uint64_t* full_b = bars + kStagesP;
-  uint64_t* empty = bars + 2 * kStagesP;
-  uint64_t* accum = bars + 3 * kStagesP;
-  uint64_t* wfull = accum + 1;           // [kWStages] packed tile landed (TMA)
-  uint64_t* wempty = wfull + kWStages;   // [kWStages] the dequant warps read it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + kWStages);
+  uint8_t* sb = smem + SA * NMT * A_STAGE;           // [SB][B_STAGE]
+  uint8_t* sw = sb + SB * B_STAGE;                   // [SW][BN rows][BK * BITS / 8 bytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sw + SW * W_STAGE_MAX);
+  uint64_t* full_a = bars;                // [SA] activation tile landed (TMA)
+  uint64_t* empty_a = full_a + SA;        // [SA] the MMAs that read it completed
+  uint64_t* full_b = empty_a + SA;        // [SB] dequantized weights written
+  uint64_t* empty_b = full_b + SB;        // [SB] the MMAs that read them completed
+  uint64_t* accum = empty_b + SB;
+  uint64_t* wfull = accum + 1;            // [SW] packed tile landed (TMA)
+  uint64_t* wempty = wfull + SW;          // [SW] the dequant warps read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + SW);
   float* red = reinterpret_cast<float*>(smem);  // split-K slots, after the main loop
 
   const int warp = threadIdx.x >> 5;
@@ -232,13 +241,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   const int nkb = (klen + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStagesP; ++i) {
+    for (int i = 0; i < SA; ++i) {
       mbar_init(&full_a[i], 1);
+      mbar_init(&empty_a[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
       mbar_init(&full_b[i], kDqWarps);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty_b[i], 1);
     }
     mbar_init(accum, 1);
-    for (int i = 0; i < kWStages; ++i) {
+    for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], kDqWarps);
     }
@@ -258,29 +270,29 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       tma_prefetch_desc(&amap);
       pdl_wait();  // A may be written by the preceding kernel
       for (int kb = 0; kb < nkb; ++kb) {
-        const int slot = kb % kStagesP;
-        if (!mbar_wait(&empty[slot], ((kb / kStagesP) & 1) ^ 1, 0x201)) break;
+        const int slot = kb % SA;
+        if (!mbar_wait(&empty_a[slot], ((kb / SA) & 1) ^ 1, 0x201)) break;
         mbar_arrive_expect_tx(&full_a[slot], NMT * A_STAGE);
 #pragma unroll
         for (int i = 0; i < NMT; ++i)
           tma_load_2d(&amap, &full_a[slot], sa + (slot * NMT + i) * A_STAGE, k0 + kb * BK, m0 + i * BM);
       }
-      for (int kb = max(0, nkb - kStagesP); kb < nkb; ++kb)
-        if (!mbar_wait(&full_a[kb % kStagesP], (kb / kStagesP) & 1, 0x202)) break;
+      for (int kb = max(0, nkb - SA); kb < nkb; ++kb)
+        if (!mbar_wait(&full_a[kb % SA], (kb / SA) & 1, 0x202)) break;
     } else if (lane == 16) {
       // ---------------- packed weights: TMA producer (no dependency wait: weights are inputs) ----------------
       tma_prefetch_desc(&wmap);
       for (int kb = 0; kb < nkb; ++kb) {
-        const int ws = kb % kWStages;
-        if (!mbar_wait(&wempty[ws], ((kb / kWStages) & 1) ^ 1, 0x208)) break;
+        const int ws = kb % SW;
+        if (!mbar_wait(&wempty[ws], ((kb / SW) & 1) ^ 1, 0x208)) break;
         mbar_arrive_expect_tx(&wfull[ws], W_STAGE);
         if (p.l2_keep)
           tma_load_2d_hint(&wmap, &wfull[ws], sw + ws * W_STAGE, (k0 + kb * BK) * BITS / 32, n0, policy_evict_last());
         else
           tma_load_2d(&wmap, &wfull[ws], sw + ws * W_STAGE, (k0 + kb * BK) * BITS / 32, n0);
       }
-      for (int kb = max(0, nkb - kWStages); kb < nkb; ++kb)
-        if (!mbar_wait(&wfull[kb % kWStages], (kb / kWStages) & 1, 0x209)) break;
+      for (int kb = max(0, nkb - SW); kb < nkb; ++kb)
+        if (!mbar_wait(&wfull[kb % SW], (kb / SW) & 1, 0x209)) break;
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -288,21 +300,21 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     if (lane == 0) {
       bool ok = true;
       for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int slot = kb % kStagesP;
-        const uint32_t par = (kb / kStagesP) & 1;
-        ok = mbar_wait(&full_a[slot], par, 0x203) && mbar_wait(&full_b[slot], par, 0x204);
+        const int as = kb % SA, bs = kb % SB;
+        ok = mbar_wait(&full_a[as], (kb / SA) & 1, 0x203) && mbar_wait(&full_b[bs], (kb / SB) & 1, 0x204);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t b0 = smem_u32(sb + slot * B_STAGE);
+        const uint32_t b0 = smem_u32(sb + bs * B_STAGE);
 #pragma unroll
         for (int i = 0; i < NMT; ++i) {
-          const uint32_t a0 = smem_u32(sa + (slot * NMT + i) * A_STAGE);
+          const uint32_t a0 = smem_u32(sa + (as * NMT + i) * A_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk)
             umma_f16(tmem + 256u * i, sw128_desc(a0 + kk * UMMA_K * 2), sw128_desc(b0 + kk * UMMA_K * 2),
                      (kb | kk) != 0);
         }
-        umma_commit(&empty[slot]);
+        umma_commit(&empty_a[as]);  // each commit tracks every MMA issued so far
+        umma_commit(&empty_b[bs]);
       }
       umma_commit(accum);
     }
@@ -390,8 +402,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           const uint32_t nzs_hi = hmul2u(bcast16((unsigned short)z_hi), s_hi) ^ 0x80008000u;
           // this stage's packed words: row r of the TMA tile (INT4: two 16-byte
           // chunks, swapped in rows with bit 2 set by SWIZZLE_32B; INT2: one)
-          const int ws = kb % kWStages;
-          if (!mbar_wait(&wfull[ws], (kb / kWStages) & 1, 0x207)) {
+          const int ws = kb % SW;
+          if (!mbar_wait(&wfull[ws], (kb / SW) & 1, 0x207)) {
             ok = false;
             break;
           }
@@ -406,8 +418,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
               cur[0] = lds128(wr);
             }
           }
-          const int slot = kb % kStagesP;
-          if (!mbar_wait(&empty[slot], ((kb / kStagesP) & 1) ^ 1, 0x205)) {
+          const int slot = kb % SB;
+          if (!mbar_wait(&empty_b[slot], ((kb / SB) & 1) ^ 1, 0x205)) {
             ok = false;
             break;
           }
@@ -676,7 +688,7 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (st != TLQ_OK) return st;
 
-  const size_t smem = 1024 + (size_t)PCfg<NMT>::STAGES * PCfg<NMT>::STAGE + (size_t)kWStages * W_STAGE_MAX + 256;
+  const size_t smem = (size_t)PCfg<NMT>::SMEM;
   auto kern = prefill_kernel<BITS, EPI, NMT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
