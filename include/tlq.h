@@ -118,6 +118,24 @@ typedef struct {
 tlq_status tl_quant_gemm_batched(const tl_gemm_desc* descs, int count, void* stream);
 
 /*
+ * tl_quant_gemm_batched_host -- tl_quant_gemm_batched on HOST activations and
+ * outputs: one host -> device copy of the step's activations, the batched
+ * GEMMs, one device -> host copy of the outputs, in that order on `stream`.
+ * Same source passages as tl_quant_gemm.
+ *   hostA   a_bytes of activations (pinned host memory for asynchronous
+ *           copies; pageable memory works but the copy blocks the caller).
+ *   devA    device staging of a_bytes; every descriptor's A lies inside it.
+ *   hostC   c_bytes of outputs (pinned host memory); written when the stream
+ *           reaches the copy.
+ *   devC    device staging of c_bytes; every descriptor's C lies inside it.
+ *   Calls on two streams with two staging sets overlap one call's copies with
+ *   the other's GEMMs.  Returns the errors of tl_quant_gemm_batched, TLQ_EINVAL
+ *   for null or misplaced buffers, TLQ_ECUDA for a failed copy.
+ */
+tlq_status tl_quant_gemm_batched_host(const tl_gemm_desc* descs, int count, const void* hostA, void* devA,
+                                      size_t a_bytes, void* hostC, const void* devC, size_t c_bytes, void* stream);
+
+/*
  * tl_pack_weights -- pack quantization codes into the kernels' weight format.
  *
  * Source: "beta-Informed Deployment Features", CTX-TIER, "Details of the

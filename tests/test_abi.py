@@ -175,6 +175,27 @@ def test_dequant_fp16_rejects_bad_arguments(clib):
     assert "overlap" in tlq.tl_last_error()
 
 
+def test_batched_host_rejects_bad_arguments_before_copying(clib):
+    import weight_only_int4_quant_gb300 as tlq
+
+    hA, dA, hC, dC = 1 << 20, 2 << 20, 3 << 20, 4 << 20
+    D = tlq._GemmDesc
+    good = D(dA, 5 << 20, 6 << 20, 7 << 20, dC, 1, 64, 256, 4, 128)
+
+    def call(descs, n=1, **kw):
+        a = dict(hA=hA, dA=dA, ab=4096, hC=hC, dC=dC, cb=4096)
+        a.update(kw)
+        return clib.tl_quant_gemm_batched_host(descs, n, a["hA"], a["dA"], a["ab"], a["hC"], a["dC"], a["cb"], None)
+
+    one = (D * 1)(good)
+    assert call(one, hA=None) == tlq.TLQ_EINVAL
+    assert call(one, dC=dA + 64) == tlq.TLQ_EINVAL and "overlap" in tlq.tl_last_error()
+    assert call(one, ab=256) == tlq.TLQ_EINVAL and "inside devA" in tlq.tl_last_error()  # A needs 512 bytes
+    bad_bits = (D * 1)(D(dA, 5 << 20, 6 << 20, 7 << 20, dC, 1, 64, 256, 3, 128))
+    assert call(bad_bits) == tlq.TLQ_EINVAL and "bits" in tlq.tl_last_error()
+    assert call(one, n=0) == tlq.TLQ_EINVAL
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     import weight_only_int4_quant_gb300 as tlq
 

@@ -329,3 +329,42 @@ def test_batched_many_problems_and_errors(lib):
     with pytest.raises(lib.TLQError, match="overlap"):
         lib.tl_quant_gemm_batched([(p0["A"], p0["W"], p0["s"], p0["z"], p0["C"], 4, 128),
                                    (p1["A"], p1["W"], p1["s"], p1["z"], p0["C"], 4, 128)])
+
+
+def test_batched_host_buffers_equal_device_call(lib):
+    """tl_quant_gemm_batched_host (host activations in, host outputs out) gives
+    the device call's outputs bit for bit, also when two calls alternate
+    between two streams and two staging sets."""
+    shapes = [(1, 256, 1024), (4, 512, 2048), (16, 256, 1024)]
+    rng = np.random.default_rng(9)
+    probs = []
+    for (M, N, K) in shapes:
+        case = synth.gemm_case(M, N, K, 4, 128, seed=M + N)
+        probs.append((case, lib.pack_weights(dev(case["codes"]), 4), dev(case["scales"]), dev(case["zeros"])))
+    na = sum(M * K for (M, N, K) in shapes)
+    nc = sum(M * N for (M, N, K) in shapes)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    sets = []
+    for b in range(2):
+        dA = torch.empty(na, dtype=torch.float16, device="cuda")
+        dC = torch.empty(nc, dtype=torch.float16, device="cuda")
+        descs, oa, oc = [], 0, 0
+        for (case, W, S, Z), (M, N, K) in zip(probs, shapes):
+            descs.append((dA[oa:oa + M * K].view(M, K), W, S, Z, dC[oc:oc + M * N].view(M, N), 4, 128))
+            oa += M * K
+            oc += M * N
+        sets.append((dA, dC, lib.gemm_descs(descs)))
+    hostA = [torch.from_numpy(np.concatenate([(c["A"] * (1 + b)).astype(np.float16).ravel() for c, *_ in probs]))
+             .pin_memory() for b in range(2)]
+    hostC = [torch.empty(nc, dtype=torch.float16).pin_memory() for _ in range(2)]
+    for it in range(4):
+        b = it & 1
+        dA, dC, d = sets[b]
+        lib.tl_quant_gemm_batched_host(d, hostA[b], dA, hostC[b], dC, streams[b])
+    torch.cuda.synchronize()
+    for b in range(2):
+        dA, dC, d = sets[b]
+        dA.copy_(hostA[b].cuda())
+        lib.tl_quant_gemm_batched(d)
+        torch.cuda.synchronize()
+        assert torch.equal(hostC[b].view(torch.int16), dC.cpu().view(torch.int16)), b

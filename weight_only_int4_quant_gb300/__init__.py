@@ -22,7 +22,7 @@ __all__ = [
     "tl_requant_int4_to_int2", "tl_requant_int4_to_int2_batched", "requant_int4_to_int2",
     "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward", "quant_gemm_swiglu",
     "interleave_rows", "SwiGLUBlock", "tl_dequant_fp16", "dequant_fp16",
-    "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
+    "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked", "tl_quant_gemm_batched_host",
 ]
 
 # every symbol include/tlq.h declares
@@ -32,6 +32,7 @@ EXPORTED = (
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "tl_requant_int4_to_int2",
     "tl_requant_int4_to_int2_batched", "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward",
     "tl_dequant_fp16", "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
+    "tl_quant_gemm_batched_host",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -115,6 +116,8 @@ def load():
             "tl_quant_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P], I),
             "tl_interleave_rows": ([P, P, P, I, ctypes.c_size_t, P], I),
             "tl_dequant_fp16": ([P, P, P, P, I, I, I, I, P], I),
+            "tl_quant_gemm_batched_host": ([ctypes.POINTER(_GemmDesc), I, P, P, ctypes.c_size_t, P, P,
+                                            ctypes.c_size_t, P], I),
             "tl_loop_block_forward_chunked": ([P, ctypes.POINTER(_Block), I, I, I, P], I),
             "tl_swiglu_block_forward_chunked": ([P, ctypes.POINTER(_SwigluBlock), I, I, I, P], I),
             "tl_swiglu_block_forward": ([P, ctypes.POINTER(_SwigluBlock), I, I, P], I),
@@ -196,6 +199,26 @@ def tl_quant_gemm_batched(descs, stream=None) -> None:
     if not isinstance(descs, ctypes.Array):
         descs = gemm_descs(descs)
     _raise_if(load().tl_quant_gemm_batched(descs, len(descs), _stream(stream)))
+
+
+def tl_quant_gemm_batched_host(descs, hostA, devA, hostC, devC, stream=None) -> None:
+    """The batched call on host buffers: hostA (CPU tensor, pinned) -> devA,
+    the GEMMs, devC -> hostC (CPU tensor, pinned), in order on `stream`.
+    Every descriptor's A / C must be a view into devA / devC."""
+    import torch
+
+    for t, name, cuda in ((hostA, "hostA", False), (hostC, "hostC", False), (devA, "devA", True), (devC, "devC", True)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda != cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous %s tensor" % (name, "CUDA" if cuda else "host"))
+    if hostA.numel() * hostA.element_size() != devA.numel() * devA.element_size() or \
+            hostC.numel() * hostC.element_size() != devC.numel() * devC.element_size():
+        raise ValueError("host and device buffers must have the same sizes")
+    if not isinstance(descs, ctypes.Array):
+        descs = gemm_descs(descs)
+    _raise_if(load().tl_quant_gemm_batched_host(descs, len(descs), hostA.data_ptr(), devA.data_ptr(),
+                                                devA.numel() * devA.element_size(), hostC.data_ptr(),
+                                                devC.data_ptr(), devC.numel() * devC.element_size(),
+                                                _stream(stream)))
 
 
 def tl_pack_weights(codes, W, bits: int, stream=None) -> None:

@@ -167,6 +167,38 @@ tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint1
   return run_gemm(plain_args(A, Wpacked, scales, zeros, C, M, N, K, bits, group), static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+tlq_status check_batched(const tl_gemm_desc* d, int count);
+}  // namespace
+
+tlq_status tl_quant_gemm_batched_host(const tl_gemm_desc* d, int count, const void* hostA, void* devA, size_t a_bytes,
+                                      void* hostC, const void* devC, size_t c_bytes, void* stream_) {
+  g_msg[0] = 0;
+  const char* who = "tl_quant_gemm_batched_host";
+  if (!hostA || !devA || !hostC || !devC) return set_error(TLQ_EINVAL, "%s: null buffer", who);
+  if (!d || count < 1) return set_error(TLQ_EINVAL, "%s: null descriptors or count %d", who, count);
+  if (overlaps(devA, a_bytes, devC, c_bytes)) return set_error(TLQ_EINVAL, "%s: devA and devC overlap", who);
+  // every problem reads inside devA and writes inside devC (rows of lda = K / ldc = N)
+  const char* a0 = static_cast<const char*>(devA);
+  const char* c0 = static_cast<const char*>(devC);
+  for (int i = 0; i < count; ++i) {
+    const char* ap = reinterpret_cast<const char*>(d[i].A);
+    const char* cp = reinterpret_cast<const char*>(d[i].C);
+    const size_t ab = (size_t)d[i].M * d[i].K * 2, cb = (size_t)d[i].M * d[i].N * 2;
+    if (!ap || !cp || ap < a0 || ap + ab > a0 + a_bytes || cp < c0 || cp + cb > c0 + c_bytes)
+      return set_error(TLQ_EINVAL, "%s[%d]: A must lie inside devA and C inside devC", who, i);
+  }
+  tlq_status vst = check_batched(d, count);  // everything is validated before the first copy
+  if (vst != TLQ_OK) return vst;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cudaError_t e = cudaMemcpyAsync(devA, hostA, a_bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_error(e, "tl_quant_gemm_batched_host: copy to the device");
+  tlq_status st = tl_quant_gemm_batched(d, count, stream_);
+  if (st != TLQ_OK) return st;
+  e = cudaMemcpyAsync(hostC, devC, c_bytes, cudaMemcpyDeviceToHost, stream);
+  return cuda_error(e, "tl_quant_gemm_batched_host: copy to the host");
+}
+
 tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales, const uint16_t* zeros,
                                 uint16_t* C, int M, int N2, int K, int bits, int group, void* stream) {
   g_msg[0] = 0;
@@ -211,9 +243,9 @@ tlq_status tl_interleave_rows(const void* a, const void* b, void* out, int rows,
   return cuda_error(e, "tl_interleave_rows: copy");
 }
 
-tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_) {
-  g_msg[0] = 0;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+namespace {
+// Validation of a batched call (shapes, pointers, aliasing); nothing launched.
+tlq_status check_batched(const tl_gemm_desc* d, int count) {
   if (!d || count < 0) return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: null descriptors or count %d", count);
   char who[64];
   for (int i = 0; i < count; ++i) {
@@ -229,6 +261,15 @@ tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_
       if (i < j && overlaps(d[i].C, (size_t)d[i].M * d[i].N * 2, d[j].C, (size_t)d[j].M * d[j].N * 2))
         return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: outputs of problems %d and %d overlap", i, j);
     }
+  return TLQ_OK;
+}
+}  // namespace
+
+tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_) {
+  g_msg[0] = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  tlq_status vst = check_batched(d, count);
+  if (vst != TLQ_OK) return vst;
   // decode-sized problems share launches (one per bit width, up to 16 problems each)
   for (int bits : {4, 2}) {
     GemmArgs batch[kMaxDecodeProblems];
