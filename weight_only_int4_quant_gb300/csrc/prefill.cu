@@ -66,6 +66,7 @@ static_assert((2 * PCfg<2>::SA + 2 * PCfg<2>::SB + 1 + 2 * PCfg<2>::SW) * 8 + 4 
 // split-K slots: ksplit x BM rows x (BN / ksplit + 4) floats, largest at ksplit = 8
 static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::RING, "split-K slots fit in the rings");
 static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<2>::RING, "split-K slots fit in the rings");
+static_assert(2 * BM * BN * 2 <= PCfg<2>::RING && BM * BN * 2 <= PCfg<1>::RING, "staged C tiles fit in the rings");
 
 // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16,
 // both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -206,7 +207,7 @@ __device__ __forceinline__ void store_out(const PrefillParams& p, int m, int n, 
 template <int BITS, int EPI, int NMT>
 __global__ void __launch_bounds__(kThreadsP, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
-                   const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap cmap, const PrefillParams p) {
   constexpr int SA = PCfg<NMT>::SA, SB = PCfg<NMT>::SB, SW = PCfg<NMT>::SW;
   constexpr uint32_t kTmemCols = PCfg<NMT>::TMEM_COLS;
   constexpr int CPW = 32 / BITS;
@@ -488,7 +489,53 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int q = warp & 3;        // TMEM lane quarter this warp may access
     const int half = warp >> 2;    // column half
     const int mrow = 32 * q + lane;
-    if (acc_ok) {
+    if constexpr (EPI == kEpiStore || EPI == kEpiRelu) {
+      if (p.ksplit == 1) {
+        // Converted tiles go to shared memory (the rings are idle: every load
+        // was consumed by a completed MMA) in the 128-byte-swizzled layout of
+        // the C tensor map, 64 columns x 128 rows per box, and leave through
+        // TMA tile stores, which drop rows past M and columns past N.
+        uint8_t* so = smem;  // [NMT][4 column blocks][128 rows][128 bytes]
+        if (acc_ok) {
+#pragma unroll 1
+          for (int ic = 0; ic < 4 * NMT; ++ic) {
+            const int cc = ic & 3;
+            const int mt = ic >> 2;
+            const int col = half * 128 + cc * 32;
+            uint32_t v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * mt + col), v);
+            uint32_t h[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              __half lo = __float2half_rn(__uint_as_float(v[2 * i]));
+              __half hi = __float2half_rn(__uint_as_float(v[2 * i + 1]));
+              if constexpr (EPI == kEpiRelu) {
+                lo = relu_half(lo);
+                hi = relu_half(hi);
+              }
+              h[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+            }
+            const uint32_t row = smem_u32(so + (mt * 4 + (col >> 6)) * (BM * 128)) + (uint32_t)mrow * 128u;
+            const uint32_t c0 = (uint32_t)((col & 63) >> 3);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              sts128(row + (((c0 + j) ^ (uint32_t)(mrow & 7)) << 4), h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_barrier(1, kDqWarps * 32);  // all eight epilogue warps, whatever their wait returned
+        if (threadIdx.x == 0 && acc_ok) {
+          pdl_wait();  // C may be read by the preceding kernel
+          for (int mt = 0; mt < NMT; ++mt)
+            for (int cb = 0; cb < 4; ++cb) {
+              const int x = n0 + cb * 64, y = m0 + mt * BM;
+              if (x < p.N && y < p.M) tma_store_2d(&cmap, so + (mt * 4 + cb) * (BM * 128), x, y);
+            }
+          bulk_commit_group();
+          bulk_wait_all();
+        }
+      }
+    } else if (acc_ok) {
       if (p.ksplit == 1) {
         pdl_wait();
 #pragma unroll 1
@@ -521,25 +568,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     h[i] = (uint32_t)__half_as_ushort(a0) | ((uint32_t)__half_as_ushort(a1) << 16);
                   }
                   *reinterpret_cast<uint4*>(p.C + (size_t)m * p.ldc + nb / 2) = make_uint4(h[0], h[1], h[2], h[3]);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int c8 = 0; c8 < 4; ++c8) {
-                const int nb = n0 + col + c8 * 8;
-                if (nb < p.N) {  // N is a multiple of 8
-                  uint32_t h[4];
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    __half lo = __float2half_rn(__uint_as_float(v[c8 * 8 + 2 * i]));
-                    __half hi = __float2half_rn(__uint_as_float(v[c8 * 8 + 2 * i + 1]));
-                    if constexpr (EPI == kEpiRelu) {
-                      lo = relu_half(lo);
-                      hi = relu_half(hi);
-                    }
-                    h[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-                  }
-                  *reinterpret_cast<uint4*>(p.C + (size_t)m * p.ldc + nb) = make_uint4(h[0], h[1], h[2], h[3]);
                 }
               }
             }
@@ -688,6 +716,15 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (st != TLQ_OK) return st;
 
+  // C as 64-column x 128-row SWIZZLE_128B boxes for the tile-store epilogue
+  // (store / ReLU without a k split); unused otherwise
+  CUtensorMap cmap = amap;
+  if ((EPI == kEpiStore || EPI == kEpiRelu) && p.ksplit == 1) {
+    st = encode_tiled_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.C, (uint64_t)a.N, (uint64_t)a.M,
+                         (uint64_t)a.ldc * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (st != TLQ_OK) return st;
+  }
+
   const size_t smem = (size_t)PCfg<NMT>::SMEM;
   auto kern = prefill_kernel<BITS, EPI, NMT>;
   static std::once_flag once;
@@ -718,7 +755,7 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   }
   lc.attrs = attrs;
   lc.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, wmap, p);
+  cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, wmap, cmap, p);
   if (e != cudaSuccess) return cuda_error(e, "prefill: launch");
   if (log_enabled())
     fprintf(stderr,
