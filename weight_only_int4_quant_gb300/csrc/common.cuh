@@ -133,6 +133,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the sources of every bulk copy of this thread have been read (shared memory reusable)
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Bulk copy from this CTA's shared memory to shared memory of a CTA of the
+// cluster (addresses from mapa), completing transaction bytes on the
+// destination's mbarrier.  16-byte aligned addresses, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                                    uint32_t mbar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
+               : "memory");
+}
 // every bulk store of this thread has completed (its global writes included)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

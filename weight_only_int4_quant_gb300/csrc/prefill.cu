@@ -63,6 +63,13 @@ static_assert(BN == kDqWarps * 32, "one dequant thread per weight row");
 static_assert(PCfg<1>::SMEM <= 232448 && PCfg<2>::SMEM <= 232448, "shared memory");
 static_assert((2 * PCfg<1>::SA + 2 * PCfg<1>::SB + 1 + 2 * PCfg<1>::SW) * 8 + 4 <= 256, "barriers fit");
 static_assert((2 * PCfg<2>::SA + 2 * PCfg<2>::SB + 1 + 2 * PCfg<2>::SW) * 8 + 4 <= 256, "barriers fit");
+static_assert((2 * PCfg<1>::SA + 2 * PCfg<1>::SB + 1 + 2 * PCfg<1>::SW) * 8 + 4 <= 240 &&
+                  (2 * PCfg<2>::SA + 2 * PCfg<2>::SB + 1 + 2 * PCfg<2>::SW) * 8 + 4 <= 240,
+              "the split-K receive barrier sits at byte 240 of the barrier area");
+// split-K staging + slots: 2 (ks - 1) slices of BM x (BN / ks) floats, at most 2 x 7 / 8 x BM x BN x 4 bytes
+static_assert(2 * 7 * (BM * BN * 4 / 8) <= PCfg<1>::RING + PCfg<1>::SW * W_STAGE_MAX &&
+                  2 * 7 * (BM * BN * 4 / 8) <= PCfg<2>::RING + PCfg<2>::SW * W_STAGE_MAX,
+              "split-K staging fits in the idle rings");
 // split-K slots: ksplit x BM rows x (BN / ksplit + 4) floats, largest at ksplit = 8
 static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::RING, "split-K slots fit in the rings");
 static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<2>::RING, "split-K slots fit in the rings");
@@ -230,6 +237,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   uint64_t* wfull = accum + 1;            // [SW] packed tile landed (TMA)
   uint64_t* wempty = wfull + SW;          // [SW] the dequant warps read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + SW);
+  uint64_t* rbar = bars + 30;  // split-K: partial slices of the peers landed (bulk copies)
   float* red = reinterpret_cast<float*>(smem);  // split-K slots, after the main loop
 
   const int warp = threadIdx.x >> 5;
@@ -251,6 +259,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       mbar_init(&empty_b[i], 1);
     }
     mbar_init(accum, 1);
+    mbar_init(rbar, 1);
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], kDqWarps);
@@ -578,69 +587,139 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   }
 
   // ---------------- split-K: reduce partial tiles across the cluster ----------------
-  // Rank o owns columns [o * cpr, (o + 1) * cpr).  Once per token tile: after
-  // a cluster barrier (every rank's stage memory is idle, or the previous
-  // round's slots are summed), each rank pushes its partial columns to their
-  // owners with remote stores, slot = its own rank; after a second barrier
-  // each owner sums its slots in rank order (fixed, deterministic) with local
-  // loads and writes the outputs.
+  // Rank o owns columns [o * cpr, (o + 1) * cpr).  Once per token tile:
+  //  * each owner arms its receive barrier for the ks - 1 peer slices, and a
+  //    cluster barrier makes sure every rank is armed and the previous round
+  //    is summed;
+  //  * every rank writes the columns owned by its peers from TMEM into local
+  //    staging (one dense, XOR-swizzled 128 x cpr slice per peer) and one
+  //    thread sends each slice with a single bulk copy into the owner's slot
+  //    for this rank;
+  //  * each owner waits for its slices and adds, in rank order (fixed, so
+  //    deterministic), its own columns (straight from TMEM) and the peers'.
+  // Measured: per-thread 16-byte remote stores of the partials (one token row
+  // per lane) took as long as the k loop itself at M = 128.
   if (p.ksplit > 1) {
     const int ks = p.ksplit;
     const int cpr = BN / ks;  // 32, 64 or 128: a 32-column TMEM block never straddles two owners
-    const int pitch = cpr + 4;  // floats per row of a slot (16-byte aligned, staggered banks)
-    const uint32_t red_addr = smem_u32(red);
+    const uint32_t slice = (uint32_t)(BM * cpr * 4);
+    uint8_t* stage = smem;                           // [ks - 1][BM][cpr] floats, to the peers
+    uint8_t* slots = smem + (ks - 1) * slice;        // [ks - 1][BM][cpr] floats, from the peers
+    const int q = warp & 3, half = warp >> 2;
+    const int mrow = 32 * q + lane;
+    // byte offset of float c of row r inside a slice (16-byte chunks XOR-swizzled by r & 7)
+    auto soff = [&](int r, int c) -> uint32_t {
+      return (uint32_t)(r * cpr * 4) + ((((uint32_t)(c >> 2)) ^ (uint32_t)(r & 7)) << 4) + (uint32_t)(c & 3) * 4u;
+    };
 #pragma unroll 1
     for (int mt = 0; mt < NMT; ++mt) {
-      __syncwarp();
-      cluster_sync();
-      if (warp < kDqWarps && acc_ok) {
-        const int q = warp & 3, half = warp >> 2;
-        const int mrow = 32 * q + lane;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int col = half * 128 + cc * 32;
-          uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * mt + col), v);
-          const int owner = col / cpr;
-          const uint32_t dst = map_shared_rank(
-              red_addr + (uint32_t)(((rank * BM + mrow) * pitch + (col - owner * cpr)) * 4), (uint32_t)owner);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_shared_cluster_v4(dst + 16u * i, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
+      if (threadIdx.x == 0) {
+        bulk_wait_read_all();  // the previous round's staging has been sent
+        mbar_arrive_expect_tx(rbar, (uint32_t)(ks - 1) * slice);
       }
       __syncwarp();
       cluster_sync();
-      if (mt == 0) pdl_wait();
-      const int quads = cpr / 4;
-      for (int it = threadIdx.x; it < BM * quads; it += kThreadsP) {
-        const int mm = it / quads;
-        const int c4 = 4 * (it - mm * quads);
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < ks; ++j) {
-          const float4 x = *reinterpret_cast<const float4*>(red + ((size_t)(j * BM + mm) * pitch + c4));
-          a[0] += x.x;
-          a[1] += x.y;
-          a[2] += x.z;
-          a[3] += x.w;
-        }
-        const int m = m0 + mt * BM + mm, n = n0 + rank * cpr + c4;
-        if (m < p.M) {
-          if constexpr (EPI == kEpiSwiglu) {
-            if (n < p.N) {  // N is a multiple of 16: the quad is whole
-              const __half a0 = swiglu_half(__float2half_rn(a[0]), __float2half_rn(a[1]));
-              const __half a1 = swiglu_half(__float2half_rn(a[2]), __float2half_rn(a[3]));
-              *reinterpret_cast<uint32_t*>(p.C + (size_t)m * p.ldc + n / 2) =
-                  (uint32_t)__half_as_ushort(a0) | ((uint32_t)__half_as_ushort(a1) << 16);
-            }
-          } else {
+      if (warp < kDqWarps && acc_ok) {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          const int col = half * 128 + cc * 32;
+          const int owner = col / cpr;
+          if (owner == rank) continue;  // added from TMEM by this CTA below
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * mt + col), v);
+          const uint32_t base = smem_u32(stage + (owner < rank ? owner : owner - 1) * slice);
+          const int c0 = col - owner * cpr;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (n + i < p.N) store_out<EPI>(p, m, n + i, a[i]);
+          for (int i = 0; i < 8; ++i)
+            sts128(base + soff(mrow, c0 + 4 * i), v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+      fence_proxy_async_smem();  // staged slices -> the bulk copies (async proxy)
+      __syncthreads();
+      if (threadIdx.x == 0 && acc_ok) {
+        for (int o = 0; o < ks; ++o) {
+          if (o == rank) continue;
+          const int src = o < rank ? o : o - 1;       // my staging slice for owner o
+          const int dst = rank < o ? rank : rank - 1;  // my slot at owner o
+          bulk_copy_s2cluster(map_shared_rank(smem_u32(slots + dst * slice), (uint32_t)o), stage + src * slice,
+                              slice, map_shared_rank(smem_u32(rbar), (uint32_t)o));
+        }
+        bulk_commit_group();
+      }
+      const bool got = mbar_wait(rbar, (uint32_t)(mt & 1), 0x20A);
+      if (mt == 0) pdl_wait();
+      if (warp < kDqWarps && acc_ok && got) {
+        // this thread: row mrow, columns [half * cpr / 2, (half + 1) * cpr / 2) of the owned slice
+        const int ncol = cpr / 2;
+        const int cbeg = half * ncol;
+#pragma unroll 1
+        for (int cb = 0; cb < ncol; cb += 32) {
+          const int w = ncol < 32 ? ncol : 32;   // 16 when cpr = 32
+          const int tcol = rank * cpr + cbeg + cb;
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * mt + (tcol & ~31)), v);
+          const bool upper = (tcol & 31) != 0;  // this thread's 16 columns are the upper half (w = 16)
+          const int m = m0 + mt * BM + mrow;
+#pragma unroll
+          for (int c8 = 0; c8 < 32; c8 += 8) {
+            if (c8 >= w) break;
+            float own[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              own[i] = __uint_as_float(c8 < 16 ? (upper ? v[16 + c8 + i] : v[c8 + i]) : v[c8 + i]);
+            float a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = 0.f;
+            for (int j = 0; j < ks; ++j) {
+              if (j == rank) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[i] += own[i];
+              } else {
+                const uint8_t* sl = slots + (j < rank ? j : j - 1) * slice;
+                const int c = cbeg + cb + c8;
+                const float4 x0 = *reinterpret_cast<const float4*>(sl + soff(mrow, c));
+                const float4 x1 = *reinterpret_cast<const float4*>(sl + soff(mrow, c + 4));
+                a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w;
+                a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
+              }
+            }
+            const int n = n0 + rank * cpr + cbeg + cb + c8;
+            if (m < p.M && n < p.N) {  // N is a multiple of 16 (SwiGLU) or 8: the group of 8 is whole
+              if constexpr (EPI == kEpiSwiglu) {
+                uint32_t hh[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  const __half x0 = swiglu_half(__float2half_rn(a[4 * i]), __float2half_rn(a[4 * i + 1]));
+                  const __half x1 = swiglu_half(__float2half_rn(a[4 * i + 2]), __float2half_rn(a[4 * i + 3]));
+                  hh[i] = (uint32_t)__half_as_ushort(x0) | ((uint32_t)__half_as_ushort(x1) << 16);
+                }
+                *reinterpret_cast<uint2*>(p.C + (size_t)m * p.ldc + n / 2) = make_uint2(hh[0], hh[1]);
+              } else if constexpr (EPI == kEpiResidual) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) store_out<EPI>(p, m, n + i, a[i]);
+              } else {
+                uint32_t hh[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  __half lo = __float2half_rn(a[2 * i]), hi = __float2half_rn(a[2 * i + 1]);
+                  if constexpr (EPI == kEpiRelu) {
+                    lo = relu_half(lo);
+                    hi = relu_half(hi);
+                  }
+                  hh[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+                }
+                *reinterpret_cast<uint4*>(p.C + (size_t)m * p.ldc + n) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+              }
+            }
           }
         }
       }
     }
+    if (threadIdx.x == 0) bulk_wait_read_all();  // no copy still reads this CTA's memory at exit
+    // every peer has received its slices from this CTA before any CTA of the
+    // cluster leaves (its slots must stay valid until then)
+    __syncwarp();
+    cluster_sync();
   }
 
   // ---------------- teardown ----------------
