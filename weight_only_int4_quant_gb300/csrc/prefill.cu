@@ -92,6 +92,7 @@ struct PrefillParams {
   int ksplit;
   int l2_keep;  // stream the weights evict-last (kept in L2)
   int szvec;    // K/group % 8 == 0 and 16-byte aligned scale/zero arrays: 8 groups per 16-byte load
+  int gshift;   // log2(group) when group is a power of two, else -1
 };
 
 // Half i (0..7) of a 16-byte vector, as the low 16 bits.
@@ -379,114 +380,119 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     for (int j = 0; j < kPrefetch; ++j)
       if (!szvec && j < nkb) issue(j, sring[j], zring[j]);
 
+    // One stage: dequantize this thread's row of the packed tile into the B
+    // ring (s_lo.. are raw FP16 bits of the scale / zero of the stage's first
+    // and, for two groups per stage, second group).
+    auto do_stage = [&](int kb, uint32_t s_lo, uint32_t s_hi, uint32_t z_lo, uint32_t z_hi) -> bool {
+      s_lo = bcast16((unsigned short)s_lo);
+      s_hi = bcast16((unsigned short)s_hi);
+      const uint32_t nzs_lo = hmul2u(bcast16((unsigned short)z_lo), s_lo) ^ 0x80008000u;  // -(z * s)
+      const uint32_t nzs_hi = hmul2u(bcast16((unsigned short)z_hi), s_hi) ^ 0x80008000u;
+      // this stage's packed words: row r of the TMA tile (INT4: two 16-byte
+      // chunks, swapped in rows with bit 2 set by SWIZZLE_32B; INT2: one)
+      const int ws = kb % SW;
+      if (!mbar_wait(&wfull[ws], (kb / SW) & 1, 0x207)) {
+        return false;
+      }
+      uint4 cur[NV];
+      {
+        const uint32_t wr = smem_u32(sw + ws * W_STAGE) + (uint32_t)r * (BK * BITS / 8);
+        if constexpr (BITS == 4) {
+          const uint32_t sw32 = (uint32_t)((r >> 2) & 1) << 4;
+          cur[0] = lds128(wr + sw32);
+          cur[1] = lds128(wr + (sw32 ^ 16u));
+        } else {
+          cur[0] = lds128(wr);
+        }
+      }
+      const int slot = kb % SB;
+      if (!mbar_wait(&empty_b[slot], ((kb / SB) & 1) ^ 1, 0x205)) {
+        return false;
+      }
+      const uint32_t brow = smem_u32(sb + slot * B_STAGE) + (uint32_t)r * 128u;
+      const int ks = k0 + kb * BK;
+      uint32_t wv[WPS];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        wv[4 * v + 0] = cur[v].x;
+        wv[4 * v + 1] = cur[v].y;
+        wv[4 * v + 2] = cur[v].z;
+        wv[4 * v + 3] = cur[v].w;
+      }
+      if (row_ok && ks + BK <= p.K) {  // full stage: no per-word checks
+#pragma unroll
+        for (int wj = 0; wj < WPS; ++wj) {
+          const bool hi = two_groups && (wj >= WPS / 2);
+          uint32_t o[OUTW];
+          dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
+          if constexpr (BITS == 4) {
+            sts128(brow + (((uint32_t)wj ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
+          } else {
+            sts128(brow + (((uint32_t)(2 * wj) ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
+            sts128(brow + (((uint32_t)(2 * wj + 1) ^ (uint32_t)(r & 7)) << 4), o[4], o[5], o[6], o[7]);
+          }
+        }
+      } else {
+#pragma unroll
+      for (int wj = 0; wj < WPS; ++wj) {
+        const bool hi = two_groups && (wj >= WPS / 2);
+        uint32_t o[OUTW];
+        dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
+        const bool valid = row_ok && (ks + wj * CPW < p.K);
+        if constexpr (BITS == 4) {
+          const uint32_t c = (uint32_t)wj;
+          const uint32_t addr = brow + ((c ^ (uint32_t)(r & 7)) << 4);
+          if (valid) sts128(addr, o[0], o[1], o[2], o[3]);
+          else sts128(addr, 0, 0, 0, 0);
+        } else {
+          const uint32_t c0 = (uint32_t)(2 * wj), c1 = c0 + 1;
+          const uint32_t a0 = brow + ((c0 ^ (uint32_t)(r & 7)) << 4);
+          const uint32_t a1 = brow + ((c1 ^ (uint32_t)(r & 7)) << 4);
+          if (valid) {
+            sts128(a0, o[0], o[1], o[2], o[3]);
+            sts128(a1, o[4], o[5], o[6], o[7]);
+          } else {
+            sts128(a0, 0, 0, 0, 0);
+            sts128(a1, 0, 0, 0, 0);
+          }
+        }
+      }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&full_b[slot]);
+        mbar_arrive(&wempty[ws]);  // its words are consumed
+      }
+      return true;
+    };
+
     bool ok = true;
-    for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
+    if (szvec) {
+      // plain stage loop (no unrolled copies: the kernel's code stays small)
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int kpos = k0 + kb * BK;
+        const int g0 = p.gshift >= 0 ? (kpos >> p.gshift) : kpos / p.group;
+        if ((g0 >> 3) > win) {  // a stage spans at most two groups: the window moves by one
+          sv = svn;
+          zv = zvn;
+          ++win;
+          load_win(win + 1, svn, zvn);
+        }
+        // with two groups per stage g0 is even, so g0 + 1 stays in the window
+        const uint32_t s_lo = pick16(sv, g0 & 7), z_lo = pick16(zv, g0 & 7);
+        ok = do_stage(kb, s_lo, two_groups ? pick16(sv, (g0 + 1) & 7) : s_lo, z_lo,
+                      two_groups ? pick16(zv, (g0 + 1) & 7) : z_lo);
+      }
+    } else {
+      for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
 #pragma unroll
-      for (int j = 0; j < kPrefetch; ++j) {
-        const int kb = kb0 + j;
-        if (kb < nkb && ok) {
-          uint32_t s_lo, s_hi, z_lo, z_hi;
-          if (szvec) {
-            const int g0 = (k0 + kb * BK) / p.group;
-            if ((g0 >> 3) > win) {  // a stage spans at most two groups: the window moves by one
-              sv = svn;
-              zv = zvn;
-              ++win;
-              load_win(win + 1, svn, zvn);
-            }
-            // with two groups per stage g0 is even, so g0 + 1 stays in the window
-            s_lo = pick16(sv, g0 & 7);
-            z_lo = pick16(zv, g0 & 7);
-            s_hi = two_groups ? pick16(sv, (g0 + 1) & 7) : s_lo;
-            z_hi = two_groups ? pick16(zv, (g0 + 1) & 7) : z_lo;
-          } else {
-            s_lo = sring[j][0];
-            s_hi = sring[j][1];
-            z_lo = zring[j][0];
-            z_hi = zring[j][1];
+        for (int j = 0; j < kPrefetch; ++j) {
+          const int kb = kb0 + j;
+          if (kb < nkb && ok) {
+            const uint32_t s_lo = sring[j][0], s_hi = sring[j][1], z_lo = zring[j][0], z_hi = zring[j][1];
             if (kb + kPrefetch < nkb) issue(kb + kPrefetch, sring[j], zring[j]);
-          }
-          s_lo = bcast16((unsigned short)s_lo);
-          s_hi = bcast16((unsigned short)s_hi);
-          const uint32_t nzs_lo = hmul2u(bcast16((unsigned short)z_lo), s_lo) ^ 0x80008000u;  // -(z * s)
-          const uint32_t nzs_hi = hmul2u(bcast16((unsigned short)z_hi), s_hi) ^ 0x80008000u;
-          // this stage's packed words: row r of the TMA tile (INT4: two 16-byte
-          // chunks, swapped in rows with bit 2 set by SWIZZLE_32B; INT2: one)
-          const int ws = kb % SW;
-          if (!mbar_wait(&wfull[ws], (kb / SW) & 1, 0x207)) {
-            ok = false;
-            break;
-          }
-          uint4 cur[NV];
-          {
-            const uint32_t wr = smem_u32(sw + ws * W_STAGE) + (uint32_t)r * (BK * BITS / 8);
-            if constexpr (BITS == 4) {
-              const uint32_t sw32 = (uint32_t)((r >> 2) & 1) << 4;
-              cur[0] = lds128(wr + sw32);
-              cur[1] = lds128(wr + (sw32 ^ 16u));
-            } else {
-              cur[0] = lds128(wr);
-            }
-          }
-          const int slot = kb % SB;
-          if (!mbar_wait(&empty_b[slot], ((kb / SB) & 1) ^ 1, 0x205)) {
-            ok = false;
-            break;
-          }
-          const uint32_t brow = smem_u32(sb + slot * B_STAGE) + (uint32_t)r * 128u;
-          const int ks = k0 + kb * BK;
-          uint32_t wv[WPS];
-#pragma unroll
-          for (int v = 0; v < NV; ++v) {
-            wv[4 * v + 0] = cur[v].x;
-            wv[4 * v + 1] = cur[v].y;
-            wv[4 * v + 2] = cur[v].z;
-            wv[4 * v + 3] = cur[v].w;
-          }
-          if (row_ok && ks + BK <= p.K) {  // full stage: no per-word checks
-#pragma unroll
-            for (int wj = 0; wj < WPS; ++wj) {
-              const bool hi = two_groups && (wj >= WPS / 2);
-              uint32_t o[OUTW];
-              dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
-              if constexpr (BITS == 4) {
-                sts128(brow + (((uint32_t)wj ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
-              } else {
-                sts128(brow + (((uint32_t)(2 * wj) ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
-                sts128(brow + (((uint32_t)(2 * wj + 1) ^ (uint32_t)(r & 7)) << 4), o[4], o[5], o[6], o[7]);
-              }
-            }
-          } else {
-#pragma unroll
-          for (int wj = 0; wj < WPS; ++wj) {
-            const bool hi = two_groups && (wj >= WPS / 2);
-            uint32_t o[OUTW];
-            dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
-            const bool valid = row_ok && (ks + wj * CPW < p.K);
-            if constexpr (BITS == 4) {
-              const uint32_t c = (uint32_t)wj;
-              const uint32_t addr = brow + ((c ^ (uint32_t)(r & 7)) << 4);
-              if (valid) sts128(addr, o[0], o[1], o[2], o[3]);
-              else sts128(addr, 0, 0, 0, 0);
-            } else {
-              const uint32_t c0 = (uint32_t)(2 * wj), c1 = c0 + 1;
-              const uint32_t a0 = brow + ((c0 ^ (uint32_t)(r & 7)) << 4);
-              const uint32_t a1 = brow + ((c1 ^ (uint32_t)(r & 7)) << 4);
-              if (valid) {
-                sts128(a0, o[0], o[1], o[2], o[3]);
-                sts128(a1, o[4], o[5], o[6], o[7]);
-              } else {
-                sts128(a0, 0, 0, 0, 0);
-                sts128(a1, 0, 0, 0, 0);
-              }
-            }
-          }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&full_b[slot]);
-            mbar_arrive(&wempty[ws]);  // its words are consumed
+            ok = do_stage(kb, s_lo, s_hi, z_lo, z_hi);
           }
         }
       }
@@ -778,6 +784,9 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   p.l2_keep = a.l2_keep;
   p.szvec = ((a.K / a.group) % 8 == 0 && (reinterpret_cast<uintptr_t>(a.S) & 15) == 0 &&
              (reinterpret_cast<uintptr_t>(a.Z) & 15) == 0) ? 1 : 0;
+  p.gshift = -1;
+  for (int sh = 5; sh < 31; ++sh)
+    if ((1 << sh) == a.group) p.gshift = sh;
   p.kslice = per2 * BK;
   p.ksplit = (a.K + p.kslice - 1) / p.kslice;
   if (p.ksplit != ksplit) return set_error(TLQ_EINVAL, "prefill: inconsistent k split");
