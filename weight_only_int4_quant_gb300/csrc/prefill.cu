@@ -35,10 +35,7 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int kDqWarps = 8;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreadsP = 10 * 32;
+constexpr int kEpiWarps = 8;  // warps that own the TMEM accumulators in the epilogue (one row per thread)
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int kPrefetch = 3;          // scale/zero global-load distance (stages)
@@ -57,9 +54,16 @@ struct PCfg {
   static constexpr int RING = SA * NMT * A_STAGE + SB * B_STAGE;  // A and B rings (also the split-K slots)
   static constexpr int SMEM = 1024 + RING + SW * W_STAGE_MAX + 256;
   static constexpr uint32_t TMEM_COLS = 256u * NMT;
+  // Dequantizing warps: with one token tile the MMAs of a stage are short and
+  // the dequantization is the critical path, so two warps share each weight
+  // row (half of the stage's words each): 16 warps, four per scheduler, hide
+  // its latency.  With two token tiles the MMAs are the longer part: 8 warps.
+  static constexpr int DQW = NMT == 1 ? 16 : 8;
+  static constexpr int TMA_WARP = DQW, MMA_WARP = DQW + 1;
+  static constexpr int THREADS = (DQW + 2) * 32;
 };
 
-static_assert(BN == kDqWarps * 32, "one dequant thread per weight row");
+static_assert(BN == kEpiWarps * 32, "one epilogue thread per weight row");
 static_assert(PCfg<1>::SMEM <= 232448 && PCfg<2>::SMEM <= 232448, "shared memory");
 static_assert((2 * PCfg<1>::SA + 2 * PCfg<1>::SB + 1 + 2 * PCfg<1>::SW) * 8 + 4 <= 256, "barriers fit");
 static_assert((2 * PCfg<2>::SA + 2 * PCfg<2>::SB + 1 + 2 * PCfg<2>::SW) * 8 + 4 <= 256, "barriers fit");
@@ -213,14 +217,13 @@ __device__ __forceinline__ void store_out(const PrefillParams& p, int m, int n, 
 }
 
 template <int BITS, int EPI, int NMT>
-__global__ void __launch_bounds__(kThreadsP, 1)
+__global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
                    const __grid_constant__ CUtensorMap cmap, const PrefillParams p) {
   constexpr int SA = PCfg<NMT>::SA, SB = PCfg<NMT>::SB, SW = PCfg<NMT>::SW;
   constexpr uint32_t kTmemCols = PCfg<NMT>::TMEM_COLS;
   constexpr int CPW = 32 / BITS;
   constexpr int WPS = BK / CPW;                 // packed words per row per stage (8 or 4)
-  constexpr int NV = WPS / 4;                   // uint4 loads per row per stage (2 or 1)
   constexpr int OUTW = BITS == 4 ? 4 : 8;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -239,7 +242,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   uint64_t* wempty = wfull + SW;          // [SW] the dequant warps read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + SW);
   uint64_t* rbar = bars + 30;  // split-K: partial slices of the peers landed (bulk copies)
-  float* red = reinterpret_cast<float*>(smem);  // split-K slots, after the main loop
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -256,14 +258,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       mbar_init(&empty_a[i], 1);
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(&full_b[i], kDqWarps);
+      mbar_init(&full_b[i], PCfg<NMT>::DQW);
       mbar_init(&empty_b[i], 1);
     }
     mbar_init(accum, 1);
     mbar_init(rbar, 1);
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
-      mbar_init(&wempty[i], kDqWarps);
+      mbar_init(&wempty[i], PCfg<NMT>::DQW);
     }
     fence_mbar_init();
   }
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   if (threadIdx.x == 0) pdl_launch_dependents();
   bool acc_ok = true;  // dequant warps: the accumulator is complete
 
-  if (warp == kTmaWarp) {
+  if (warp == PCfg<NMT>::TMA_WARP) {
     // ---------------- activations: TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&amap);
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (!mbar_wait(&wfull[kb % SW], (kb / SW) & 1, 0x209)) break;
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == PCfg<NMT>::MMA_WARP) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = true;
@@ -332,7 +334,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     __syncwarp();
   } else {
     // ---------------- dequantize weights into the B stages ----------------
-    const int r = threadIdx.x;  // weight row inside the tile, 0..255
+    constexpr int NPART = PCfg<NMT>::DQW / 8;    // threads per weight row
+    constexpr int WPP = WPS / NPART;             // packed words per thread per stage
+    const int r = (warp & 7) * 32 + lane;        // weight row inside the tile, 0..255
+    const int part = warp >> 3;                  // which WPP words of the row's stage
+    const int w0 = part * WPP;
     const int n = n0 + r;
     const bool row_ok = n < p.N;
     const int G = p.K / p.group;
@@ -394,15 +400,27 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       if (!mbar_wait(&wfull[ws], (kb / SW) & 1, 0x207)) {
         return false;
       }
-      uint4 cur[NV];
+      uint32_t wv[WPP];  // this thread's words: w0 .. w0 + WPP - 1 of the row
       {
         const uint32_t wr = smem_u32(sw + ws * W_STAGE) + (uint32_t)r * (BK * BITS / 8);
         if constexpr (BITS == 4) {
-          const uint32_t sw32 = (uint32_t)((r >> 2) & 1) << 4;
-          cur[0] = lds128(wr + sw32);
-          cur[1] = lds128(wr + (sw32 ^ 16u));
+          const uint32_t sw32 = (uint32_t)((r >> 2) & 1) << 4;  // chunk of words 0..3
+          if constexpr (NPART == 1) {
+            const uint4 c0 = lds128(wr + sw32), c1 = lds128(wr + (sw32 ^ 16u));
+            wv[0] = c0.x; wv[1] = c0.y; wv[2] = c0.z; wv[3] = c0.w;
+            wv[4] = c1.x; wv[5] = c1.y; wv[6] = c1.z; wv[7] = c1.w;
+          } else {
+            const uint4 c = lds128(wr + (part ? (sw32 ^ 16u) : sw32));
+            wv[0] = c.x; wv[1] = c.y; wv[2] = c.z; wv[3] = c.w;
+          }
         } else {
-          cur[0] = lds128(wr);
+          const uint4 c = lds128(wr);
+          if constexpr (NPART == 1) {
+            wv[0] = c.x; wv[1] = c.y; wv[2] = c.z; wv[3] = c.w;
+          } else {
+            wv[0] = part ? c.z : c.x;
+            wv[1] = part ? c.w : c.y;
+          }
         }
       }
       const int slot = kb % SB;
@@ -411,20 +429,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       const uint32_t brow = smem_u32(sb + slot * B_STAGE) + (uint32_t)r * 128u;
       const int ks = k0 + kb * BK;
-      uint32_t wv[WPS];
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        wv[4 * v + 0] = cur[v].x;
-        wv[4 * v + 1] = cur[v].y;
-        wv[4 * v + 2] = cur[v].z;
-        wv[4 * v + 3] = cur[v].w;
-      }
       if (row_ok && ks + BK <= p.K) {  // full stage: no per-word checks
 #pragma unroll
-        for (int wj = 0; wj < WPS; ++wj) {
+        for (int lj = 0; lj < WPP; ++lj) {
+          const int wj = w0 + lj;
           const bool hi = two_groups && (wj >= WPS / 2);
           uint32_t o[OUTW];
-          dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
+          dequant_word<BITS>(wv[lj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
           if constexpr (BITS == 4) {
             sts128(brow + (((uint32_t)wj ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
           } else {
@@ -434,10 +445,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
       } else {
 #pragma unroll
-      for (int wj = 0; wj < WPS; ++wj) {
+      for (int lj = 0; lj < WPP; ++lj) {
+        const int wj = w0 + lj;
         const bool hi = two_groups && (wj >= WPS / 2);
         uint32_t o[OUTW];
-        dequant_word<BITS>(wv[wj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
+        dequant_word<BITS>(wv[lj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
         const bool valid = row_ok && (ks + wj * CPW < p.K);
         if constexpr (BITS == 4) {
           const uint32_t c = (uint32_t)wj;
@@ -501,6 +513,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // ---------------- epilogue: TMEM -> registers -> global ----------------
     acc_ok = mbar_wait(accum, 0, 0x206);
     tc_fence_after();
+    if (warp < kEpiWarps) {  // the epilogue: one accumulator row per thread of warps 0..7
     const int q = warp & 3;        // TMEM lane quarter this warp may access
     const int half = warp >> 2;    // column half
     const int mrow = 32 * q + lane;
@@ -538,7 +551,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           }
         }
         fence_proxy_async_smem();
-        named_barrier(1, kDqWarps * 32);  // all eight epilogue warps, whatever their wait returned
+        named_barrier(1, kEpiWarps * 32);  // all eight epilogue warps, whatever their wait returned
         if (threadIdx.x == 0 && acc_ok) {
           pdl_wait();  // C may be read by the preceding kernel
           for (int mt = 0; mt < NMT; ++mt)
@@ -590,6 +603,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
       }
     }
+    }  // epilogue warps
   }
 
   // ---------------- split-K: reduce partial tiles across the cluster ----------------
@@ -625,7 +639,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       __syncwarp();
       cluster_sync();
-      if (warp < kDqWarps && acc_ok) {
+      if (warp < kEpiWarps && acc_ok) {
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           const int col = half * 128 + cc * 32;
@@ -654,7 +668,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
       const bool got = mbar_wait(rbar, (uint32_t)(mt & 1), 0x20A);
       if (mt == 0) pdl_wait();
-      if (warp < kDqWarps && acc_ok && got) {
+      if (warp < kEpiWarps && acc_ok && got) {
         // this thread: row mrow, columns [half * cpr / 2, (half + 1) * cpr / 2) of the owned slice
         const int ncol = cpr / 2;
         const int cbeg = half * ncol;
@@ -824,7 +838,7 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
 
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)ntile, (unsigned)mtile, (unsigned)p.ksplit);
-  lc.blockDim = dim3(kThreadsP, 1, 1);
+  lc.blockDim = dim3(PCfg<NMT>::THREADS, 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
   cudaLaunchAttribute attrs[2];
