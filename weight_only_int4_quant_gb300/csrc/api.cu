@@ -410,6 +410,7 @@ struct BlockSpec {
   uint16_t *h, *qkv_out, *o_out, *act_out;
   int normalize;
   const char* who;
+  bool no_alloc = false;  // no device allocation in any launch (GEMMs run without a k split)
 };
 
 tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_t stream) {
@@ -462,6 +463,7 @@ tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_
     a.group = b.group;
     a.M = M;
     a.l2_keep = keep ? 1 : 0;
+    a.no_alloc = b.no_alloc ? 1 : 0;
     a.A = reinterpret_cast<const __half*>(A);
     a.lda = lda;
     a.W = p->W;
@@ -496,6 +498,7 @@ tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void
                        b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, "tl_loop_block_forward"};
   return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
 }
+
 
 namespace {
 // Chunk-first prefill: rows [r0, r0 + chunk) run through all L iterations,
@@ -567,3 +570,15 @@ tlq_status tl_selftest_wait_timeout(unsigned limit_us, void* stream) {
 }
 
 }  // extern "C"
+namespace tlq {
+// The ReLU loop block with no device allocation in any launch (the entry
+// point for callers that cannot allocate; its scratch comes from the caller).
+tlq_status loop_block_forward_no_alloc(float* x, const tl_block* b, int L, int M, const char* who, void* stream) {
+  if (!x || !b) return set_error(TLQ_EINVAL, "%s: null x or block", who);
+  BlockSpec s = {{&b->qkv, &b->o, &b->up, &b->down}, b->bits, b->group, b->D, b->up.N, false,
+                 b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, who};
+  s.no_alloc = true;
+  return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
+}
+}  // namespace tlq
+

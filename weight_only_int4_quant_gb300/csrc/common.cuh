@@ -133,18 +133,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// the sources of every bulk copy of this thread have been read (shared memory reusable)
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Bulk copy from this CTA's shared memory to shared memory of a CTA of the
-// cluster (addresses from mapa), completing transaction bytes on the
-// destination's mbarrier.  16-byte aligned addresses, size a multiple of 16.
-__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
-                                                    uint32_t mbar_cluster) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst_cluster),
-               "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
-               : "memory");
-}
 // every bulk store of this thread has completed (its global writes included)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -338,7 +326,8 @@ struct GemmArgs {
   int ldx;
   int M, N, K, bits, group;
   int epi;
-  int l2_keep = 0;  // 1: stream the weights with an L2 evict-last policy (reused soon, e.g. the loop block)
+  int l2_keep = 0;   // 1: stream the weights with an L2 evict-last policy (reused soon, e.g. the loop block)
+  int no_alloc = 0;  // 1: the launch may not allocate device memory (the prefill kernel then splits no k)
 };
 
 // Error reporting (thread-local message)
@@ -368,6 +357,7 @@ bool pdl_enabled();
 constexpr int kMaxDecodeProblems = 16;
 tlq_status launch_decode(const GemmArgs* a, int count, cudaStream_t stream);
 tlq_status launch_prefill(const GemmArgs& a, cudaStream_t stream);
+tlq_status loop_block_forward_no_alloc(float* x, const tl_block* b, int L, int M, const char* who, void* stream);
 tlq_status launch_pack(const uint8_t* codes, uint32_t* W, int N, int K, int bits, cudaStream_t stream);
 tlq_status launch_unpack(const uint32_t* W, uint8_t* codes, int N, int K, int bits, cudaStream_t stream);
 // INT4 -> INT2 re-quantization of up to kMaxRequantProblems weights sharing

@@ -10,17 +10,20 @@
 // Tile: NMT x 128 tokens (UMMA M, NMT = 1 or 2) x 256 weight rows (UMMA N) x
 // 64 k per stage, FP32 accumulators in TMEM (256 columns per 128 tokens).
 // With NMT = 2 one dequantized weight tile feeds two token tiles, halving the
-// dequantization work per MMA.  Warp roles (320 threads):
-//   warps 0-7  dequantize: each thread owns one weight row of the tile, reads
-//              its packed words straight from global memory (three stages
-//              ahead), rebuilds exact FP16 weights (q - z) * s and stores them
-//              in the UMMA K-major SWIZZLE_128B layout; after the main loop the
-//              same warps drain the accumulator (tcgen05.ld) in the epilogue.
-//   warp 8     TMA producer of the activation tiles (SWIZZLE_128B).
-//   warp 9     one elected thread issues tcgen05.mma (kind::f16, 4 x K=16 per
-//              stage) and commits stage release / accumulator-ready barriers.
+// dequantization work per MMA.  Warp roles (DQW = 16 dequantizing warps with
+// one token tile, 8 with two):
+//   warps 0 .. DQW-1  dequantize: the packed words of a stage (TMA ring) become
+//              exact FP16 weights (q - z) * s in the UMMA K-major SWIZZLE_128B
+//              layout of the B ring (two threads per weight row with one
+//              token tile, one with two); after the main loop warps 0-7 drain
+//              the accumulator (tcgen05.ld) in the epilogue.
+//   warp DQW   TMA producer: lane 0 the activation tiles (SWIZZLE_128B),
+//              lane 16 the packed weight tiles.
+//   warp DQW+1 one elected thread issues tcgen05.mma (kind::f16, 4 x K=16 per
+//              stage and token tile) and commits the stage release and
+//              accumulator-ready barriers.
 // Short-M problems split K over the CTAs of a thread-block cluster; partial
-// tiles are reduced in a fixed rank order through distributed shared memory
+// tiles are reduced in a fixed rank order through an FP32 workspace in L2
 // (deterministic, no atomics).  Every mbarrier wait is bounded.
 #include <cstdio>
 #include <cstdlib>
@@ -67,16 +70,6 @@ static_assert(BN == kEpiWarps * 32, "one epilogue thread per weight row");
 static_assert(PCfg<1>::SMEM <= 232448 && PCfg<2>::SMEM <= 232448, "shared memory");
 static_assert((2 * PCfg<1>::SA + 2 * PCfg<1>::SB + 1 + 2 * PCfg<1>::SW) * 8 + 4 <= 256, "barriers fit");
 static_assert((2 * PCfg<2>::SA + 2 * PCfg<2>::SB + 1 + 2 * PCfg<2>::SW) * 8 + 4 <= 256, "barriers fit");
-static_assert((2 * PCfg<1>::SA + 2 * PCfg<1>::SB + 1 + 2 * PCfg<1>::SW) * 8 + 4 <= 240 &&
-                  (2 * PCfg<2>::SA + 2 * PCfg<2>::SB + 1 + 2 * PCfg<2>::SW) * 8 + 4 <= 240,
-              "the split-K receive barrier sits at byte 240 of the barrier area");
-// split-K staging + slots: 2 (ks - 1) slices of BM x (BN / ks) floats, at most 2 x 7 / 8 x BM x BN x 4 bytes
-static_assert(2 * 7 * (BM * BN * 4 / 8) <= PCfg<1>::RING + PCfg<1>::SW * W_STAGE_MAX &&
-                  2 * 7 * (BM * BN * 4 / 8) <= PCfg<2>::RING + PCfg<2>::SW * W_STAGE_MAX,
-              "split-K staging fits in the idle rings");
-// split-K slots: ksplit x BM rows x (BN / ksplit + 4) floats, largest at ksplit = 8
-static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<1>::RING, "split-K slots fit in the rings");
-static_assert(BM * (BN + 4 * 8) * 4 <= PCfg<2>::RING, "split-K slots fit in the rings");
 static_assert(2 * BM * BN * 2 <= PCfg<2>::RING && BM * BN * 2 <= PCfg<1>::RING, "staged C tiles fit in the rings");
 
 // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16,
@@ -97,6 +90,7 @@ struct PrefillParams {
   int l2_keep;  // stream the weights evict-last (kept in L2)
   int szvec;    // K/group % 8 == 0 and 16-byte aligned scale/zero arrays: 8 groups per 16-byte load
   int gshift;   // log2(group) when group is a power of two, else -1
+  float* ws;    // k split: FP32 partial slices, NMT * ksplit^2 slices of BM x BN/ksplit per cluster
 };
 
 // Half i (0..7) of a 16-byte vector, as the low 16 bits.
@@ -241,7 +235,6 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
   uint64_t* wfull = accum + 1;            // [SW] packed tile landed (TMA)
   uint64_t* wempty = wfull + SW;          // [SW] the dequant warps read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + SW);
-  uint64_t* rbar = bars + 30;  // split-K: partial slices of the peers landed (bulk copies)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -262,7 +255,6 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
       mbar_init(&empty_b[i], 1);
     }
     mbar_init(accum, 1);
-    mbar_init(rbar, 1);
     for (int i = 0; i < SW; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], PCfg<NMT>::DQW);
@@ -606,40 +598,29 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
     }  // epilogue warps
   }
 
-  // ---------------- split-K: reduce partial tiles across the cluster ----------------
-  // Rank o owns columns [o * cpr, (o + 1) * cpr).  Once per token tile:
-  //  * each owner arms its receive barrier for the ks - 1 peer slices, and a
-  //    cluster barrier makes sure every rank is armed and the previous round
-  //    is summed;
-  //  * every rank writes the columns owned by its peers from TMEM into local
-  //    staging (one dense, XOR-swizzled 128 x cpr slice per peer) and one
-  //    thread sends each slice with a single bulk copy into the owner's slot
-  //    for this rank;
-  //  * each owner waits for its slices and adds, in rank order (fixed, so
-  //    deterministic), its own columns (straight from TMEM) and the peers'.
-  // Measured: per-thread 16-byte remote stores of the partials (one token row
-  // per lane) took as long as the k loop itself at M = 128.
+  // ---------------- split-K: reduce partial tiles through L2 ----------------
+  // Rank o owns columns [o * cpr, (o + 1) * cpr).  Every rank writes the
+  // columns its peers own from TMEM into the launch's FP32 workspace: one
+  // 128 x cpr slice per (token tile, owner, writer), stored as [cpr / 4][128
+  // rows][4] so that a warp's 32 rows are one contiguous 512-byte store.  A
+  // cluster barrier (release / acquire at cluster scope) publishes them, and
+  // each owner adds, in rank order (fixed, so deterministic), its own columns
+  // straight from TMEM and the peers' slices read from L2.
+  // Measured: the same exchange pushed through distributed shared memory
+  // (one bulk copy per peer between the ranks' shared memories) took 8-9 us
+  // per launch, mostly waiting for the copies to land; per-thread remote
+  // stores were slower still.
   if (p.ksplit > 1) {
     const int ks = p.ksplit;
     const int cpr = BN / ks;  // 32, 64 or 128: a 32-column TMEM block never straddles two owners
-    const uint32_t slice = (uint32_t)(BM * cpr * 4);
-    uint8_t* stage = smem;                           // [ks - 1][BM][cpr] floats, to the peers
-    uint8_t* slots = smem + (ks - 1) * slice;        // [ks - 1][BM][cpr] floats, from the peers
+    const size_t slice = (size_t)BM * cpr;  // floats
+    float* wsc = p.ws + (size_t)(blockIdx.x + gridDim.x * blockIdx.y) * NMT * ks * ks * slice;
     const int q = warp & 3, half = warp >> 2;
     const int mrow = 32 * q + lane;
-    // byte offset of float c of row r inside a slice (16-byte chunks XOR-swizzled by r & 7)
-    auto soff = [&](int r, int c) -> uint32_t {
-      return (uint32_t)(r * cpr * 4) + ((((uint32_t)(c >> 2)) ^ (uint32_t)(r & 7)) << 4) + (uint32_t)(c & 3) * 4u;
-    };
+    pdl_wait();  // the workspace and C may still be in use by the preceding kernel
+    if (warp < kEpiWarps && acc_ok) {
 #pragma unroll 1
-    for (int mt = 0; mt < NMT; ++mt) {
-      if (threadIdx.x == 0) {
-        bulk_wait_read_all();  // the previous round's staging has been sent
-        mbar_arrive_expect_tx(rbar, (uint32_t)(ks - 1) * slice);
-      }
-      __syncwarp();
-      cluster_sync();
-      if (warp < kEpiWarps && acc_ok) {
+      for (int mt = 0; mt < NMT; ++mt) {
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           const int col = half * 128 + cc * 32;
@@ -647,28 +628,20 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
           if (owner == rank) continue;  // added from TMEM by this CTA below
           uint32_t v[32];
           tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * mt + col), v);
-          const uint32_t base = smem_u32(stage + (owner < rank ? owner : owner - 1) * slice);
-          const int c0 = col - owner * cpr;
+          float4* sl = reinterpret_cast<float4*>(wsc + ((size_t)(mt * ks + owner) * ks + rank) * slice);
+          const int c40 = (col - owner * cpr) >> 2;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            sts128(base + soff(mrow, c0 + 4 * i), v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            __stcg(sl + (size_t)(c40 + i) * BM + mrow,
+                   make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                               __uint_as_float(v[4 * i + 3])));
         }
       }
-      fence_proxy_async_smem();  // staged slices -> the bulk copies (async proxy)
-      __syncthreads();
-      if (threadIdx.x == 0 && acc_ok) {
-        for (int o = 0; o < ks; ++o) {
-          if (o == rank) continue;
-          const int src = o < rank ? o : o - 1;       // my staging slice for owner o
-          const int dst = rank < o ? rank : rank - 1;  // my slot at owner o
-          bulk_copy_s2cluster(map_shared_rank(smem_u32(slots + dst * slice), (uint32_t)o), stage + src * slice,
-                              slice, map_shared_rank(smem_u32(rbar), (uint32_t)o));
-        }
-        bulk_commit_group();
-      }
-      const bool got = mbar_wait(rbar, (uint32_t)(mt & 1), 0x20A);
-      if (mt == 0) pdl_wait();
-      if (warp < kEpiWarps && acc_ok && got) {
+    }
+    cluster_sync();  // every rank's slices are in the workspace
+    if (warp < kEpiWarps && acc_ok) {
+#pragma unroll 1
+      for (int mt = 0; mt < NMT; ++mt) {
         // this thread: row mrow, columns [half * cpr / 2, (half + 1) * cpr / 2) of the owned slice
         const int ncol = cpr / 2;
         const int cbeg = half * ncol;
@@ -690,15 +663,15 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
             float a[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) a[i] = 0.f;
+            const int c4 = (cbeg + cb + c8) >> 2;  // column quad inside the owned slice
             for (int j = 0; j < ks; ++j) {
               if (j == rank) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) a[i] += own[i];
               } else {
-                const uint8_t* sl = slots + (j < rank ? j : j - 1) * slice;
-                const int c = cbeg + cb + c8;
-                const float4 x0 = *reinterpret_cast<const float4*>(sl + soff(mrow, c));
-                const float4 x1 = *reinterpret_cast<const float4*>(sl + soff(mrow, c + 4));
+                const float4* sl = reinterpret_cast<const float4*>(wsc + ((size_t)(mt * ks + rank) * ks + j) * slice);
+                const float4 x0 = __ldcg(sl + (size_t)c4 * BM + mrow);
+                const float4 x1 = __ldcg(sl + (size_t)(c4 + 1) * BM + mrow);
                 a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w;
                 a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
               }
@@ -735,11 +708,6 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
         }
       }
     }
-    if (threadIdx.x == 0) bulk_wait_read_all();  // no copy still reads this CTA's memory at exit
-    // every peer has received its slices from this CTA before any CTA of the
-    // cluster leaves (its slots must stay valid until then)
-    __syncwarp();
-    cluster_sync();
   }
 
   // ---------------- teardown ----------------
@@ -749,6 +717,28 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// The split-K workspaces come from the device's default stream-ordered memory
+// pool.  Freed blocks stay in the pool (release threshold raised once per
+// device, outside stream capture) instead of going back to the driver at
+// every synchronization, so a launch after a synchronize does not map new
+// memory.
+void keep_pool_memory(cudaStream_t stream) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev]) return;
+  cudaMemPool_t pool;
+  if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+    uint64_t keep = uint64_t(1) << 30;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  }
+  done[dev] = true;
 }
 
 // k split of a grid of `tiles` output tiles: double it while the grid stays
@@ -767,7 +757,9 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   const int nkb = (a.K + BK - 1) / BK;
   int ks = 1;
   const char* env = getenv("TLQ_PREFILL_KSPLIT");
-  if (env) {
+  if (a.no_alloc) {
+    ks = 1;  // a k split needs a workspace
+  } else if (env) {
     ks = atoi(env);
   } else {
     ks = ksplit_for(ntile * mtile, nkb, sms);
@@ -857,7 +849,21 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   }
   lc.attrs = attrs;
   lc.numAttrs = na;
+  // k split: the partial slices go through a stream-ordered FP32 workspace of
+  // this launch (NMT * ksplit^2 slices of BM x BN/ksplit floats per cluster,
+  // i.e. ksplit partial tiles), freed in stream order after it
+  p.ws = nullptr;
+  if (p.ksplit > 1) {
+    const size_t wsb = (size_t)ntile * mtile * NMT * p.ksplit * BM * BN * sizeof(float);
+    keep_pool_memory(stream);
+    cudaError_t ea = cudaMallocAsync(reinterpret_cast<void**>(&p.ws), wsb, stream);
+    if (ea != cudaSuccess) return cuda_error(ea, "prefill: split-K workspace");
+  }
   cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, wmap, cmap, p);
+  if (p.ws) {
+    const cudaError_t ef = cudaFreeAsync(p.ws, stream);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) return cuda_error(e, "prefill: launch");
   if (log_enabled())
     fprintf(stderr,
@@ -881,7 +887,7 @@ tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
     const int ntile = (a.N + BN - 1) / BN;
     const int mt2 = (a.M + 2 * BM - 1) / (2 * BM);
     const int nkb = (a.K + BK - 1) / BK;
-    const int ks2 = ksplit_for(ntile * mt2, nkb, sms);
+    const int ks2 = a.no_alloc ? 1 : ksplit_for(ntile * mt2, nkb, sms);
     const int ctas2 = ntile * mt2 * ks2;
     nmt = (a.M > BM && 5 * ctas2 >= 3 * sms && (ks2 == 1 || (ks2 == 2 && nkb / ks2 >= 32))) ? 2 : 1;
   }

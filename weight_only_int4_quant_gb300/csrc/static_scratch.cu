@@ -6,7 +6,8 @@
 // hands the layer its input and output tensors, or code that must not touch
 // the allocator at all.  For them the four FP16 intermediates of the loop
 // block (norm output, QKV, O and UP activations) live in one static device
-// array of this file instead of caller-owned buffers.
+// array of this file instead of caller-owned buffers, and the GEMMs run
+// without the prefill kernel's k split (which needs a workspace).
 #include <mutex>
 
 #include "common.cuh"
@@ -66,5 +67,5 @@ extern "C" tlq_status tl_loop_block_forward_static_scratch(float* x, const tl_bl
   b.qkv_out = reinterpret_cast<uint16_t*>(base + hb);
   b.o_out = reinterpret_cast<uint16_t*>(base + hb + qb);
   b.up_out = reinterpret_cast<uint16_t*>(base + hb + qb + ob);
-  return tl_loop_block_forward(x, &b, L, M, stream);
+  return tlq::loop_block_forward_no_alloc(x, &b, L, M, "tl_loop_block_forward_static_scratch", stream);
 }
