@@ -741,29 +741,11 @@ void keep_pool_memory(cudaStream_t stream) {
   done[dev] = true;
 }
 
-// k split of a grid of `tiles` output tiles: double it while the grid stays
-// within half the SMs and every slice keeps at least 4 stages.
-int ksplit_for(int tiles, int nkb, int sms) {
-  int ks = 1;
-  while (ks < 8 && tiles * ks * 2 <= sms && nkb / (ks * 2) >= 4) ks *= 2;
-  return ks;
-}
-
 template <int BITS, int EPI, int NMT>
-tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
-  const int sms = device_info().sms;
+tlq_status launch_impl(const GemmArgs& a, int ks, cudaStream_t stream) {
   const int ntile = (a.N + BN - 1) / BN;
   const int mtile = (a.M + BM * NMT - 1) / (BM * NMT);
   const int nkb = (a.K + BK - 1) / BK;
-  int ks = 1;
-  const char* env = getenv("TLQ_PREFILL_KSPLIT");
-  if (a.no_alloc) {
-    ks = 1;  // a k split needs a workspace
-  } else if (env) {
-    ks = atoi(env);
-  } else {
-    ks = ksplit_for(ntile * mtile, nkb, sms);
-  }
   if (ks != 1 && ks != 2 && ks != 4 && ks != 8) return set_error(TLQ_EINVAL, "prefill: k split %d", ks);
   const int per = (nkb + ks - 1) / ks;
   const int ks_eff = (nkb + per - 1) / per;
@@ -873,25 +855,97 @@ tlq_status launch_impl(const GemmArgs& a, cudaStream_t stream) {
   return TLQ_OK;
 }
 
-// Two token tiles per CTA (one dequantized weight tile feeds both) when M
-// has two tiles and that grid fills most SMs, either without a k split or
-// with a 2-way split whose slices keep at least 32 stages (the reduction runs
-// once per token tile; measured slower with shorter slices or wider splits);
-// TLQ_PREFILL_NMT=1|2 forces the choice.
+// Clusters of `ks` CTAs of this kernel that fit on the GPU at once (one CTA
+// per SM; a cluster needs ks free SMs of one GPC), from the occupancy API,
+// cached per cluster size.
+template <int BITS, int EPI, int NMT>
+int max_clusters(int ks) {
+  static std::mutex mu;
+  static int cache[4] = {0, 0, 0, 0};
+  const int idx = ks == 1 ? 0 : ks == 2 ? 1 : ks == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[idx] == 0) {
+    int n = 0;
+    if (ks == 1) {
+      n = device_info().sms;
+    } else {
+      auto kern = prefill_kernel<BITS, EPI, NMT>;
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PCfg<NMT>::SMEM);
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3(1, 1, (unsigned)ks);
+      lc.blockDim = dim3(PCfg<NMT>::THREADS, 1, 1);
+      lc.dynamicSmemBytes = PCfg<NMT>::SMEM;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = 1;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = (unsigned)ks;
+      lc.attrs = &at;
+      lc.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = device_info().sms / (2 * ks);  // conservative: half the SMs
+      }
+    }
+    cache[idx] = n;
+  }
+  return cache[idx];
+}
+
+// Estimated time of a launch with NMT token tiles per CTA and a k split of
+// ks: waves x (stages per slice x stage time + fixed cost).  The constants
+// are measured on GB300 (sweeps of every projection shape at M = 256 ..
+// 1024, graph-replayed): a 64-k stage takes about 0.70 us with one token
+// tile and 0.77 us with two (SMs busy with other CTAs); the fixed cost
+// (launch, first stage, epilogue) is about 1.6 / 3.5 us without a k split
+// and 8.3 / 13.5 us with one (the partial tiles' exchange through L2).
+double prefill_estimate_us(int nmt, int ks, int tiles, int nkb, int clusters) {
+  const int waves = (tiles + clusters - 1) / clusters;
+  const int stages = (nkb + ks - 1) / ks;
+  const double stage_us = nmt == 1 ? 0.70 : 0.77;
+  const double fixed_us = ks == 1 ? (nmt == 1 ? 1.6 : 3.5) : (nmt == 1 ? 8.3 : 13.5);
+  return waves * (stages * stage_us + fixed_us);
+}
+
+// Token tiles per CTA (two share one dequantized weight tile) and k split:
+// the candidate with the smallest estimate among NMT in {1, 2} (2 only when
+// M has two token tiles) and ks in {1, 2, 4, 8} with slices of at least 4
+// stages; ties keep the first (fewer tiles, smaller split).
+// TLQ_PREFILL_NMT=1|2 and TLQ_PREFILL_KSPLIT=1|2|4|8 force either choice;
+// callers that may not allocate get no k split.
 template <int BITS, int EPI>
 tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
-  int nmt = 0;
-  if (const char* e = getenv("TLQ_PREFILL_NMT")) nmt = atoi(e);
-  if (nmt != 1 && nmt != 2) {
-    const int sms = device_info().sms;
-    const int ntile = (a.N + BN - 1) / BN;
-    const int mt2 = (a.M + 2 * BM - 1) / (2 * BM);
-    const int nkb = (a.K + BK - 1) / BK;
-    const int ks2 = a.no_alloc ? 1 : ksplit_for(ntile * mt2, nkb, sms);
-    const int ctas2 = ntile * mt2 * ks2;
-    nmt = (a.M > BM && 5 * ctas2 >= 3 * sms && (ks2 == 1 || (ks2 == 2 && nkb / ks2 >= 32))) ? 2 : 1;
+  int force_nmt = 0, force_ks = 0;
+  if (const char* e = getenv("TLQ_PREFILL_NMT")) force_nmt = atoi(e);
+  if (const char* e = getenv("TLQ_PREFILL_KSPLIT")) force_ks = atoi(e);
+  if (force_nmt != 1 && force_nmt != 2) force_nmt = 0;
+  if (a.no_alloc) force_ks = 1;  // a k split needs a workspace
+  const int ntile = (a.N + BN - 1) / BN;
+  const int nkb = (a.K + BK - 1) / BK;
+  int best_nmt = 1, best_ks = 1;
+  double best = 1e30;
+  for (int nmt = 1; nmt <= 2; ++nmt) {
+    if (force_nmt && nmt != force_nmt) continue;
+    if (nmt == 2 && a.M <= BM && !force_nmt) continue;
+    const int tiles = ntile * ((a.M + BM * nmt - 1) / (BM * nmt));
+    for (int ks = 1; ks <= 8; ks *= 2) {
+      if (force_ks ? ks != force_ks : (ks > 1 && nkb / ks < 4)) continue;
+      const int clusters = nmt == 1 ? max_clusters<BITS, EPI, 1>(ks) : max_clusters<BITS, EPI, 2>(ks);
+      const double t = prefill_estimate_us(nmt, ks, tiles, nkb, clusters);
+      if (t < best) {
+        best = t;
+        best_nmt = nmt;
+        best_ks = ks;
+      }
+    }
   }
-  return nmt == 2 ? launch_impl<BITS, EPI, 2>(a, s) : launch_impl<BITS, EPI, 1>(a, s);
+  if (best > 1e29) return set_error(TLQ_EINVAL, "prefill: k split %d", force_ks);
+  if (log_enabled()) {
+    const int c1 = best_nmt == 1 ? max_clusters<BITS, EPI, 1>(best_ks) : max_clusters<BITS, EPI, 2>(best_ks);
+    fprintf(stderr, "[tlq] prefill M=%d N=%d K=%d: %d token tile(s), k split %d (%d clusters fit), est %.1f us\n",
+            a.M, a.N, a.K, best_nmt, best_ks, c1, best);
+  }
+  return best_nmt == 2 ? launch_impl<BITS, EPI, 2>(a, best_ks, s) : launch_impl<BITS, EPI, 1>(a, best_ks, s);
 }
 
 template <int BITS>
