@@ -106,6 +106,24 @@ def test_decode_deterministic(lib):
     assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
 
 
+@pytest.mark.parametrize("bits,group,N,K", [(4, 128, 200, 2048), (4, 32, 96, 512), (4, 64, 136, 384),
+                                            (2, 64, 72, 448), (2, 128, 120, 2048), (4, 128, 64, 8192)])
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_decode_unit_heights_bitwise(lib, monkeypatch, bits, group, N, K, M):
+    """Units of 16, 32 and 64 weight rows (TLQ_DECODE_ROWS) give the same
+    bits, ragged last units included: a row's sums do not depend on the rows
+    that share its unit.  The oracle agrees with all of them."""
+    case = synth.gemm_case(M, N, K, bits, group, seed=M + N + K)
+    outs = {}
+    for rows in ("16", "32", "64"):
+        monkeypatch.setenv("TLQ_DECODE_ROWS", rows)
+        _, outs[rows] = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(outs["16"], ref, "16-row units int%d g%d M%d N%d K%d" % (bits, group, M, N, K))
+    for rows in ("32", "64"):
+        assert np.array_equal(outs[rows].view(np.uint16), outs["16"].view(np.uint16)), rows
+
+
 # ---------------------------------------------------------------------------
 # full-size decode configurations (the four D = 2048 projections), sampled
 # outputs against the oracle evaluated point by point

@@ -796,13 +796,20 @@ bool build_unit_lists(DecodeLaunch& L, int grid) {
   return true;
 }
 
+bool same_args(const GemmArgs& x, const GemmArgs& y) {
+  return x.A == y.A && x.lda == y.lda && x.W == y.W && x.S == y.S && x.Z == y.Z && x.C == y.C && x.ldc == y.ldc &&
+         x.X == y.X && x.ldx == y.ldx && x.M == y.M && x.N == y.N && x.K == y.K && x.bits == y.bits &&
+         x.group == y.group && x.epi == y.epi && x.l2_keep == y.l2_keep && x.no_alloc == y.no_alloc;
+}
+
+// The launch description of a call: tensor maps, problem table, unit lists,
+// shared memory size and grid.
 template <int BITS, int RGW, int NT>
-tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
+tlq_status build_launch(const GemmArgs* a, int count, DecodeLaunch& L, size_t& smem_out, int& grid_out,
+                        int& units_out) {
   using F = Fmt<BITS>;
   constexpr int ROWS = 16 * RGW;
   constexpr int MT = 8 * NT;
-  static_assert(sizeof(DecodeLaunch) < 30000, "kernel parameter space");
-  DecodeLaunch L;
   memset(&L, 0, sizeof(L));
   // problems with more k-blocks per unit first (snake order then balances)
   int order[kMaxProblems];
@@ -859,6 +866,37 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   if (smem > (size_t)device_info().smem_optin)
     return set_error(TLQ_EUNSUPPORTED, "decode: K/group = %d needs %zu bytes of shared memory (limit %d)", gmax,
                      smem, device_info().smem_optin);
+  const int grid = std::max(1, std::min(units, device_info().sms));
+  L.listed = build_unit_lists(L, grid) ? 1 : 0;
+  if (units > kMaxRounds * grid)
+    return set_error(TLQ_EUNSUPPORTED, "decode: %d row tiles exceed %d per launch", units, kMaxRounds * grid);
+  smem_out = smem;
+  grid_out = grid;
+  units_out = units;
+  return TLQ_OK;
+}
+
+// Launch descriptions of the last few calls per kernel, keyed by their full
+// argument lists: a decode loop repeats the same calls, and rebuilding the
+// description (12 tensor maps and the longest-first lists of a decode step)
+// costs more host time than the launch itself.
+constexpr int kLaunchCache = 8;
+
+template <int BITS, int RGW, int NT>
+tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
+  constexpr int ROWS = 16 * RGW;
+  static_assert(sizeof(DecodeLaunch) < 30000, "kernel parameter space");
+  struct Entry {
+    bool valid;
+    int count;
+    GemmArgs args[kMaxProblems];
+    DecodeLaunch L;
+    size_t smem;
+    int grid, units;
+  };
+  static std::mutex mu;
+  static Entry cache[kLaunchCache];
+  static int next = 0;
   auto kern = decode_kernel<BITS, RGW, NT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -867,10 +905,31 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   });
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "decode: cudaFuncSetAttribute");
 
-  const int grid = std::max(1, std::min(units, device_info().sms));
-  L.listed = build_unit_lists(L, grid) ? 1 : 0;
-  if (units > kMaxRounds * grid)
-    return set_error(TLQ_EUNSUPPORTED, "decode: %d row tiles exceed %d per launch", units, kMaxRounds * grid);
+  std::lock_guard<std::mutex> lk(mu);
+  Entry* hit = nullptr;
+  for (Entry& e : cache) {
+    if (!e.valid || e.count != count) continue;
+    bool same = true;
+    for (int i = 0; i < count && same; ++i) same = same_args(e.args[i], a[i]);
+    if (same) {
+      hit = &e;
+      break;
+    }
+  }
+  if (!hit) {
+    Entry& e = cache[next];
+    next = (next + 1) % kLaunchCache;
+    e.valid = false;
+    tlq_status st = build_launch<BITS, RGW, NT>(a, count, e.L, e.smem, e.grid, e.units);
+    if (st != TLQ_OK) return st;
+    e.count = count;
+    for (int i = 0; i < count; ++i) e.args[i] = a[i];
+    e.valid = true;
+    hit = &e;
+  }
+  const DecodeLaunch& L = hit->L;
+  const size_t smem = hit->smem;
+  const int grid = hit->grid, units = hit->units;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
@@ -889,6 +948,40 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   return TLQ_OK;
 }
 
+// Rows per unit: 64, halved while the launch would have fewer row tiles than
+// a third of the SMs, and once more when every problem has long rows (at
+// least 32 k-blocks), since a long unit on few SMs then sets the time.
+// Measured on the projection shapes at M = 1, 4, 16 (single launches): O
+// (N = 2048, K = 2048) is fastest with 32-row units (2.64 against 3.26 us at
+// M = 1), DOWN (N = 2048, K = 8192) with 16-row units (6.56 against 9.45 us);
+// QKV, UP and the batched decode step keep 64.  Launches whose weights are
+// kept in L2 (the loop block) also keep 64: they are short, and the next
+// kernel's early start on the SMs they leave idle matters more (the loop
+// block at M = 1 measured 5 % slower, INT2 14 %, with the smaller units).
+// The unit height does not change any result: every row's sums are formed
+// the same way.  TLQ_DECODE_ROWS=16|32|64 forces it.
+template <int BITS>
+int decode_rgw(const GemmArgs* a, int count) {
+  if (const char* e = getenv("TLQ_DECODE_ROWS")) {
+    const int r = atoi(e);
+    if (r == 16 || r == 32 || r == 64) return r / 16;
+  }
+  for (int i = 0; i < count; ++i)
+    if (a[i].l2_keep) return 4;
+  const int sms = device_info().sms;
+  bool long_rows = true;
+  for (int i = 0; i < count; ++i) long_rows &= (a[i].K + Fmt<BITS>::KBLK - 1) / Fmt<BITS>::KBLK >= 32;
+  auto units = [&](int rgw) {
+    int u = 0;
+    for (int i = 0; i < count; ++i) u += (a[i].N + 16 * rgw - 1) / (16 * rgw);
+    return u;
+  };
+  int rgw = 4;
+  while (rgw > 1 && 3 * units(rgw) < sms) rgw /= 2;
+  if (rgw > 1 && rgw < 4 && long_rows && units(rgw) < sms) rgw /= 2;
+  return rgw;
+}
+
 // One launch per call: the two-token-tile kernel when any problem has M > 8
 // (its problems with M <= 8 take the one-tile path inside it).  Splitting the
 // call into a one-tile and a two-tile launch was measured slower for the INT4
@@ -897,7 +990,11 @@ template <int BITS>
 tlq_status dispatch_bits(const GemmArgs* a, int count, cudaStream_t s) {
   bool two = false;
   for (int i = 0; i < count; ++i) two |= a[i].M > 8;
-  return two ? launch_impl<BITS, 4, 2>(a, count, s) : launch_impl<BITS, 4, 1>(a, count, s);
+  switch (decode_rgw<BITS>(a, count)) {
+    case 1: return two ? launch_impl<BITS, 1, 2>(a, count, s) : launch_impl<BITS, 1, 1>(a, count, s);
+    case 2: return two ? launch_impl<BITS, 2, 2>(a, count, s) : launch_impl<BITS, 2, 1>(a, count, s);
+    default: return two ? launch_impl<BITS, 4, 2>(a, count, s) : launch_impl<BITS, 4, 1>(a, count, s);
+  }
 }
 
 }  // namespace
