@@ -349,7 +349,7 @@ def kernel_hash():
 # dram bytes (read + write) per launch of the decode kernel for the headline
 # step, from the ncu capture summarised in profiles/ (None until captured for
 # the current kernel source).
-NCU_TRAFFIC = {"kernel_hash": "f3ea37d43d4b1305", "bytes_per_step": 81990144}  # profiles/decode_kernel_int4_decode_step.md
+NCU_TRAFFIC = {"kernel_hash": "cba6c383ea698f1d", "bytes_per_step": 82121472}  # profiles/decode_kernel_int4_decode_step.md
 
 
 def run_tlq(args, rank, world, dist):
