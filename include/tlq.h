@@ -13,9 +13,18 @@
  * void* (NULL = the legacy default stream).
  *
  * Conventions shared by every entry point
- *  - Ownership: the caller owns all memory.  No entry point allocates device
- *    memory or keeps state between calls (tl_loop_block_forward_static_scratch
- *    uses a static array the library owns, see there).
+ *  - Ownership: the caller owns every input, output and scratch buffer.
+ *    The one device allocation the library makes is transient: a GEMM with
+ *    M > 16 whose tiles would leave SMs idle splits K over a thread-block
+ *    cluster and takes an FP32 workspace for the partial tiles from the
+ *    device's stream-ordered pool (cudaMallocAsync before the kernel,
+ *    cudaFreeAsync after it, both on `stream`; under graph capture they
+ *    become memory nodes).  The pool's release threshold is raised once per
+ *    device so that freed blocks stay cached.  tl_loop_block_forward_static_
+ *    scratch allocates nothing: it uses a static array the library owns and
+ *    runs its GEMMs without a k split.  Host state: the library keeps the
+ *    launch descriptions (tensor maps, work lists) of recent calls, keyed by
+ *    their full argument lists; it keeps no device state between calls.
  *  - Ordering: calls are asynchronous and ordered on `stream`.  Apart from
  *    tl_loop_block_forward_static_scratch the library holds no shared
  *    scratch, so calls on different streams with disjoint buffers may run
@@ -34,6 +43,12 @@
  *  - Determinism: identical inputs give bit-identical outputs on every call
  *    (no floating-point atomics, fixed reduction order) -- "Model", section
  *    "Determinism".
+ *  - Environment (read by the library; none is needed): TLQ_LOG=1 prints each
+ *    launch's configuration to stderr; TLQ_PDL=0 turns programmatic dependent
+ *    launch off; TLQ_PREFILL_NMT=1|2, TLQ_PREFILL_KSPLIT=1|2|4|8 and
+ *    TLQ_DECODE_ROWS=16|32|64 force the kernels' tiling choices (for tests
+ *    and measurements; the results of the decode kernel do not depend on
+ *    TLQ_DECODE_ROWS).
  */
 #ifndef TLQ_H_
 #define TLQ_H_
