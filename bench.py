@@ -240,19 +240,23 @@ class StepGraphs:
     def __init__(self, torch, run, phases, min_chunk=16):
         self.torch, self.run, self.phases = torch, run, phases
         self.chunk = phases * max(1, -(-min_chunk // phases))
+        # warm the launch path outside capture, then capture on the same stream
+        # (the library sets up per-stream resources, such as the side streams
+        # of a batched call, outside capture only)
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            for p in range(phases):  # warm the launch path outside capture
+            for p in range(phases):
                 run(p)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
+        self.stream = s
         self.main = self._capture(self.chunk, 0)
         self.rest = {}
 
     def _capture(self, n, start):
         g = self.torch.cuda.CUDAGraph()
-        with self.torch.cuda.graph(g):
+        with self.torch.cuda.graph(g, stream=self.stream):
             for i in range(n):
                 self.run((start + i) % self.phases)
         self.torch.cuda.synchronize()

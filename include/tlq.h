@@ -122,8 +122,11 @@ typedef struct {
  * tl_quant_gemm_batched -- several independent quant_gemm problems in as few
  * launches as possible: every problem with M <= 16 of one bit width goes into
  * one persistent decode launch (up to 16 problems per launch), each larger
- * problem gets its own tensor-core launch.  Results equal `count` separate
- * tl_quant_gemm calls.  Same source passages as tl_quant_gemm; batching is a
+ * problem gets its own tensor-core launch.  Those launches run side by side
+ * on up to three library-owned streams per caller stream, forked from
+ * `stream` and joined back with events (so the call's work still completes in
+ * `stream` order, and a graph capture of `stream` records the fork and join).
+ * Results equal `count` separate tl_quant_gemm calls.  Same source passages as tl_quant_gemm; batching is a
  * launch-overhead measure of this library (the layers of one decode step that
  * do not depend on each other, or several requests at once).
  *   descs  HOST array of `count` descriptors (count >= 0; 0 is a no-op).

@@ -1,4 +1,5 @@
 // C ABI of libtlq: argument validation, dispatch and error reporting.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -265,6 +266,64 @@ tlq_status check_batched(const tl_gemm_desc* d, int count) {
 }
 }  // namespace
 
+namespace {
+// Side streams for the independent prefill problems of one batched call: per
+// (device, caller stream) three non-blocking streams, with events that fork
+// them from the caller's stream and join them back.  The problems then run
+// side by side (each launch alone fills only part of the GPU at short M);
+// the event record / wait pairs also carry the fork and join into a graph
+// capture of the caller's stream.  Sets are created outside stream capture
+// (a capture with no set for its stream launches the problems in order).
+constexpr int kSideStreams = 3;
+constexpr int kSideSets = 16;
+struct SideSet {
+  int dev;
+  cudaStream_t caller;
+  cudaStream_t s[kSideStreams];
+  cudaEvent_t fork, join[kSideStreams];
+};
+std::mutex g_side_mu;
+SideSet g_side[kSideSets];
+int g_nside = 0;
+
+SideSet* side_streams(cudaStream_t caller) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  for (int i = 0; i < g_nside; ++i)
+    if (g_side[i].dev == dev && g_side[i].caller == caller) return &g_side[i];
+  if (g_nside == kSideSets) return nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+  SideSet& e = g_side[g_nside];
+  e.dev = dev;
+  e.caller = caller;
+  int made = 0;
+  bool ok = cudaEventCreateWithFlags(&e.fork, cudaEventDisableTiming) == cudaSuccess;
+  for (; ok && made < kSideStreams; ++made) {
+    if (cudaStreamCreateWithFlags(&e.s[made], cudaStreamNonBlocking) != cudaSuccess) {
+      ok = false;
+      break;
+    }
+    if (cudaEventCreateWithFlags(&e.join[made], cudaEventDisableTiming) != cudaSuccess) {
+      cudaStreamDestroy(e.s[made]);
+      ok = false;
+      break;
+    }
+  }
+  if (!ok) {
+    for (int k = 0; k < made; ++k) {
+      cudaStreamDestroy(e.s[k]);
+      cudaEventDestroy(e.join[k]);
+    }
+    cudaGetLastError();
+    return nullptr;
+  }
+  ++g_nside;
+  return &e;
+}
+}  // namespace
+
 tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_) {
   g_msg[0] = 0;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -289,14 +348,31 @@ tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_
       if (st != TLQ_OK) return st;
     }
   }
-  for (int i = 0; i < count; ++i) {
-    if (d[i].M <= 16) continue;
-    tlq_status st = launch_prefill(plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N,
-                                              d[i].K, d[i].bits, d[i].group),
-                                   stream);
-    if (st != TLQ_OK) return st;
+  // the other problems: one prefill launch each, several at a time on side streams
+  int np = 0;
+  for (int i = 0; i < count; ++i) np += d[i].M > 16;
+  SideSet* ss = np > 1 ? side_streams(stream) : nullptr;
+  const int used = ss ? std::min(np - 1, kSideStreams) : 0;
+  if (ss) {
+    cudaError_t e = cudaEventRecord(ss->fork, stream);
+    for (int k = 0; k < used && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(ss->s[k], ss->fork, 0);
+    if (e != cudaSuccess) return cuda_error(e, "tl_quant_gemm_batched: fork");
   }
-  return TLQ_OK;
+  tlq_status st = TLQ_OK;
+  for (int i = 0, j = 0; i < count && st == TLQ_OK; ++i) {
+    if (d[i].M <= 16) continue;
+    const int lane = used ? j % (used + 1) : 0;  // 0: the caller's stream
+    ++j;
+    st = launch_prefill(plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
+                                   d[i].bits, d[i].group),
+                        lane ? ss->s[lane - 1] : stream);
+  }
+  for (int k = 0; k < used; ++k) {  // join even after a failed launch
+    cudaError_t e = cudaEventRecord(ss->join[k], ss->s[k]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ss->join[k], 0);
+    if (e != cudaSuccess && st == TLQ_OK) st = cuda_error(e, "tl_quant_gemm_batched: join");
+  }
+  return st;
 }
 
 tlq_status tl_pack_weights(const uint8_t* codes, uint32_t* Wpacked, int N, int K, int bits, void* stream) {
