@@ -353,7 +353,7 @@ def kernel_hash():
 # dram bytes (read + write) per launch of the decode kernel for the headline
 # step, from the ncu capture summarised in profiles/ (None until captured for
 # the current kernel source).
-NCU_TRAFFIC = {"kernel_hash": "ae65a74f45eb4465", "bytes_per_step": 82124288}  # profiles/decode_kernel_int4_decode_step.md
+NCU_TRAFFIC = {"kernel_hash": "45e6d1b88a26a99b", "bytes_per_step": 82026240}  # profiles/decode_kernel_int4_decode_step.md
 
 
 def run_tlq(args, rank, world, dist):
