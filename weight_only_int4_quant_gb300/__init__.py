@@ -195,7 +195,10 @@ def gemm_descs(problems):
 def tl_quant_gemm_batched(descs, stream=None) -> None:
     """Run independent quant_gemm problems in as few launches as possible;
     ``descs`` is a list of (A, W, scales, zeros, C, bits, group) tuples or the
-    array gemm_descs() returns."""
+    array gemm_descs() returns.  Problems with M > 16 run side by side on the
+    library's side streams for ``stream``, joined back before later work on
+    ``stream``; capture a graph on a stream that has made one call outside
+    capture to keep that in the graph."""
     if not isinstance(descs, ctypes.Array):
         descs = gemm_descs(descs)
     _raise_if(load().tl_quant_gemm_batched(descs, len(descs), _stream(stream)))
