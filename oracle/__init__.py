@@ -21,7 +21,8 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   quant_gemm                       exact rational sum rounded once (brute force),
                                    closed forms, torch binary64 matmul
   quant_gemm_points                equality with quant_gemm
-  rms_norm_half                    closed forms (constant rows, scale invariance)
+  rms_norm_half                    closed forms (constant rows, scale invariance),
+                                   exact rational values where eps matters
   loop_block                       brute force on tiny shapes, closed form
                                    (zero update), split-iteration invariant
   swiglu                           closed forms (g = 0, u = 0, large |g|),
@@ -61,7 +62,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + ".tmp%d" % os.getpid()
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-               "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+               "-fno-fast-math", "-fopenmp", _SRC, "-o", tmp, "-lm"]
         subprocess.check_call(cmd)
         os.replace(tmp, _SO)
     return _SO
@@ -90,6 +91,7 @@ def _load():
                 "orc_requant_int4_to_int2": [P, P, P, I, I, I, P, P, P],
                 "orc_swiglu": [P, P, P, ctypes.c_size_t],
                 "orc_loop_block_swiglu": [P, I, I, I, P, P, P, P, P, I, I, I, I, ctypes.c_double],
+                "orc_set_threads": [I],
             }.items():
                 f = getattr(lib, name)
                 f.restype = ctypes.c_int
@@ -114,6 +116,13 @@ def _half_bits(a) -> np.ndarray:
 def _check(rc: int, what: str):
     if rc != 0:
         raise ValueError("oracle %s rejected its arguments (rc=%d)" % (what, rc))
+
+
+def set_threads(n: int) -> int:
+    """Host threads the GEMM's output rows are shared over (1 = single
+    thread); 0 keeps the current count.  Returns the count in effect.  The
+    results do not depend on it: every output is the same k-order sum."""
+    return _load().orc_set_threads(int(n))
 
 
 # ----------------------------------------------------------------------------

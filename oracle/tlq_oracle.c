@@ -41,6 +41,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ------------------------------------------------------------------ */
 /* IEEE-754 binary16 <-> binary64, written from the format definition. */
@@ -185,39 +188,56 @@ int orc_dequant_half(const uint32_t* W, const uint16_t* scales, const uint16_t* 
 /* ------------------------------------------------------------------ */
 
 /* C[m][n] (row stride ldc) = fp16( sum_k A[m][k] (row stride lda) * w[n][k] ).
- * Binary64 accumulation in plain k order, one final rounding. */
+ * Binary64 accumulation in plain k order, one final rounding.  Output rows n
+ * are independent, so they are shared out over the host's threads (OpenMP);
+ * each output is still the same plain k-order sum whatever the thread count. */
 int orc_quant_gemm(const uint16_t* A, int lda, const uint32_t* W, const uint16_t* scales,
                    const uint16_t* zeros, uint16_t* C, int ldc, int M, int N, int K,
                    int bits, int group) {
   if (check_shape(N, K, bits, group) || M < 0 || lda < K || ldc < N) return -1;
-  double* wrow = (double*)malloc(sizeof(double) * (size_t)K);
   double* arow = (double*)malloc(sizeof(double) * (size_t)K * (M > 0 ? M : 1));
-  if (!wrow || !arow) {
-    free(wrow);
-    free(arow);
-    return -2;
-  }
+  if (!arow) return -2;
   for (int m = 0; m < M; ++m)
     for (int k = 0; k < K; ++k) arow[(size_t)m * K + k] = orc_half_to_double(A[(size_t)m * lda + k]);
   int wpr = K * bits / 32;
   int G = K / group;
-  for (int n = 0; n < N; ++n) {
-    for (int k = 0; k < K; ++k) {
-      double q = (double)code_at(W + (size_t)n * wpr, k, bits);
-      double s = orc_half_to_double(scales[(size_t)n * G + k / group]);
-      double z = orc_half_to_double(zeros[(size_t)n * G + k / group]);
-      wrow[k] = (q - z) * s;
+  int bad = 0;
+#pragma omp parallel reduction(| : bad)
+  {
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!wrow) bad = 1;
+#pragma omp for schedule(static)
+    for (int n = 0; n < N; ++n) {
+      if (!wrow) continue;
+      for (int k = 0; k < K; ++k) {
+        double q = (double)code_at(W + (size_t)n * wpr, k, bits);
+        double s = orc_half_to_double(scales[(size_t)n * G + k / group]);
+        double z = orc_half_to_double(zeros[(size_t)n * G + k / group]);
+        wrow[k] = (q - z) * s;
+      }
+      for (int m = 0; m < M; ++m) {
+        double acc = 0.0;
+        const double* a = arow + (size_t)m * K;
+        for (int k = 0; k < K; ++k) acc += a[k] * wrow[k];
+        C[(size_t)m * ldc + n] = orc_double_to_half(acc);
+      }
     }
-    for (int m = 0; m < M; ++m) {
-      double acc = 0.0;
-      const double* a = arow + (size_t)m * K;
-      for (int k = 0; k < K; ++k) acc += a[k] * wrow[k];
-      C[(size_t)m * ldc + n] = orc_double_to_half(acc);
-    }
+    free(wrow);
   }
-  free(wrow);
   free(arow);
-  return 0;
+  return bad ? -2 : 0;
+}
+
+/* Thread count of the OpenMP loops above (1 = the plain single-thread
+ * oracle); returns the count now in effect. */
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
 }
 
 /* The same definition evaluated at P chosen output positions (pm[i], pn[i]);
