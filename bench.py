@@ -165,6 +165,10 @@ class Workload:
             self.C[M, name] = self.C_flat[oc:oc + M * N].view(M, N)
             oa += M * K
             oc += M * N
+        # each tensor-core problem's own k-split workspace (the problems of a
+        # step may run side by side), allocated here by torch
+        self.ws = {(M, name): tlq.gemm_workspace(M, shapes[name][0], shapes[name][1], bits, self.group)
+                   for M in Ms for name in shapes}
         torch.cuda.synchronize()
         self.step_bytes = sum(gemm_bytes(M, N, K, bits, self.group) for M in Ms for (N, K) in shapes.values())
         self.step_flops = sum(2 * M * N * K for M in Ms for (N, K) in shapes.values())
@@ -185,7 +189,8 @@ class Workload:
                 cp = self.copies[(len(self.Ms) * i + j) % ncopy]
                 for name in self.shapes:
                     W, s, z = cp[name]
-                    probs.append((self.A[M, name], W, s, z, self.C[M, name], self.bits, self.group))
+                    probs.append((self.A[M, name], W, s, z, self.C[M, name], self.bits, self.group,
+                                  self.ws[M, name]))
             self._descs[key] = self.tlq.gemm_descs(probs)
         return self._descs[key]
 
@@ -209,7 +214,7 @@ class Workload:
                     N, K = self.shapes[name]
                     W, s, z = cp[name]
                     probs.append((A_flat[oa:oa + M * K].view(M, K), W, s, z, C_flat[oc:oc + M * N].view(M, N),
-                                  self.bits, self.group))
+                                  self.bits, self.group, self.ws[M, name] if tag == 0 else None))
                     oa += M * K
                     oc += M * N
             self._descs_on[key] = self.tlq.gemm_descs(probs)
@@ -351,9 +356,9 @@ def kernel_hash():
 
 
 # dram bytes (read + write) per launch of the decode kernel for the headline
-# step, from the ncu capture summarised in profiles/ (None until captured for
-# the current kernel source).
-NCU_TRAFFIC = {"kernel_hash": "45e6d1b88a26a99b", "bytes_per_step": 82026240}  # profiles/decode_kernel_int4_decode_step.md
+# step, from one ncu capture of that launch; used only while the kernel source
+# hashes to the captured one.
+NCU_TRAFFIC = {"kernel_hash": "45e6d1b88a26a99b", "bytes_per_step": 82026240}
 
 
 def run_tlq(args, rank, world, dist):
@@ -680,9 +685,11 @@ def run_fp16_body(tlq, torch, peaks, l2):
             Cq = [torch.empty((M, N), dtype=torch.float16, device="cuda") for (N, _) in synth.SHAPES.values()]
             q = sets[0]
 
+            wsq = [tlq.gemm_workspace(M, N, K, 4, group) for (N, K) in synth.SHAPES.values()]
+
             def run_quant():
-                for (W, s, z, _), (N, K), C in zip(q, synth.SHAPES.values(), Cq):
-                    tlq.tl_quant_gemm(A[K], W, s, z, C, 4, group)
+                for (W, s, z, _), (N, K), C, ws in zip(q, synth.SHAPES.values(), Cq, wsq):
+                    tlq.tl_quant_gemm_ws(A[K], W, s, z, C, 4, group, ws)
 
             def run_dense():
                 for (_, _, _, body), (N, K), C in zip(q, synth.SHAPES.values(), Cq):

@@ -13,18 +13,19 @@
  * void* (NULL = the legacy default stream).
  *
  * Conventions shared by every entry point
- *  - Ownership: the caller owns every input, output and scratch buffer.
- *    The one device allocation the library makes is transient: a GEMM with
- *    M > 16 whose tiles would leave SMs idle splits K over a thread-block
- *    cluster and takes an FP32 workspace for the partial tiles from the
- *    device's stream-ordered pool (cudaMallocAsync before the kernel,
- *    cudaFreeAsync after it, both on `stream`; under graph capture they
- *    become memory nodes).  The pool's release threshold is raised once per
- *    device so that freed blocks stay cached.  tl_loop_block_forward_static_
- *    scratch allocates nothing: it uses a static array the library owns and
- *    runs its GEMMs without a k split.  Host state: the library keeps the
- *    launch descriptions (tensor maps, work lists) of recent calls, keyed by
- *    their full argument lists; it keeps no device state between calls.
+ *  - Ownership: the caller owns every input, output, scratch and workspace
+ *    buffer; the library allocates no device memory in any call.  A GEMM
+ *    with M > 16 whose tiles would leave SMs idle splits K over a
+ *    thread-block cluster and exchanges partial tiles through an FP32
+ *    workspace that the caller passes (tl_quant_gemm_ws, the workspace fields
+ *    of tl_gemm_desc, tl_block and tl_swiglu_block); the size it wants comes
+ *    from tl_quant_gemm_workspace_size.  With no workspace, or one too small,
+ *    the kernel keeps K whole (same arithmetic per output, possibly slower).
+ *    tl_loop_block_forward_static_scratch also needs no caller scratch: it
+ *    uses a static array the library owns.  Host state: the library keeps
+ *    the launch descriptions (tensor maps, work lists) of recent calls, keyed
+ *    by their full argument lists, and for tl_quant_gemm_batched up to three
+ *    side streams per caller stream; it keeps no device state between calls.
  *  - Ordering: calls are asynchronous and ordered on `stream`.  Apart from
  *    tl_loop_block_forward_static_scratch the library holds no shared
  *    scratch, so calls on different streams with disjoint buffers may run
@@ -99,7 +100,8 @@ const char* tl_version(void);
  *   group   a multiple of 32 (bits = 4) or 64 (bits = 2), dividing K;
  *           group = K (one scale per row) is allowed.
  *   M <= 16 runs the bandwidth-bound decode kernel, larger M the tensor-core
- *   (tcgen05) prefill kernel.
+ *   (tcgen05) prefill kernel, here without a k split (no workspace; see
+ *   tl_quant_gemm_ws).
  * Returns TLQ_OK, TLQ_EINVAL (null pointer, misalignment, bad shape/bits/
  * group), or TLQ_ECUDA.
  */
@@ -107,8 +109,40 @@ tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint1
                          const uint16_t* zeros, uint16_t* C, int M, int N, int K, int bits,
                          int group, void* stream);
 
-/* One problem of tl_quant_gemm_batched: the arguments of one tl_quant_gemm
- * call (device pointers, same layouts and rules). */
+/*
+ * tl_quant_gemm_workspace_size -- bytes of FP32 workspace with which the
+ * tensor-core kernel would split K for this problem (its planner's choice
+ * with no limit on the workspace); 0 when it would not split (always for
+ * M <= 16) or for an invalid shape.  Honors TLQ_PREFILL_NMT / _KSPLIT.
+ * A library choice (launch shape), not an operation of the pages.
+ */
+size_t tl_quant_gemm_workspace_size(int M, int N, int K, int bits, int group);
+
+/*
+ * tl_quant_gemm_ws -- tl_quant_gemm with a caller-owned workspace for the
+ * tensor-core kernel's k split (same operation, layouts and errors).
+ *   workspace        device buffer, 16-byte aligned, or NULL; must not
+ *                    overlap A, C or the weights.  Its contents on entry do
+ *                    not matter; on return they are undefined.  Calls whose
+ *                    executions overlap on the GPU need separate workspaces.
+ *   workspace_bytes  its size.  The kernel splits K only with a split whose
+ *                    workspace fits (the largest it wants is
+ *                    tl_quant_gemm_workspace_size); results of each output do
+ *                    not depend on it beyond FP32 summation order.
+ */
+tlq_status tl_quant_gemm_ws(const uint16_t* A, const uint32_t* Wpacked, const uint16_t* scales,
+                            const uint16_t* zeros, uint16_t* C, int M, int N, int K, int bits, int group,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* One problem of tl_quant_gemm_batched: the arguments of one
+ * tl_quant_gemm_ws call (device pointers, same layouts and rules), plus the
+ * packed weight's row stride.
+ *   ldw        row stride of Wpacked in 32-bit words; 0 = compact rows of
+ *              K*bits/32 words; else >= K*bits/32 and a multiple of 4 (an
+ *              INT2 weight converted in place keeps the INT4 stride K/8).
+ *   workspace  this problem's own k-split workspace (NULL / 0: none); the
+ *              problems of one call may run at the same time, so their
+ *              workspaces must not overlap. */
 typedef struct {
   const uint16_t* A;
   const uint32_t* Wpacked;
@@ -116,6 +150,9 @@ typedef struct {
   const uint16_t* zeros;
   uint16_t* C;
   int M, N, K, bits, group;
+  int ldw;
+  void* workspace;
+  size_t workspace_bytes;
 } tl_gemm_desc;
 
 /*
@@ -196,13 +233,17 @@ tlq_status tl_unpack_weights(const uint32_t* Wpacked, uint8_t* codes, int N, int
  *           16-byte aligned; read only.
  *   s4, z4  FP16 [N][K/group] scales / zeros of W4; finite values.
  *   W2      uint32 [N][K/16] output, compact INT2 rows; 16-byte aligned; must
- *           not overlap any other argument.
+ *           not overlap any other argument -- or exactly W4: converted in
+ *           place ("Details of the shipped kernel", storage reuse), the INT2
+ *           rows keeping the INT4 row stride of K/8 words with the second
+ *           half of every row left untouched; GEMMs then read it with
+ *           ldw = K/8 (tl_qproj, tl_gemm_desc).
  *   s2, z2  FP16 [N][K/group] output scales / zeros.  Each may be exactly its
  *           input (s2 == s4, z2 == z4: converted in place) or overlap nothing.
  *   N >= 1; K >= 1; group a multiple of 64 dividing K (the INT2 kernel's
  *   rule); the INT2 weight keeps the INT4 weight's group.
  *   The caller owns every buffer; W4 may be freed once the stream has passed
- *   the call.  Returns TLQ_OK, TLQ_EINVAL (null, misaligned, overlapping or
+ *   an out-of-place call.  Returns TLQ_OK, TLQ_EINVAL (null, misaligned, overlapping or
  *   bad shape) or TLQ_ECUDA.
  */
 tlq_status tl_requant_int4_to_int2(const uint32_t* W4, const uint16_t* s4, const uint16_t* z4, uint32_t* W2,
@@ -255,6 +296,12 @@ tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const ui
                                 const uint16_t* zeros, uint16_t* C, int M, int N2, int K, int bits, int group,
                                 void* stream);
 
+/* tl_quant_gemm_swiglu with a caller-owned k-split workspace (the rules of
+ * tl_quant_gemm_ws; its size from tl_quant_gemm_workspace_size(M, N2, K, ...)). */
+tlq_status tl_quant_gemm_swiglu_ws(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales,
+                                   const uint16_t* zeros, uint16_t* C, int M, int N2, int K, int bits, int group,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * tl_dequant_fp16 -- the FP16 body of a quantized weight: out[n][k] =
  * fp16_RNE((q - z) * s), each weight rounded once from its exact value, +0
@@ -283,13 +330,16 @@ tlq_status tl_dequant_fp16(const uint32_t* Wpacked, const uint16_t* scales, cons
 tlq_status tl_interleave_rows(const void* a, const void* b, void* out, int rows, size_t row_bytes, void* stream);
 
 /* One quantized projection of the loop block: weights [N][K] in the packed
- * format, FP16 scales/zeros [N][K/group]. */
+ * format, FP16 scales/zeros [N][K/group]; ldw is the weight's row stride in
+ * 32-bit words (0 = compact rows of K*bits/32 words; else >= that and a
+ * multiple of 4, e.g. K/8 for an INT2 weight converted in place). */
 typedef struct {
   const uint32_t* W;
   const uint16_t* s;
   const uint16_t* z;
   int N;
   int K;
+  int ldw;
 } tl_qproj;
 
 /*
@@ -301,6 +351,10 @@ typedef struct {
  * normalize = 1 applies the per-row RMS pre-norm h = fp16(x / sqrt(mean x^2 +
  * 1e-5)) before the QKV projection (the block's LayerNorm position, "Model",
  * "VRAM cost", with buf.norm as its FP16 output); 0 feeds fp16(x) directly.
+ * workspace / workspace_bytes: the caller's k-split workspace for the block's
+ * GEMMs with M > 16 (they run one after another and share it; NULL / 0 = no
+ * k split); the largest tl_quant_gemm_workspace_size of the four GEMMs at M
+ * rows is what they can use.  Must not overlap any other buffer.
  */
 typedef struct {
   tl_qproj qkv, o, up, down;
@@ -312,6 +366,8 @@ typedef struct {
   uint16_t* o_out;
   uint16_t* up_out;
   int normalize;
+  void* workspace;
+  size_t workspace_bytes;
 } tl_block;
 
 /*
@@ -325,7 +381,8 @@ typedef struct {
  *   gate_up : N = 2*F, K = D, rows interleaved (see tl_quant_gemm_swiglu)
  *   down    : N = D, K = F
  * Scratch (caller-owned device FP16, at least M rows): h [M][D],
- * qkv_out [M][3D], o_out [M][D], act_out [M][F].  normalize as tl_block.
+ * qkv_out [M][3D], o_out [M][D], act_out [M][F].  normalize and workspace as
+ * tl_block.
  */
 typedef struct {
   tl_qproj qkv, o, gate_up, down;
@@ -337,6 +394,8 @@ typedef struct {
   uint16_t* o_out;
   uint16_t* act_out;
   int normalize;
+  void* workspace;
+  size_t workspace_bytes;
 } tl_swiglu_block;
 
 /*
@@ -392,14 +451,41 @@ tlq_status tl_swiglu_block_forward_chunked(float* x, const tl_swiglu_block* bloc
                                            void* stream);
 
 /*
+ * tl_loop_block_to_int2 / tl_swiglu_block_to_int2 -- the context-length tier
+ * switch of a loop block: its four weights (the SwiGLU block's fused gate/up
+ * weight re-quantizes row by row like the two it holds) are re-quantized
+ * INT4 -> INT2 as tl_requant_int4_to_int2 does, and the HOST block
+ * description is rewritten (bits = 2, each projection's W / s / z / ldw) so
+ * later forwards run the INT2 kernels.
+ *
+ * Source: "beta-Informed Deployment Features", CTX-TIER, "What Phase 2
+ * ships", item 2 (apply_tier_to_model: the loop block's weights re-quantized,
+ * the bit width flipped so the dispatcher routes to int2_gemm) and Phase 2b
+ * (compact INT2 buffers, the INT4 ones released).
+ *   block  HOST pointer; an INT4 block (bits = 4, compact INT4 rows, a group
+ *          that is a multiple of 64).
+ *   dst    HOST array of four destinations (qkv, o, up or gate_up, down), each
+ *          with the weight's N and K: W compact INT2 rows (K/16 words) or the
+ *          INT4 weight itself (in place, ldw = K/8 afterwards); s / z new
+ *          arrays or the INT4 ones (converted in place).  NULL: everything in
+ *          place (no new memory at all).
+ *   Every check happens before the launch; on an error the block is left as
+ *   it was.  Out of place, the INT4 buffers may be freed once `stream` has
+ *   passed the call.  Returns TLQ_OK, TLQ_EINVAL or TLQ_ECUDA.
+ */
+tlq_status tl_loop_block_to_int2(tl_block* block, const tl_qproj* dst, void* stream);
+tlq_status tl_swiglu_block_to_int2(tl_swiglu_block* block, const tl_qproj* dst, void* stream);
+
+/*
  * tl_loop_block_forward_static_scratch -- tl_loop_block_forward for callers
  * that cannot allocate device memory or provide scratch buffers (a serving
  * runtime that forbids allocation after start-up, a plugin interface that only
  * passes a layer its inputs and outputs).  There is no counterpart on the
  * pages: it is a packaging choice of this library.
  *
- * Identical arithmetic to tl_loop_block_forward; block->h, qkv_out, o_out and
- * up_out are ignored (may be NULL).  The four FP16 intermediates live in one
+ * Identical arithmetic to tl_loop_block_forward; block->h, qkv_out, o_out,
+ * up_out and workspace are ignored (may be NULL): the GEMMs run without a k
+ * split.  The four FP16 intermediates live in one
  * 4 MiB static device array inside the library, which every GPU that loads
  * the library holds until the process exits.  The call allocates nothing
  * (no cudaMalloc, cudaFree or allocating library routine).
@@ -407,8 +493,10 @@ tlq_status tl_swiglu_block_forward_chunked(float* x, const tl_swiglu_block* bloc
  *   must fit in 4 MiB -- e.g. M <= 113 at D = 2048, F = 8192 -- otherwise
  *   TLQ_EINVAL with a message that names the sizes, and nothing is launched.
  *   First call on a device: looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.
+ *   device, with that device current) and keeps it for the life of the
+ *   process; make that first call before any stream capture.  A device reset
+ *   (cudaDeviceReset) invalidates the kept address: after one, this entry
+ *   point must not be called again in the same process.
  *   All calls on a device share the one array, which keeps whatever the last
  *   call left in it; every intermediate is fully written before it is read,
  *   so nothing needs clearing.  Calls whose executions overlap on the GPU

@@ -180,7 +180,7 @@ def test_batched_host_rejects_bad_arguments_before_copying(clib):
 
     hA, dA, hC, dC = 1 << 20, 2 << 20, 3 << 20, 4 << 20
     D = tlq._GemmDesc
-    good = D(dA, 5 << 20, 6 << 20, 7 << 20, dC, 1, 64, 256, 4, 128)
+    good = D(dA, 5 << 20, 6 << 20, 7 << 20, dC, 1, 64, 256, 4, 128, 0, None, 0)
 
     def call(descs, n=1, **kw):
         a = dict(hA=hA, dA=dA, ab=4096, hC=hC, dC=dC, cb=4096)
@@ -191,9 +191,86 @@ def test_batched_host_rejects_bad_arguments_before_copying(clib):
     assert call(one, hA=None) == tlq.TLQ_EINVAL
     assert call(one, dC=dA + 64) == tlq.TLQ_EINVAL and "overlap" in tlq.tl_last_error()
     assert call(one, ab=256) == tlq.TLQ_EINVAL and "inside devA" in tlq.tl_last_error()  # A needs 512 bytes
-    bad_bits = (D * 1)(D(dA, 5 << 20, 6 << 20, 7 << 20, dC, 1, 64, 256, 3, 128))
+    bad_bits = (D * 1)(D(dA, 5 << 20, 6 << 20, 7 << 20, dC, 1, 64, 256, 3, 128, 0, None, 0))
     assert call(bad_bits) == tlq.TLQ_EINVAL and "bits" in tlq.tl_last_error()
     assert call(one, n=0) == tlq.TLQ_EINVAL
+
+
+def test_workspace_and_stride_arguments_are_checked(clib):
+    """The k-split workspace and the weight row stride are validated before
+    anything is launched (the addresses are never dereferenced)."""
+    import weight_only_int4_quant_gb300 as tlq
+
+    A, W, S, Z, C, WS = 1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 8 << 20
+
+    def g(ws=WS, nb=1 << 20, **kw):
+        a = dict(A=A, W=W, S=S, Z=Z, C=C, M=128, N=64, K=256, bits=4, group=128)
+        a.update(kw)
+        return clib.tl_quant_gemm_ws(a["A"], a["W"], a["S"], a["Z"], a["C"], a["M"], a["N"], a["K"], a["bits"],
+                                     a["group"], ws, nb, None)
+
+    assert g(ws=WS + 8) == tlq.TLQ_EINVAL and "aligned" in tlq.tl_last_error()
+    assert g(ws=None, nb=64) == tlq.TLQ_EINVAL and "null workspace" in tlq.tl_last_error()
+    assert g(ws=C) == tlq.TLQ_EINVAL and "overlaps" in tlq.tl_last_error()
+    assert g(ws=W - 64) == tlq.TLQ_EINVAL  # runs into the weights
+    assert g(bits=3) == tlq.TLQ_EINVAL
+    # the size query: no split for decode sizes or invalid shapes, a split for
+    # a short-M tensor-core problem that would leave SMs idle
+    assert clib.tl_quant_gemm_workspace_size(16, 2048, 2048, 4, 128) == 0
+    assert clib.tl_quant_gemm_workspace_size(128, 2048, 2048, 3, 128) == 0
+    D = tlq._GemmDesc
+    good = D(A, W, S, Z, C, 1, 64, 256, 4, 128, 0, None, 0)
+    for bad in (D(A, W, S, Z, C, 1, 64, 256, 4, 128, 30, None, 0),     # ldw below the row's 32 words
+                D(A, W, S, Z, C, 1, 64, 256, 4, 128, 34, None, 0),     # not a multiple of 4
+                D(A, W, S, Z, C, 1, 64, 256, 4, 128, 0, WS + 4, 64)):  # misaligned workspace
+        assert clib.tl_quant_gemm_batched((D * 1)(bad), 1, None) == tlq.TLQ_EINVAL
+    # two problems' workspaces may not overlap (they may run at the same time)
+    two = (D * 2)(D(A, W, S, Z, C, 128, 64, 256, 4, 128, 0, WS, 4096),
+                  D(A + 65536, W, S, Z, C + 65536, 128, 64, 256, 4, 128, 0, WS + 1024, 4096))
+    assert clib.tl_quant_gemm_batched(two, 2, None) == tlq.TLQ_EINVAL and "workspace" in tlq.tl_last_error()
+    assert clib.tl_quant_gemm_swiglu_ws(A, W, S, Z, C, 4, 64, 256, 4, 128, WS + 8, 64, None) == tlq.TLQ_EINVAL
+    assert good.ldw == 0
+
+
+def test_tier_switch_rejects_bad_blocks(clib):
+    """tl_loop_block_to_int2 / tl_swiglu_block_to_int2 check everything before
+    their launch and leave the block as it was on an error."""
+    import weight_only_int4_quant_gb300 as tlq
+
+    assert clib.tl_loop_block_to_int2(None, None, None) == tlq.TLQ_EINVAL
+    assert clib.tl_swiglu_block_to_int2(None, None, None) == tlq.TLQ_EINVAL
+    blk = tlq._Block()
+    blk.bits, blk.group, blk.D = 2, 128, 64
+    assert clib.tl_loop_block_to_int2(ctypes.byref(blk), None, None) == tlq.TLQ_EINVAL
+    assert "INT4" in tlq.tl_last_error()
+    base = 1 << 24
+    for i, name in enumerate(("qkv", "o", "up", "down")):
+        N, K = {"qkv": (192, 64), "o": (64, 64), "up": (128, 64), "down": (64, 128)}[name]
+        setattr(blk, name, tlq._QProj(base + i * (1 << 20), base + i * (1 << 20) + (1 << 19),
+                                      base + i * (1 << 20) + (3 << 18), N, K, 0))
+    blk.bits, blk.group = 4, 32  # INT2 groups are multiples of 64
+    assert clib.tl_loop_block_to_int2(ctypes.byref(blk), None, None) == tlq.TLQ_EINVAL
+    assert blk.bits == 4 and blk.qkv.ldw == 0
+    blk.group = 64
+    dst = (tlq._QProj * 4)()
+    for i in range(4):
+        dst[i] = tlq._QProj(base + (8 + i) * (1 << 20), blk.qkv.s, blk.qkv.z, 1, 64, 0)  # wrong N
+    assert clib.tl_loop_block_to_int2(ctypes.byref(blk), dst, None) == tlq.TLQ_EINVAL
+    assert blk.bits == 4
+
+
+def test_library_sources_allocate_nothing():
+    """The library makes no device or host-pinned allocation anywhere: every
+    buffer is the caller's (the allocation-free entry point's static array is
+    a file-scope __device__ variable, not an allocation call)."""
+    csrc = os.path.join(ROOT, "weight_only_int4_quant_gb300", "csrc")
+    banned = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cuMemAlloc\w*|cuMemFree\w*|cudaMemPool\w*|cudaHostAlloc|"
+                        r"cudaMallocHost|cudaMallocManaged|cuMemCreate|cudaMallocAsync)\b")
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name)).read()
+        code = re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))  # calls, not comments
+        hits = banned.findall(code)
+        assert not hits, (name, hits)
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 import synth
-from parity import assert_close, assert_points_close
+from parity import assert_close, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -125,8 +125,8 @@ def test_decode_unit_heights_bitwise(lib, monkeypatch, bits, group, N, K, M):
 
 
 # ---------------------------------------------------------------------------
-# full-size decode configurations (the four D = 2048 projections), sampled
-# outputs against the oracle evaluated point by point
+# full-size decode configurations (the four D = 2048 projections): every
+# output against the oracle
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("bits", [4, 2])
@@ -137,13 +137,9 @@ def test_decode_full_size_sampled(lib, bits, proj, M):
     group = synth.DIST[bits]["group"]
     case = synth.gemm_case(M, N, K, bits, group, seed=0)
     Wd, C = run_case(lib, case)
-    rng = np.random.default_rng(M + N)
-    P = 512
-    pm = rng.integers(0, M, P)
-    pn = rng.integers(0, N, P)
-    ref = oracle.quant_gemm_points(case["A"], Wd.cpu().numpy().view(np.uint32), case["scales"], case["zeros"],
-                                   bits, group, pm, pn)
-    assert_points_close(C[pm, pn], ref, "int%d %s M%d" % (bits, proj, M))
+    # every row (M <= 16) against the oracle, with the per-row bound
+    ref = oracle.quant_gemm(case["A"], Wd.cpu().numpy().view(np.uint32), case["scales"], case["zeros"], bits, group)
+    assert_close(C, ref, "int%d %s M%d" % (bits, proj, M))
 
 
 def test_gemv_config_full_oracle(lib):
@@ -275,15 +271,56 @@ def test_prefill_full_size_sampled(lib, proj, M):
     N, K = synth.SHAPES[proj]
     case = synth.gemm_case(M, N, K, 4, 128, seed=0, a_scale=0.5)
     Wd, C = run_case(lib, case)
-    rng = np.random.default_rng(M * 7 + N)
-    P = 512
-    pm = rng.integers(0, M, P)
-    pn = rng.integers(0, N, P)
-    ref = oracle.quant_gemm_points(case["A"], Wd.cpu().numpy().view(np.uint32), case["scales"], case["zeros"],
-                                   4, 128, pm, pn)
-    assert_points_close(C[pm, pn], ref, "prefill %s M%d" % (proj, M))
+    # 16 whole rows (spread over every 128-token tile position) against the
+    # oracle evaluated on those rows only, with the per-row bound
+    rows = sample_rows(M, 16, np.random.default_rng(M * 7 + N))
+    ref = oracle.quant_gemm(case["A"][rows], Wd.cpu().numpy().view(np.uint32), case["scales"], case["zeros"], 4, 128)
+    assert_close(C[rows], ref, "prefill %s M%d" % (proj, M))
     # every row/column finite and the full output in the range the inputs allow
     assert np.all(np.isfinite(C.astype(np.float32)))
+
+
+# ---------------------------------------------------------------------------
+# the caller-owned k-split workspace
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("proj", ["o", "down"])
+def test_prefill_workspace_is_optional(lib, proj):
+    """M = 128 on a projection whose tiles leave SMs idle: the kernel asks for
+    a k-split workspace.  Without one (tl_quant_gemm), with one too small for
+    its first choice and with the size it asks for, every sampled row matches
+    the oracle (the split changes only the FP32 summation order), a call with
+    the full workspace repeats bit for bit, and nothing is drawn from the
+    device's stream-ordered pool."""
+    from devmem import default_pool_high_watermark
+
+    N, K = synth.SHAPES[proj]
+    M = 128
+    case = synth.gemm_case(M, N, K, 4, 128, seed=17, a_scale=0.5)
+    need = lib.tl_quant_gemm_workspace_size(M, N, K, 4, 128)
+    assert need > 0
+    Wd = gpu_pack(lib, case["codes"], 4)
+    A, s, z = dev(case["A"]), dev(case["scales"]), dev(case["zeros"])
+    rows = sample_rows(M, 16, np.random.default_rng(3))
+    ref = oracle.quant_gemm(case["A"][rows], Wd.cpu().numpy().view(np.uint32), case["scales"], case["zeros"], 4, 128)
+    outs = {}
+    for label, nbytes in (("none", 0), ("small", need // 2 - 16), ("full", need)):
+        C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+        torch.cuda.synchronize()
+        default_pool_high_watermark(reset=True)
+        if ws is None:
+            lib.tl_quant_gemm(A, Wd, s, z, C, 4, 128)
+        else:
+            lib.tl_quant_gemm_ws(A, Wd, s, z, C, 4, 128, ws)
+        torch.cuda.synchronize()
+        assert default_pool_high_watermark() == 0, label
+        lib.tl_check_status()
+        outs[label] = C
+        assert_close(C.cpu().numpy()[rows], ref, "%s workspace %s" % (proj, label))
+    C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    lib.tl_quant_gemm_ws(A, Wd, s, z, C, 4, 128, torch.empty(need, dtype=torch.uint8, device="cuda"))
+    assert torch.equal(C.view(torch.int16), outs["full"].view(torch.int16))
 
 
 # ---------------------------------------------------------------------------
@@ -312,11 +349,11 @@ def test_batched_equals_separate_calls_bitwise(lib):
     # and a sample against the oracle
     rng = np.random.default_rng(5)
     for p, (M, N, K, bits, group) in zip(probs, specs):
-        pm, pn = rng.integers(0, M, 64), rng.integers(0, N, 64)
+        rows = sample_rows(M, 4, rng)
         c = p["case"]
-        ref = oracle.quant_gemm_points(c["A"], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
-                                       group, pm, pn)
-        assert_points_close(p["C"].cpu().numpy()[pm, pn], ref, "batched M%d N%d K%d" % (M, N, K))
+        ref = oracle.quant_gemm(c["A"][rows], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
+                                group)
+        assert_close(p["C"].cpu().numpy()[rows], ref, "batched M%d N%d K%d" % (M, N, K))
 
 
 def test_batched_prefill_side_streams_in_a_graph(lib):
@@ -328,7 +365,10 @@ def test_batched_prefill_side_streams_in_a_graph(lib):
     specs = [(128, 512, 1024, 4, 128), (200, 256, 2048, 4, 128), (256, 768, 512, 4, 128), (130, 1024, 1024, 4, 128),
              (5, 512, 1024, 4, 128)]
     probs = _problems(specs, seed=40)
-    descs = lib.gemm_descs([(p["A"], p["W"], p["s"], p["z"], p["C"], 4, 128) for p in probs])
+    for p, (M, N, K, bits, group) in zip(probs, specs):  # each prefill problem its own k-split workspace
+        p["ws"] = lib.gemm_workspace(M, N, K, bits, group)
+    assert any(p["ws"] is not None for p in probs)
+    descs = lib.gemm_descs([(p["A"], p["W"], p["s"], p["z"], p["C"], 4, 128, p["ws"]) for p in probs])
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -350,11 +390,11 @@ def test_batched_prefill_side_streams_in_a_graph(lib):
             assert torch.equal(p["C"].view(torch.int16), d.view(torch.int16))
     rng = np.random.default_rng(9)
     for p, (M, N, K, bits, group) in zip(probs, specs):
-        pm, pn = rng.integers(0, M, 64), rng.integers(0, N, 64)
+        rows = sample_rows(M, 8, rng)
         c = p["case"]
-        ref = oracle.quant_gemm_points(c["A"], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
-                                       group, pm, pn)
-        assert_points_close(p["C"].cpu().numpy()[pm, pn], ref, "side streams M%d N%d K%d" % (M, N, K))
+        ref = oracle.quant_gemm(c["A"][rows], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
+                                group)
+        assert_close(p["C"].cpu().numpy()[rows], ref, "side streams M%d N%d K%d" % (M, N, K))
 
 
 def test_batched_mixed_bits_and_paths(lib):

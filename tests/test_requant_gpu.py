@@ -223,8 +223,97 @@ def test_requant_argument_errors(lib):
     W2 = torch.zeros((8, 16), dtype=torch.int32, device="cuda")
     with pytest.raises(lib.TLQError):
         lib.tl_requant_int4_to_int2(W4, s, s.clone(), W2, s.clone(), s.clone(), 96)  # not a multiple of 64
-    with pytest.raises(lib.TLQError):  # W2 inside W4
-        lib.tl_requant_int4_to_int2(W4, s, s.clone(), W4.view(-1)[:128].view(8, 16), s.clone(), s.clone(), 128)
+    with pytest.raises(lib.TLQError):  # W2 inside W4 without being it (W2 == W4 is the in-place mode)
+        lib.tl_requant_int4_to_int2(W4, s, s.clone(), W4.view(-1)[4:132].view(8, 16), s.clone(), s.clone(), 128)
     zs = s.clone()
     with pytest.raises(lib.TLQError):  # s2 overlapping z4 without being it
         lib.tl_requant_int4_to_int2(W4, s, zs, W2, zs, s.clone(), 128)
+
+
+# ---------------------------------------------------------------------------
+# in place ("Details of the shipped kernel", storage reuse): W2 == W4, the
+# INT2 rows keep the INT4 row stride of K/8 words
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,group", [(64, 256, 128), (37, 512, 64), (16, 768, 192), (5, 2048, 1024),
+                                       (3, 4096, 4096), (300, 8192, 128)])
+@pytest.mark.parametrize("kind", ["workload", "signed", "degenerate"])
+def test_requant_in_place_bit_exact(lib, N, K, group, kind):
+    """Through a strided view: the first K/16 words of every INT4-stride row
+    are the oracle's compact INT2 row bit for bit, the rest of the row is the
+    INT4 words it held, and the scales/zeros (converted in place) match."""
+    rng = np.random.default_rng(N + K + group + len(kind))
+    codes, s4, z4 = weights(rng, N, K, group, kind)
+    W4 = oracle.pack(codes, 4)
+    with np.errstate(over="ignore"):
+        rW, rs, rz = oracle.requant_int4_to_int2(W4, s4, z4, K, group)
+    Wd, sd, zd = dev(W4.view(np.int32)), dev(s4), dev(z4)
+    lib.tl_requant_int4_to_int2(Wd, sd, zd, Wd, sd, zd, group)
+    torch.cuda.synchronize()
+    got = Wd.cpu().numpy().view(np.uint32)
+    assert np.array_equal(got[:, :K // 16], rW), "%s: %d words differ" % (kind, np.count_nonzero(got[:, :K // 16] != rW))
+    assert np.array_equal(got[:, K // 16:], W4[:, K // 16:])
+    assert np.array_equal(sd.cpu().numpy().view(np.uint16), rs.view(np.uint16))
+    assert np.array_equal(zd.cpu().numpy().view(np.uint16), rz.view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [1, 16, 256])
+def test_int2_gemm_on_in_place_weights(lib, M):
+    """The INT2 GEMM reads an in-place converted weight with its INT4 row
+    stride (ldw = K/8): same bits as on a compact copy, and the oracle's GEMM
+    on the oracle's re-quantization within the GEMM bar."""
+    N, K, group = 1024, 2048, 128
+    rng = synth.rng_for(300 + M)
+    A = synth.activations(rng, M, K, 0.5 if M > 16 else 1.0)
+    codes, s4, z4 = synth.quant_weights(rng, N, K, 4, group)
+    W4 = oracle.pack(codes, 4)
+    W2r, s2r, z2r = oracle.requant_int4_to_int2(W4, s4, z4, K, group)
+    Wd, sd, zd = dev(W4.view(np.int32)), dev(s4), dev(z4)
+    lib.tl_requant_int4_to_int2(Wd, sd, zd, Wd, sd, zd, group)
+    Ad = dev(A)
+    C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    C2 = torch.empty_like(C)
+    ws = lib.gemm_workspace(M, N, K, 2, group)
+    compact = Wd[:, :K // 16].contiguous()
+    lib.tl_quant_gemm_batched([(Ad, Wd, sd, zd, C, 2, group, ws, K // 8)])
+    lib.tl_quant_gemm_batched([(Ad, compact, sd, zd, C2, 2, group, ws, 0)])
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+    assert_close(C.cpu().numpy(), oracle.quant_gemm(A, W2r, s2r, z2r, 2, group), "in-place int2 M%d" % M)
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_loop_block_tier_switch_through_c_abi(lib, in_place):
+    """tl_loop_block_to_int2 (LoopBlock.to_int2): out of place the weights
+    move to new compact buffers, in place they stay where they were with
+    ldw = K/8; either way the switched block runs bit for bit like an INT2
+    block built from the oracle's re-quantized weights."""
+    case = synth.block_case(16, 4, seed=78, D=512, F=1024)
+    proj, host2 = {}, {}
+    for name, (codes, s, z) in case["proj"].items():
+        W4 = oracle.pack(codes, 4)
+        proj[name] = (dev(W4.view(np.int32)), dev(s), dev(z))
+        N, K = codes.shape
+        host2[name] = oracle.requant_int4_to_int2(W4, s, z, K, case["group"])
+    blk = lib.LoopBlock(proj, 4, case["group"], 16)
+    before = {name: proj[name][0].data_ptr() for name in proj}
+    blk.to_int2(in_place=in_place)
+    assert blk.bits == 2 and blk._c.bits == 2
+    for name in host2:
+        N, K = blk.dims[name]
+        moved = blk.proj[name][0].data_ptr() != before[name]
+        assert moved != in_place
+        assert blk.ldw[name] == (K // 8 if in_place else 0) == getattr(blk._c, name).ldw
+        words = blk.proj[name][0].cpu().numpy().view(np.uint32)[:, :K // 16]
+        assert np.array_equal(words, host2[name][0]), name
+    ref_blk = lib.LoopBlock({name: tuple(dev(a.view(np.int32) if a.dtype == np.uint32 else a) for a in host2[name])
+                             for name in host2}, 2, case["group"], 16)
+    for M in (1, 16):
+        x = dev(case["x0"][:M].copy())
+        y = x.clone()
+        blk.forward(x, 3)
+        ref_blk.forward(y, 3)
+        torch.cuda.synchronize()
+        lib.tl_check_status()
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32)), "M%d" % M

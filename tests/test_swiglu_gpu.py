@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import synth
-from parity import assert_close, assert_points_close
+from parity import assert_close, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -104,17 +104,16 @@ def test_swiglu_gemm_k_splits_and_token_tiles(lib, monkeypatch, bits, ks, nmt):
 @pytest.mark.parametrize("M", [1, 16, 128])
 def test_swiglu_gemm_full_size_sampled(lib, M):
     """D = 2048, F = 8192 (the gate/up pair of the pages' block), INT4 group
-    128: 512 sampled outputs against the oracle's points."""
+    128: whole rows (all of them up to M = 16, 16 sampled at M = 128) against
+    the oracle, with the per-row bound."""
     F, K, bits, group = synth.FFN, synth.D_MODEL, 4, 128
     A, gate, up = gate_up_case(M, F, K, bits, group, seed=900 + M)
     W, s, z = gpu_gate_up(lib, gate, up, bits)
     C = lib.quant_gemm_swiglu(dev(A), W, s, z, bits, group).cpu().numpy()
-    rng = np.random.default_rng(M)
-    pm = rng.integers(0, M, 512)
-    pn = rng.integers(0, F, 512)
-    g = oracle.quant_gemm_points(A, oracle.pack(gate[0], bits), gate[1], gate[2], bits, group, pm, pn)
-    u = oracle.quant_gemm_points(A, oracle.pack(up[0], bits), up[1], up[2], bits, group, pm, pn)
-    assert_points_close(C[pm, pn], oracle.swiglu(g, u), "full-size swiglu M%d" % M)
+    rows = sample_rows(M, 16, np.random.default_rng(M))
+    g = oracle.quant_gemm(A[rows], oracle.pack(gate[0], bits), gate[1], gate[2], bits, group)
+    u = oracle.quant_gemm(A[rows], oracle.pack(up[0], bits), up[1], up[2], bits, group)
+    assert_close(C[rows], oracle.swiglu(g, u), "full-size swiglu M%d" % M)
 
 
 def test_swiglu_gemm_rejects_bad_shapes(lib):
@@ -187,14 +186,16 @@ def test_swiglu_block_split_invariant_and_deterministic(lib):
     assert np.array_equal(full.view(np.uint32), rest.view(np.uint32))
 
 
-def test_swiglu_block_tier_switch(lib):
-    """SwiGLUBlock.to_int2: all five weights re-quantized in one launch (the
+@pytest.mark.parametrize("in_place", [False, True])
+def test_swiglu_block_tier_switch(lib, in_place):
+    """SwiGLUBlock.to_int2 (tl_swiglu_block_to_int2, out of place or in place
+    with the INT4 row stride kept): all five weights re-quantized in one launch (the
     fused gate/up weight row by row); the switched block equals an INT2
     block built from the oracle's re-quantized weights bit for bit, and one
     iteration matches the oracle's INT2 block."""
     case = synth.swiglu_block_case(16, 4, seed=8, D=512, F=1024)
     blk, host = make_block(lib, case, max_rows=16)
-    blk.to_int2()
+    blk.to_int2(in_place=in_place)
     assert blk.bits == 2
     host2, proj2 = {}, {}
     for name, (W4, s, z) in host.items():

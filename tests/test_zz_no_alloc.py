@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 
 import synth
+from devmem import default_pool_high_watermark
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -37,8 +38,13 @@ def test_static_scratch_matches_caller_scratch(lib, bits, M, D, F, L):
     ref = x_ref.cpu().numpy()
     for call in range(2):  # two calls in a row share (and reuse) the static array
         x = torch.from_numpy(case["x0"].copy()).cuda()
+        torch.cuda.synchronize()
+        default_pool_high_watermark(reset=True)
         lib.tl_loop_block_forward_static_scratch(x, blk, L)
         torch.cuda.synchronize()
+        # nothing came from the device's stream-ordered pool (the library's
+        # sources hold no allocation call at all: tests/test_abi.py)
+        assert default_pool_high_watermark() == 0
         lib.tl_check_status()
         assert_close(x.cpu().numpy(), ref, "static scratch call %d int%d M%d" % (call, bits, M))
 

@@ -23,6 +23,8 @@ __all__ = [
     "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward", "quant_gemm_swiglu",
     "interleave_rows", "SwiGLUBlock", "tl_dequant_fp16", "dequant_fp16",
     "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked", "tl_quant_gemm_batched_host",
+    "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws", "tl_loop_block_to_int2",
+    "tl_swiglu_block_to_int2", "gemm_workspace", "requant_descs",
 ]
 
 # every symbol include/tlq.h declares
@@ -32,7 +34,8 @@ EXPORTED = (
     "tl_loop_block_forward_static_scratch", "tl_quant_gemm_batched", "tl_requant_int4_to_int2",
     "tl_requant_int4_to_int2_batched", "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward",
     "tl_dequant_fp16", "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
-    "tl_quant_gemm_batched_host",
+    "tl_quant_gemm_batched_host", "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws",
+    "tl_loop_block_to_int2", "tl_swiglu_block_to_int2",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -47,13 +50,14 @@ class TLQError(RuntimeError):
 
 class _QProj(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("s", ctypes.c_void_p), ("z", ctypes.c_void_p),
-                ("N", ctypes.c_int), ("K", ctypes.c_int)]
+                ("N", ctypes.c_int), ("K", ctypes.c_int), ("ldw", ctypes.c_int)]
 
 
 class _GemmDesc(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("Wpacked", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("zeros", ctypes.c_void_p), ("C", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
-                ("K", ctypes.c_int), ("bits", ctypes.c_int), ("group", ctypes.c_int)]
+                ("K", ctypes.c_int), ("bits", ctypes.c_int), ("group", ctypes.c_int), ("ldw", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class _RequantDesc(ctypes.Structure):
@@ -65,14 +69,16 @@ class _Block(ctypes.Structure):
     _fields_ = [("qkv", _QProj), ("o", _QProj), ("up", _QProj), ("down", _QProj),
                 ("bits", ctypes.c_int), ("group", ctypes.c_int), ("D", ctypes.c_int),
                 ("h", ctypes.c_void_p), ("qkv_out", ctypes.c_void_p), ("o_out", ctypes.c_void_p),
-                ("up_out", ctypes.c_void_p), ("normalize", ctypes.c_int)]
+                ("up_out", ctypes.c_void_p), ("normalize", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class _SwigluBlock(ctypes.Structure):
     _fields_ = [("qkv", _QProj), ("o", _QProj), ("gate_up", _QProj), ("down", _QProj),
                 ("bits", ctypes.c_int), ("group", ctypes.c_int), ("D", ctypes.c_int),
                 ("h", ctypes.c_void_p), ("qkv_out", ctypes.c_void_p), ("o_out", ctypes.c_void_p),
-                ("act_out", ctypes.c_void_p), ("normalize", ctypes.c_int)]
+                ("act_out", ctypes.c_void_p), ("normalize", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 _lock = threading.Lock()
@@ -121,6 +127,11 @@ def load():
             "tl_loop_block_forward_chunked": ([P, ctypes.POINTER(_Block), I, I, I, P], I),
             "tl_swiglu_block_forward_chunked": ([P, ctypes.POINTER(_SwigluBlock), I, I, I, P], I),
             "tl_swiglu_block_forward": ([P, ctypes.POINTER(_SwigluBlock), I, I, P], I),
+            "tl_quant_gemm_workspace_size": ([I, I, I, I, I], ctypes.c_size_t),
+            "tl_quant_gemm_ws": ([P, P, P, P, P, I, I, I, I, I, P, ctypes.c_size_t, P], I),
+            "tl_quant_gemm_swiglu_ws": ([P, P, P, P, P, I, I, I, I, I, P, ctypes.c_size_t, P], I),
+            "tl_loop_block_to_int2": ([ctypes.POINTER(_Block), ctypes.POINTER(_QProj), P], I),
+            "tl_swiglu_block_to_int2": ([ctypes.POINTER(_SwigluBlock), ctypes.POINTER(_QProj), P], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -177,18 +188,53 @@ def tl_quant_gemm(A, W, scales, zeros, C, bits: int, group: int, stream=None) ->
     _raise_if(st)
 
 
+def tl_quant_gemm_workspace_size(M: int, N: int, K: int, bits: int, group: int) -> int:
+    """Bytes of k-split workspace the tensor-core kernel would use (0: none)."""
+    return int(load().tl_quant_gemm_workspace_size(M, N, K, bits, group))
+
+
+def gemm_workspace(M: int, N: int, K: int, bits: int, group: int, device="cuda"):
+    """A caller-owned workspace tensor for one problem (None when the kernel
+    would not split K); torch allocates it, the library never does."""
+    import torch
+
+    n = tl_quant_gemm_workspace_size(M, N, K, bits, group)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def tl_quant_gemm_ws(A, W, scales, zeros, C, bits: int, group: int, workspace=None, stream=None) -> None:
+    """tl_quant_gemm with a caller-owned k-split workspace (uint8 CUDA tensor or None)."""
+    import torch
+
+    M, K = A.shape
+    N = W.shape[0]
+    ws = _dev(workspace, (torch.uint8,), "workspace") if workspace is not None else None
+    nb = workspace.numel() if workspace is not None else 0
+    st = load().tl_quant_gemm_ws(_dev(A, (torch.float16,), "A"), _dev(W, (torch.int32, torch.uint32), "W"),
+                                 _dev(scales, (torch.float16,), "scales"), _dev(zeros, (torch.float16,), "zeros"),
+                                 _dev(C, (torch.float16,), "C"), M, N, K, bits, group, ws, nb, _stream(stream))
+    _raise_if(st)
+
+
 def gemm_descs(problems):
     """ctypes descriptor array for tl_quant_gemm_batched from
-    (A, W, scales, zeros, C, bits, group) tuples of CUDA tensors; build it
-    once and reuse it to keep per-call host work small."""
+    (A, W, scales, zeros, C, bits, group[, workspace[, ldw]]) tuples of CUDA
+    tensors (workspace: a uint8 tensor or None; ldw: the weight's row stride
+    in words, 0 = compact); build it once and reuse it to keep per-call host
+    work small (the tuples' tensors must stay alive as long as it is used)."""
     import torch
 
     arr = (_GemmDesc * len(problems))()
-    for i, (A, W, s, z, C, bits, group) in enumerate(problems):
+    for i, prob in enumerate(problems):
+        A, W, s, z, C, bits, group = prob[:7]
+        ws = prob[7] if len(prob) > 7 else None
+        ldw = prob[8] if len(prob) > 8 else 0
         M, K = A.shape
         arr[i] = _GemmDesc(_dev(A, (torch.float16,), "A"), _dev(W, (torch.int32, torch.uint32), "W"),
                            _dev(s, (torch.float16,), "scales"), _dev(z, (torch.float16,), "zeros"),
-                           _dev(C, (torch.float16,), "C"), M, W.shape[0], K, bits, group)
+                           _dev(C, (torch.float16,), "C"), M, W.shape[0], K, bits, group, ldw,
+                           _dev(ws, (torch.uint8,), "workspace") if ws is not None else None,
+                           ws.numel() if ws is not None else 0)
     return arr
 
 
@@ -252,17 +298,23 @@ def tl_requant_int4_to_int2(W4, s4, z4, W2, s2, z2, group: int, stream=None) -> 
                                              N, K, group, _stream(stream)))
 
 
-def tl_quant_gemm_swiglu(A, Wgu, scales, zeros, C, bits: int, group: int, stream=None) -> None:
+def tl_quant_gemm_swiglu(A, Wgu, scales, zeros, C, bits: int, group: int, stream=None, workspace=None) -> None:
+    """The fused gate/up GEMM with the SwiGLU epilogue; with a workspace
+    (uint8 CUDA tensor) through tl_quant_gemm_swiglu_ws."""
     import torch
 
     M, K = A.shape
     N2 = Wgu.shape[0]
     if tuple(C.shape) != (M, N2 // 2):
         raise ValueError("C must be [M, N2/2] = [%d, %d]" % (M, N2 // 2))
-    _raise_if(load().tl_quant_gemm_swiglu(_dev(A, (torch.float16,), "A"), _dev(Wgu, (torch.int32, torch.uint32), "Wgu"),
-                                          _dev(scales, (torch.float16,), "scales"),
-                                          _dev(zeros, (torch.float16,), "zeros"), _dev(C, (torch.float16,), "C"),
-                                          M, N2, K, bits, group, _stream(stream)))
+    args = (_dev(A, (torch.float16,), "A"), _dev(Wgu, (torch.int32, torch.uint32), "Wgu"),
+            _dev(scales, (torch.float16,), "scales"), _dev(zeros, (torch.float16,), "zeros"),
+            _dev(C, (torch.float16,), "C"), M, N2, K, bits, group)
+    if workspace is None:
+        _raise_if(load().tl_quant_gemm_swiglu(*args, _stream(stream)))
+    else:
+        _raise_if(load().tl_quant_gemm_swiglu_ws(*args, _dev(workspace, (torch.uint8,), "workspace"),
+                                                 workspace.numel(), _stream(stream)))
 
 
 def tl_dequant_fp16(W, scales, zeros, out, bits: int, group: int, stream=None) -> None:
@@ -376,10 +428,14 @@ def tl_selftest_wait_timeout(limit_us: int, stream=None) -> None:
 # ---------------------------------------------------------------------------
 
 def quant_gemm(A, W, scales, zeros, bits: int, group: int, stream=None):
+    """C = A . dequant(W)^T, with the k-split workspace the kernel asks for
+    (allocated here by torch)."""
     import torch
 
     C = torch.empty((A.shape[0], W.shape[0]), dtype=torch.float16, device=A.device)
-    tl_quant_gemm(A, W, scales, zeros, C, bits, group, stream)
+    K = A.shape[1]
+    ws = gemm_workspace(A.shape[0], W.shape[0], K, bits, group, A.device)
+    tl_quant_gemm_ws(A, W, scales, zeros, C, bits, group, ws, stream)
     return C
 
 
@@ -396,7 +452,8 @@ def quant_gemm_swiglu(A, Wgu, scales, zeros, bits: int, group: int, stream=None)
     import torch
 
     C = torch.empty((A.shape[0], Wgu.shape[0] // 2), dtype=torch.float16, device=A.device)
-    tl_quant_gemm_swiglu(A, Wgu, scales, zeros, C, bits, group, stream)
+    ws = gemm_workspace(A.shape[0], Wgu.shape[0], A.shape[1], bits, group, A.device)
+    tl_quant_gemm_swiglu(A, Wgu, scales, zeros, C, bits, group, stream, ws)
     return C
 
 
@@ -427,73 +484,130 @@ def unpack_weights(W, K: int, bits: int, stream=None):
     return codes
 
 
-class LoopBlock:
-    """The shared-weight loop block: four packed projections plus FP16 scratch.
+def _block_workspace(shapes, bits, group, max_rows, device):
+    """One workspace for a block's GEMMs (they run in order): the largest any
+    of them asks for at any row count up to max_rows (the planner's choice
+    changes only at multiples of the 128-token tile)."""
+    import torch
 
-    ``proj`` maps "qkv", "o", "up", "down" to (W packed int32, scales, zeros)
-    CUDA tensors; scratch for up to ``max_rows`` rows is allocated here."""
+    ms = sorted({max_rows} | set(range(128, max_rows + 1, 128)) | ({17} if max_rows > 16 else set()))
+    need = 0
+    for M in ms:
+        for (N, K) in shapes:
+            need = max(need, tl_quant_gemm_workspace_size(M, N, K, bits, group))
+    return torch.empty(need, dtype=torch.uint8, device=device) if need else None
 
-    def __init__(self, proj: dict, bits: int, group: int, max_rows: int, normalize: bool = True):
+
+def _sync(stream):
+    import torch
+
+    if stream is None:
+        torch.cuda.current_stream().synchronize()
+    elif isinstance(stream, int):
+        torch.cuda.synchronize()
+    else:
+        stream.synchronize()
+
+
+class _BlockBase:
+    """Shared parts of the two loop blocks: projection descriptions, the
+    FP16 scratch and the k-split workspace (all allocated here by torch)."""
+
+    NAMES = ()
+    STRUCT = None
+    ACT = ""
+
+    def _setup(self, proj, bits, group, max_rows, normalize, F_act):
         import torch
 
         self.proj = proj
-        self.bits, self.group, self.max_rows = bits, group, max_rows
+        self.bits, self.group, self.max_rows, self.normalize = bits, group, max_rows, normalize
         cpw = 32 // bits
-        dims = {k: (v[0].shape[0], v[0].shape[1] * cpw) for k, v in proj.items()}
-        D = dims["o"][0]
-        F = dims["up"][0]
-        self.D, self.F = D, F
+        self.dims = {k: (v[0].shape[0], v[0].shape[1] * cpw) for k, v in proj.items()}
+        self.ldw = {k: 0 for k in proj}
+        D = self.dims["o"][0]
+        self.D, self.F = D, F_act
         dev = proj["o"][0].device
         self.h = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
         self.qkv_out = torch.empty((max_rows, 3 * D), dtype=torch.float16, device=dev)
         self.o_out = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
-        self.up_out = torch.empty((max_rows, F), dtype=torch.float16, device=dev)
-        self.normalize = normalize
+        self.act = torch.empty((max_rows, F_act), dtype=torch.float16, device=dev)
+        self.workspace = _block_workspace(list(self.dims.values()), bits, group, max_rows, dev)
         self._bind()
 
     def _bind(self):
         import torch
 
-        cpw = 32 // self.bits
-        c = _Block()
-        for name in ("qkv", "o", "up", "down"):
+        c = self.STRUCT()
+        for name in self.NAMES:
             W, s, z = self.proj[name]
+            N, K = self.dims[name]
             setattr(c, name, _QProj(_dev(W, (torch.int32, torch.uint32), name + ".W"),
                                     _dev(s, (torch.float16,), name + ".s"), _dev(z, (torch.float16,), name + ".z"),
-                                    W.shape[0], W.shape[1] * cpw))
+                                    N, K, self.ldw[name]))
         c.bits, c.group, c.D = self.bits, self.group, self.D
-        c.h, c.qkv_out, c.o_out, c.up_out = (self.h.data_ptr(), self.qkv_out.data_ptr(), self.o_out.data_ptr(),
-                                             self.up_out.data_ptr())
+        c.h, c.qkv_out, c.o_out = self.h.data_ptr(), self.qkv_out.data_ptr(), self.o_out.data_ptr()
+        setattr(c, self.ACT, self.act.data_ptr())
         c.normalize = 1 if self.normalize else 0
+        c.workspace = self.workspace.data_ptr() if self.workspace is not None else None
+        c.workspace_bytes = self.workspace.numel() if self.workspace is not None else 0
         self._c = c
 
-    def to_int2(self, stream=None):
-        """The context-length tier switch ("beta-Informed Deployment
-        Features", CTX-TIER, Phase 2 / 2b): re-quantize every INT4 projection
-        to compact INT2 (scales / zeros converted in place), wait for the
-        stream, release the INT4 weights and route later forwards to the INT2
-        kernel.  One way; the group size is kept."""
+    def _to_int2(self, fn, in_place, stream):
+        """The context-length tier switch through the C ABI ("beta-Informed
+        Deployment Features", CTX-TIER, Phase 2 / 2b): one launch re-quantizes
+        every INT4 weight, the library rewrites the block description to INT2.
+        Out of place (default) the INT2 rows are compact new buffers and the
+        INT4 words are released once the stream has passed the conversion;
+        in place the INT2 rows overwrite the INT4 words at the INT4 row stride.
+        Scales and zeros are converted in place either way.  One way; the
+        group size is kept."""
         import torch
 
         if self.bits != 4:
             raise ValueError("to_int2 needs an INT4 block (bits=%d)" % self.bits)
-        new, probs = {}, []
-        for name in ("qkv", "o", "up", "down"):
-            W4, s4, z4 = self.proj[name]
-            W2 = torch.empty((W4.shape[0], W4.shape[1] // 2), dtype=torch.int32, device=W4.device)
-            new[name] = (W2, s4, z4)
-            probs.append((W4, s4, z4, W2, s4, z4))
-        tl_requant_int4_to_int2_batched(probs, self.group, stream)  # one launch for the block
-        if stream is None:
-            torch.cuda.current_stream().synchronize()
-        elif isinstance(stream, int):
-            torch.cuda.synchronize()
-        else:
-            stream.synchronize()
-        self.proj = new  # the INT4 words go back to the allocator with their last reference
+        new = {}
+        dst = None
+        if not in_place:
+            dst = (_QProj * 4)()
+            for i, name in enumerate(self.NAMES):
+                W4, s4, z4 = self.proj[name]
+                N, K = self.dims[name]
+                W2 = torch.empty((N, K // 16), dtype=torch.int32, device=W4.device)
+                new[name] = (W2, s4, z4)
+                dst[i] = _QProj(W2.data_ptr(), s4.data_ptr(), z4.data_ptr(), N, K, 0)
+        _raise_if(fn(ctypes.byref(self._c), dst, _stream(stream)))
+        _sync(stream)  # the INT4 words may go back to the allocator now
+        for name in self.NAMES:
+            self.ldw[name] = getattr(self._c, name).ldw
+        if not in_place:
+            self.proj = new
         self.bits = 2
         self._bind()
         return self
+
+
+class LoopBlock(_BlockBase):
+    """The shared-weight loop block: four packed projections plus FP16 scratch
+    and the k-split workspace.
+
+    ``proj`` maps "qkv", "o", "up", "down" to (W packed int32, scales, zeros)
+    CUDA tensors; scratch for up to ``max_rows`` rows is allocated here."""
+
+    NAMES = ("qkv", "o", "up", "down")
+    STRUCT = _Block
+    ACT = "up_out"
+
+    def __init__(self, proj: dict, bits: int, group: int, max_rows: int, normalize: bool = True):
+        self._setup(proj, bits, group, max_rows, normalize, proj["up"][0].shape[0])
+
+    @property
+    def up_out(self):
+        return self.act
+
+    def to_int2(self, stream=None, in_place: bool = False):
+        """The tier switch (tl_loop_block_to_int2)."""
+        return self._to_int2(load().tl_loop_block_to_int2, in_place, stream)
 
     def forward(self, x, L: int, stream=None, chunk: int = 0):
         """L iterations on x in place; chunk > 0 runs chunked prefill."""
@@ -504,7 +618,7 @@ class LoopBlock:
         return x
 
 
-class SwiGLUBlock:
+class SwiGLUBlock(_BlockBase):
     """The five-weight SwiGLU loop block (attn_qkv, attn_out, mlp_gate,
     mlp_up, mlp_down).
 
@@ -513,39 +627,24 @@ class SwiGLUBlock:
     by row into one [2F, ...] weight for the fused GEMM (tl_interleave_rows);
     scratch for up to ``max_rows`` rows is allocated here."""
 
-    def __init__(self, proj: dict, bits: int, group: int, max_rows: int, normalize: bool = True, stream=None):
-        import torch
+    NAMES = ("qkv", "o", "gate_up", "down")
+    STRUCT = _SwigluBlock
+    ACT = "act_out"
 
-        self.bits, self.group, self.max_rows, self.normalize = bits, group, max_rows, normalize
+    def __init__(self, proj: dict, bits: int, group: int, max_rows: int, normalize: bool = True, stream=None):
         gate, up = proj["gate"], proj["up"]
         gate_up = tuple(interleave_rows(g, u, stream) for g, u in zip(gate, up))
-        self.proj = {"qkv": proj["qkv"], "o": proj["o"], "gate_up": gate_up, "down": proj["down"]}
-        cpw = 32 // bits
-        D = proj["o"][0].shape[0]
-        F = gate[0].shape[0]
-        self.D, self.F = D, F
-        dev = proj["o"][0].device
-        self.h = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
-        self.qkv_out = torch.empty((max_rows, 3 * D), dtype=torch.float16, device=dev)
-        self.o_out = torch.empty((max_rows, D), dtype=torch.float16, device=dev)
-        self.act_out = torch.empty((max_rows, F), dtype=torch.float16, device=dev)
-        self._bind()
+        fused = {"qkv": proj["qkv"], "o": proj["o"], "gate_up": gate_up, "down": proj["down"]}
+        self._setup(fused, bits, group, max_rows, normalize, gate[0].shape[0])
 
-    def _bind(self):
-        import torch
+    @property
+    def act_out(self):
+        return self.act
 
-        cpw = 32 // self.bits
-        c = _SwigluBlock()
-        for name in ("qkv", "o", "gate_up", "down"):
-            W, s, z = self.proj[name]
-            setattr(c, name, _QProj(_dev(W, (torch.int32, torch.uint32), name + ".W"),
-                                    _dev(s, (torch.float16,), name + ".s"), _dev(z, (torch.float16,), name + ".z"),
-                                    W.shape[0], W.shape[1] * cpw))
-        c.bits, c.group, c.D = self.bits, self.group, self.D
-        c.h, c.qkv_out, c.o_out, c.act_out = (self.h.data_ptr(), self.qkv_out.data_ptr(), self.o_out.data_ptr(),
-                                              self.act_out.data_ptr())
-        c.normalize = 1 if self.normalize else 0
-        self._c = c
+    def to_int2(self, stream=None, in_place: bool = False):
+        """The tier switch for the five weights (tl_swiglu_block_to_int2; the
+        fused gate/up weight re-quantizes row by row like the two it holds)."""
+        return self._to_int2(load().tl_swiglu_block_to_int2, in_place, stream)
 
     def forward(self, x, L: int, stream=None, chunk: int = 0):
         """L iterations on x in place; chunk > 0 runs chunked prefill."""
@@ -560,30 +659,3 @@ class SwiGLUBlock:
         _raise_if(load().tl_swiglu_block_forward(_dev(x, (torch.float32,), "x"), ctypes.byref(self._c), L, M,
                                                  _stream(stream)))
         return x
-
-    def to_int2(self, stream=None):
-        """The context-length tier switch for the five weights (the fused
-        gate/up weight re-quantizes row by row like the two it holds): one
-        launch, scales / zeros in place, INT4 words released after the
-        stream has passed the conversion."""
-        import torch
-
-        if self.bits != 4:
-            raise ValueError("to_int2 needs an INT4 block (bits=%d)" % self.bits)
-        new, probs = {}, []
-        for name in ("qkv", "o", "gate_up", "down"):
-            W4, s4, z4 = self.proj[name]
-            W2 = torch.empty((W4.shape[0], W4.shape[1] // 2), dtype=torch.int32, device=W4.device)
-            new[name] = (W2, s4, z4)
-            probs.append((W4, s4, z4, W2, s4, z4))
-        tl_requant_int4_to_int2_batched(probs, self.group, stream)
-        if stream is None:
-            torch.cuda.current_stream().synchronize()
-        elif isinstance(stream, int):
-            torch.cuda.synchronize()
-        else:
-            stream.synchronize()
-        self.proj = new
-        self.bits = 2
-        self._bind()
-        return self

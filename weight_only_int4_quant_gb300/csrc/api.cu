@@ -24,6 +24,8 @@ tlq_status set_error(tlq_status st, const char* fmt, ...) {
   return st;
 }
 
+void clear_error() { g_msg[0] = 0; }
+
 tlq_status cuda_error(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return TLQ_OK;
   return set_error(TLQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
@@ -121,6 +123,21 @@ tlq_status check_gemm_call(const uint16_t* A, const uint32_t* W, const uint16_t*
   return TLQ_OK;
 }
 
+// Row stride of a packed weight in words: 0 (compact) or at least the row's
+// words, a multiple of 4 (16-byte rows for the tensor maps).
+tlq_status check_ldw(int ldw, int K, int bits, const char* who) {
+  const int wpr = K / (32 / bits);
+  if (ldw != 0 && (ldw < wpr || ldw % 4))
+    return set_error(TLQ_EINVAL, "%s: ldw=%d (0, or >= K*bits/32 = %d and a multiple of 4)", who, ldw, wpr);
+  return TLQ_OK;
+}
+
+tlq_status check_workspace(const void* ws, size_t bytes, const char* who) {
+  if (ws && !aligned16(ws)) return set_error(TLQ_EINVAL, "%s: workspace must be 16-byte aligned", who);
+  if (!ws && bytes) return set_error(TLQ_EINVAL, "%s: null workspace with %zu bytes", who, bytes);
+  return TLQ_OK;
+}
+
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   const char* a0 = static_cast<const char*>(a);
   const char* b0 = static_cast<const char*>(b);
@@ -128,7 +145,7 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
 }
 
 GemmArgs plain_args(const uint16_t* A, const uint32_t* W, const uint16_t* S, const uint16_t* Z, uint16_t* C, int M,
-                    int N, int K, int bits, int group) {
+                    int N, int K, int bits, int group, int ldw = 0, void* ws = nullptr, size_t ws_bytes = 0) {
   GemmArgs a;
   a.A = reinterpret_cast<const __half*>(A);
   a.lda = K;
@@ -145,7 +162,16 @@ GemmArgs plain_args(const uint16_t* A, const uint32_t* W, const uint16_t* S, con
   a.bits = bits;
   a.group = group;
   a.epi = kEpiStore;
+  a.ldw = ldw;
+  a.ws = ws;
+  a.ws_bytes = ws ? ws_bytes : 0;
   return a;
+}
+
+// Bytes of the packed weight (rows of ldw words, the last row only its own).
+size_t weight_bytes(int N, int K, int bits, int ldw) {
+  const size_t wpr = (size_t)K / (32 / bits);
+  return ((size_t)(N - 1) * (ldw ? (size_t)ldw : wpr) + wpr) * 4;
 }
 
 }  // namespace tlq
@@ -166,6 +192,30 @@ tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint1
   if (overlaps(A, (size_t)M * K * 2, C, (size_t)M * N * 2))
     return set_error(TLQ_EINVAL, "tl_quant_gemm: A and C overlap");
   return run_gemm(plain_args(A, Wpacked, scales, zeros, C, M, N, K, bits, group), static_cast<cudaStream_t>(stream));
+}
+
+size_t tl_quant_gemm_workspace_size(int M, int N, int K, int bits, int group) {
+  g_msg[0] = 0;
+  if (M <= 16 || check_gemm_shape(M, N, K, bits, group, "tl_quant_gemm_workspace_size") != TLQ_OK) return 0;
+  GemmArgs a = plain_args(nullptr, nullptr, nullptr, nullptr, nullptr, M, N, K, bits, group);
+  return prefill_workspace_bytes(a);
+}
+
+tlq_status tl_quant_gemm_ws(const uint16_t* A, const uint32_t* Wpacked, const uint16_t* scales,
+                            const uint16_t* zeros, uint16_t* C, int M, int N, int K, int bits, int group,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  const char* who = "tl_quant_gemm_ws";
+  tlq_status st = check_gemm_call(A, Wpacked, scales, zeros, C, M, N, K, bits, group, who);
+  if (st != TLQ_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes, who)) != TLQ_OK) return st;
+  if (overlaps(A, (size_t)M * K * 2, C, (size_t)M * N * 2)) return set_error(TLQ_EINVAL, "%s: A and C overlap", who);
+  if (workspace && (overlaps(workspace, workspace_bytes, A, (size_t)M * K * 2) ||
+                    overlaps(workspace, workspace_bytes, C, (size_t)M * N * 2) ||
+                    overlaps(workspace, workspace_bytes, Wpacked, weight_bytes(N, K, bits, 0))))
+    return set_error(TLQ_EINVAL, "%s: the workspace overlaps A, C or the weights", who);
+  return run_gemm(plain_args(A, Wpacked, scales, zeros, C, M, N, K, bits, group, 0, workspace, workspace_bytes),
+                  static_cast<cudaStream_t>(stream));
 }
 
 namespace {
@@ -200,18 +250,37 @@ tlq_status tl_quant_gemm_batched_host(const tl_gemm_desc* d, int count, const vo
   return cuda_error(e, "tl_quant_gemm_batched_host: copy to the host");
 }
 
-tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales, const uint16_t* zeros,
-                                uint16_t* C, int M, int N2, int K, int bits, int group, void* stream) {
-  g_msg[0] = 0;
-  tlq_status st = check_gemm_call(A, Wgu, scales, zeros, C, M, N2, K, bits, group, "tl_quant_gemm_swiglu");
+namespace {
+tlq_status swiglu_gemm(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales, const uint16_t* zeros,
+                       uint16_t* C, int M, int N2, int K, int bits, int group, void* ws, size_t ws_bytes, void* stream,
+                       const char* who) {
+  tlq_status st = check_gemm_call(A, Wgu, scales, zeros, C, M, N2, K, bits, group, who);
   if (st != TLQ_OK) return st;
-  if (N2 % 16) return set_error(TLQ_EINVAL, "tl_quant_gemm_swiglu: N2=%d must be a multiple of 16", N2);
-  if (overlaps(A, (size_t)M * K * 2, C, (size_t)M * (N2 / 2) * 2))
-    return set_error(TLQ_EINVAL, "tl_quant_gemm_swiglu: A and C overlap");
-  GemmArgs a = plain_args(A, Wgu, scales, zeros, C, M, N2, K, bits, group);
+  if ((st = check_workspace(ws, ws_bytes, who)) != TLQ_OK) return st;
+  if (N2 % 16) return set_error(TLQ_EINVAL, "%s: N2=%d must be a multiple of 16", who, N2);
+  if (overlaps(A, (size_t)M * K * 2, C, (size_t)M * (N2 / 2) * 2)) return set_error(TLQ_EINVAL, "%s: A and C overlap", who);
+  if (ws && (overlaps(ws, ws_bytes, A, (size_t)M * K * 2) || overlaps(ws, ws_bytes, C, (size_t)M * (N2 / 2) * 2) ||
+             overlaps(ws, ws_bytes, Wgu, weight_bytes(N2, K, bits, 0))))
+    return set_error(TLQ_EINVAL, "%s: the workspace overlaps A, C or the weights", who);
+  GemmArgs a = plain_args(A, Wgu, scales, zeros, C, M, N2, K, bits, group, 0, ws, ws_bytes);
   a.ldc = N2 / 2;
   a.epi = kEpiSwiglu;
   return run_gemm(a, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+tlq_status tl_quant_gemm_swiglu(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales, const uint16_t* zeros,
+                                uint16_t* C, int M, int N2, int K, int bits, int group, void* stream) {
+  g_msg[0] = 0;
+  return swiglu_gemm(A, Wgu, scales, zeros, C, M, N2, K, bits, group, nullptr, 0, stream, "tl_quant_gemm_swiglu");
+}
+
+tlq_status tl_quant_gemm_swiglu_ws(const uint16_t* A, const uint32_t* Wgu, const uint16_t* scales,
+                                   const uint16_t* zeros, uint16_t* C, int M, int N2, int K, int bits, int group,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  return swiglu_gemm(A, Wgu, scales, zeros, C, M, N2, K, bits, group, workspace, workspace_bytes, stream,
+                     "tl_quant_gemm_swiglu_ws");
 }
 
 tlq_status tl_dequant_fp16(const uint32_t* Wpacked, const uint16_t* scales, const uint16_t* zeros, uint16_t* out, int N,
@@ -254,6 +323,8 @@ tlq_status check_batched(const tl_gemm_desc* d, int count) {
     tlq_status st = check_gemm_call(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
                                     d[i].bits, d[i].group, who);
     if (st != TLQ_OK) return st;
+    if ((st = check_ldw(d[i].ldw, d[i].K, d[i].bits, who)) != TLQ_OK) return st;
+    if ((st = check_workspace(d[i].workspace, d[i].workspace_bytes, who)) != TLQ_OK) return st;
   }
   for (int i = 0; i < count; ++i)
     for (int j = 0; j < count; ++j) {
@@ -261,6 +332,14 @@ tlq_status check_batched(const tl_gemm_desc* d, int count) {
         return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: C of problem %d overlaps A of problem %d", i, j);
       if (i < j && overlaps(d[i].C, (size_t)d[i].M * d[i].N * 2, d[j].C, (size_t)d[j].M * d[j].N * 2))
         return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: outputs of problems %d and %d overlap", i, j);
+      const void* w = d[i].workspace;
+      const size_t wb = d[i].workspace_bytes;
+      if (!w) continue;
+      if (overlaps(w, wb, d[j].A, (size_t)d[j].M * d[j].K * 2) || overlaps(w, wb, d[j].C, (size_t)d[j].M * d[j].N * 2) ||
+          overlaps(w, wb, d[j].Wpacked, weight_bytes(d[j].N, d[j].K, d[j].bits, d[j].ldw)) ||
+          (i < j && d[j].workspace && overlaps(w, wb, d[j].workspace, d[j].workspace_bytes)))
+        return set_error(TLQ_EINVAL, "tl_quant_gemm_batched: the workspace of problem %d overlaps a buffer of problem %d",
+                         i, j);
     }
   return TLQ_OK;
 }
@@ -336,7 +415,7 @@ tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_
     for (int i = 0; i < count; ++i) {
       if (d[i].M > 16 || d[i].bits != bits) continue;
       batch[n++] = plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
-                              d[i].bits, d[i].group);
+                              d[i].bits, d[i].group, d[i].ldw);
       if (n == kMaxDecodeProblems) {
         tlq_status st = launch_decode(batch, n, stream);
         if (st != TLQ_OK) return st;
@@ -364,7 +443,7 @@ tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_
     const int lane = used ? j % (used + 1) : 0;  // 0: the caller's stream
     ++j;
     st = launch_prefill(plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
-                                   d[i].bits, d[i].group),
+                                   d[i].bits, d[i].group, d[i].ldw, d[i].workspace, d[i].workspace_bytes),
                         lane ? ss->s[lane - 1] : stream);
   }
   for (int k = 0; k < used; ++k) {  // join even after a failed launch
@@ -420,7 +499,9 @@ tlq_status check_requant_overlaps(const tl_requant_desc* d, int count, int group
   RqRegion r[6 * kMaxRequantProblems];
   int n = 0;
   for (int i = 0; i < count; ++i) {
-    const size_t b4 = (size_t)d[i].N * d[i].K / 2, b2 = (size_t)d[i].N * d[i].K / 4;
+    // in place (W2 == W4): the INT2 rows keep the INT4 stride, so W2 spans W4
+    const size_t b4 = (size_t)d[i].N * d[i].K / 2;
+    const size_t b2 = d[i].W2 == d[i].W4 ? b4 : (size_t)d[i].N * d[i].K / 4;
     const size_t bg = (size_t)d[i].N * (d[i].K / group) * 2;
     r[n++] = {d[i].W4, b4, i, 0};
     r[n++] = {d[i].s4, bg, i, 1};
@@ -435,8 +516,8 @@ tlq_status check_requant_overlaps(const tl_requant_desc* d, int count, int group
       if (b == a || (r[b].kind >= 3 && b < a)) continue;
       if (!overlaps(r[a].p, r[a].n, r[b].p, r[b].n)) continue;
       const bool same_prob = r[a].prob == r[b].prob;
-      if (same_prob && r[a].p == r[b].p && r[a].n == r[b].n && r[a].kind - r[b].kind == 3 && r[b].kind >= 1)
-        continue;  // s2 == s4 or z2 == z4: converted in place
+      if (same_prob && r[a].p == r[b].p && r[a].n == r[b].n && r[a].kind - r[b].kind == 3)
+        continue;  // W2 == W4, s2 == s4 or z2 == z4: converted in place
       static const char* names[6] = {"W4", "s4", "z4", "W2", "s2", "z2"};
       return set_error(TLQ_EINVAL, "%s: %s of problem %d overlaps %s of problem %d", who, names[r[a].kind], r[a].prob,
                        names[r[b].kind], r[b].prob);
@@ -458,9 +539,19 @@ tlq_status requant(const tl_requant_desc* d, int count, int group, void* stream,
   tlq_status st = check_requant_overlaps(d, count, group, who);
   if (st != TLQ_OK) return st;
   if (count == 0) return TLQ_OK;
-  RequantArgs a[kMaxRequantProblems];
-  for (int i = 0; i < count; ++i) a[i] = RequantArgs{d[i].W4, d[i].s4, d[i].z4, d[i].W2, d[i].s2, d[i].z2, d[i].N, d[i].K};
-  return launch_requant(a, count, group, static_cast<cudaStream_t>(stream));
+  RequantArgs out[kMaxRequantProblems], inpl[kMaxRequantProblems];
+  int no = 0, ni = 0;
+  for (int i = 0; i < count; ++i) {
+    const RequantArgs a{d[i].W4, d[i].s4, d[i].z4, d[i].W2, d[i].s2, d[i].z2, d[i].N, d[i].K};
+    if (d[i].W2 == d[i].W4) inpl[ni++] = a;
+    else out[no++] = a;
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (no) {
+    st = launch_requant(out, no, group, s);
+    if (st != TLQ_OK) return st;
+  }
+  return ni ? launch_requant_in_place(inpl, ni, group, s) : TLQ_OK;
 }
 }  // namespace
 
@@ -486,7 +577,8 @@ struct BlockSpec {
   uint16_t *h, *qkv_out, *o_out, *act_out;
   int normalize;
   const char* who;
-  bool no_alloc = false;  // no device allocation in any launch (GEMMs run without a k split)
+  void* ws;  // the caller's k-split workspace, shared by the block's GEMMs (they run in order)
+  size_t ws_bytes;
 };
 
 tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_t stream) {
@@ -511,6 +603,11 @@ tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_
     tlq_status st = check_gemm_shape(M, p->N, p->K, b.bits, b.group, names[i]);
     if (st != TLQ_OK) return st;
     if (p->N % 8) return set_error(TLQ_EINVAL, "%s: %s N=%d must be a multiple of 8", who, names[i], p->N);
+    if ((st = check_ldw(p->ldw, p->K, b.bits, names[i])) != TLQ_OK) return st;
+  }
+  {
+    tlq_status st = check_workspace(b.ws, b.ws_bytes, who);
+    if (st != TLQ_OK) return st;
   }
   if (!aligned16(b.h) || !aligned16(b.qkv_out) || !aligned16(b.o_out) || !aligned16(b.act_out))
     return set_error(TLQ_EINVAL, "%s: scratch buffers must be 16-byte aligned", who);
@@ -539,7 +636,9 @@ tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_
     a.group = b.group;
     a.M = M;
     a.l2_keep = keep ? 1 : 0;
-    a.no_alloc = b.no_alloc ? 1 : 0;
+    a.ldw = p->ldw;
+    a.ws = b.ws;
+    a.ws_bytes = b.ws ? b.ws_bytes : 0;
     a.A = reinterpret_cast<const __half*>(A);
     a.lda = lda;
     a.W = p->W;
@@ -571,7 +670,8 @@ tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void
   g_msg[0] = 0;
   if (!x || !b) return set_error(TLQ_EINVAL, "tl_loop_block_forward: null x or block");
   const BlockSpec s = {{&b->qkv, &b->o, &b->up, &b->down}, b->bits, b->group, b->D, b->up.N, false,
-                       b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, "tl_loop_block_forward"};
+                       b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, "tl_loop_block_forward",
+                       b->workspace, b->workspace_bytes};
   return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
 }
 
@@ -595,7 +695,8 @@ tlq_status tl_loop_block_forward_chunked(float* x, const tl_block* b, int L, int
   g_msg[0] = 0;
   if (!x || !b) return set_error(TLQ_EINVAL, "tl_loop_block_forward_chunked: null x or block");
   const BlockSpec s = {{&b->qkv, &b->o, &b->up, &b->down}, b->bits, b->group, b->D, b->up.N, false,
-                       b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, "tl_loop_block_forward_chunked"};
+                       b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, "tl_loop_block_forward_chunked",
+                       b->workspace, b->workspace_bytes};
   return block_forward_chunked(x, s, L, M, chunk, static_cast<cudaStream_t>(stream));
 }
 
@@ -603,7 +704,8 @@ tlq_status tl_swiglu_block_forward_chunked(float* x, const tl_swiglu_block* b, i
   g_msg[0] = 0;
   if (!x || !b) return set_error(TLQ_EINVAL, "tl_swiglu_block_forward_chunked: null x or block");
   const BlockSpec s = {{&b->qkv, &b->o, &b->gate_up, &b->down}, b->bits, b->group, b->D, b->gate_up.N / 2, true,
-                       b->h, b->qkv_out, b->o_out, b->act_out, b->normalize, "tl_swiglu_block_forward_chunked"};
+                       b->h, b->qkv_out, b->o_out, b->act_out, b->normalize, "tl_swiglu_block_forward_chunked",
+                       b->workspace, b->workspace_bytes};
   return block_forward_chunked(x, s, L, M, chunk, static_cast<cudaStream_t>(stream));
 }
 
@@ -611,8 +713,55 @@ tlq_status tl_swiglu_block_forward(float* x, const tl_swiglu_block* b, int L, in
   g_msg[0] = 0;
   if (!x || !b) return set_error(TLQ_EINVAL, "tl_swiglu_block_forward: null x or block");
   const BlockSpec s = {{&b->qkv, &b->o, &b->gate_up, &b->down}, b->bits, b->group, b->D, b->gate_up.N / 2, true,
-                       b->h, b->qkv_out, b->o_out, b->act_out, b->normalize, "tl_swiglu_block_forward"};
+                       b->h, b->qkv_out, b->o_out, b->act_out, b->normalize, "tl_swiglu_block_forward",
+                       b->workspace, b->workspace_bytes};
   return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+// The context-length tier switch of a loop block: every INT4 projection
+// re-quantized to INT2 (out of place into dst[i], or in place when dst is
+// NULL or dst[i].W is the INT4 weight itself), then the block's description
+// rewritten so later forwards take the INT2 kernels.
+tlq_status block_to_int2(tl_qproj* const* proj, int* bits, int group, const tl_qproj* dst, const char* who,
+                         void* stream) {
+  if (*bits != 4) return set_error(TLQ_EINVAL, "%s: the block holds INT%d weights (INT4 needed)", who, *bits);
+  tl_requant_desc d[4];
+  tl_qproj next[4];
+  for (int i = 0; i < 4; ++i) {
+    const tl_qproj& p = *proj[i];
+    if (p.ldw != 0 && p.ldw != p.K / 8)
+      return set_error(TLQ_EINVAL, "%s: projection %d: INT4 weights with ldw=%d (compact rows needed)", who, i, p.ldw);
+    const tl_qproj* o = dst ? &dst[i] : nullptr;
+    if (o && (o->N != p.N || o->K != p.K))
+      return set_error(TLQ_EINVAL, "%s: projection %d: destination is [%d x %d], the weight [%d x %d]", who, i, o->N,
+                       o->K, p.N, p.K);
+    uint32_t* W2 = const_cast<uint32_t*>(o ? o->W : p.W);
+    uint16_t* s2 = const_cast<uint16_t*>(o ? o->s : p.s);
+    uint16_t* z2 = const_cast<uint16_t*>(o ? o->z : p.z);
+    d[i] = tl_requant_desc{p.W, p.s, p.z, W2, s2, z2, p.N, p.K};
+    next[i] = tl_qproj{W2, s2, z2, p.N, p.K, W2 == p.W ? p.K / 8 : 0};
+  }
+  tlq_status st = requant(d, 4, group, stream, who);  // validates everything before any launch
+  if (st != TLQ_OK) return st;
+  for (int i = 0; i < 4; ++i) *proj[i] = next[i];
+  *bits = 2;
+  return TLQ_OK;
+}
+}  // namespace
+
+tlq_status tl_loop_block_to_int2(tl_block* block, const tl_qproj* dst, void* stream) {
+  g_msg[0] = 0;
+  if (!block) return set_error(TLQ_EINVAL, "tl_loop_block_to_int2: null block");
+  tl_qproj* proj[4] = {&block->qkv, &block->o, &block->up, &block->down};
+  return block_to_int2(proj, &block->bits, block->group, dst, "tl_loop_block_to_int2", stream);
+}
+
+tlq_status tl_swiglu_block_to_int2(tl_swiglu_block* block, const tl_qproj* dst, void* stream) {
+  g_msg[0] = 0;
+  if (!block) return set_error(TLQ_EINVAL, "tl_swiglu_block_to_int2: null block");
+  tl_qproj* proj[4] = {&block->qkv, &block->o, &block->gate_up, &block->down};
+  return block_to_int2(proj, &block->bits, block->group, dst, "tl_swiglu_block_to_int2", stream);
 }
 
 tlq_status tl_check_status(void* stream) {
@@ -647,14 +796,12 @@ tlq_status tl_selftest_wait_timeout(unsigned limit_us, void* stream) {
 
 }  // extern "C"
 namespace tlq {
-// The ReLU loop block with no device allocation in any launch (the entry
-// point for callers that cannot allocate; its scratch comes from the caller).
-tlq_status loop_block_forward_no_alloc(float* x, const tl_block* b, int L, int M, const char* who, void* stream) {
+// The ReLU loop block under a caller-chosen name (the allocation-free entry
+// point reports its own name in messages).
+tlq_status loop_block_forward_named(float* x, const tl_block* b, int L, int M, const char* who, void* stream) {
   if (!x || !b) return set_error(TLQ_EINVAL, "%s: null x or block", who);
-  BlockSpec s = {{&b->qkv, &b->o, &b->up, &b->down}, b->bits, b->group, b->D, b->up.N, false,
-                 b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, who};
-  s.no_alloc = true;
+  const BlockSpec s = {{&b->qkv, &b->o, &b->up, &b->down}, b->bits, b->group, b->D, b->up.N, false,
+                       b->h, b->qkv_out, b->o_out, b->up_out, b->normalize, who, b->workspace, b->workspace_bytes};
   return block_forward(x, s, L, M, static_cast<cudaStream_t>(stream));
 }
 }  // namespace tlq
-

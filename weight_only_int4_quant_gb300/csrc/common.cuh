@@ -254,12 +254,16 @@ struct GemmArgs {
   int ldx;
   int M, N, K, bits, group;
   int epi;
-  int l2_keep = 0;   // 1: stream the weights with an L2 evict-last policy (reused soon, e.g. the loop block)
-  int no_alloc = 0;  // 1: the launch may not allocate device memory (the prefill kernel then splits no k)
+  int l2_keep = 0;       // 1: stream the weights with an L2 evict-last policy (reused soon, e.g. the loop block)
+  int ldw = 0;           // packed-weight row stride in 32-bit words (0: compact rows of K*bits/32 words)
+  void* ws = nullptr;    // caller-owned workspace for the prefill kernel's k split (nullptr: no k split)
+  size_t ws_bytes = 0;
 };
 
 // Error reporting (thread-local message)
 tlq_status set_error(tlq_status st, const char* fmt, ...);
+// Clears the calling thread's message (every entry point starts with it).
+void clear_error();
 tlq_status cuda_error(cudaError_t e, const char* what);
 
 // Tensor-map encoding through the driver entry point (no -lcuda needed).
@@ -285,7 +289,10 @@ bool pdl_enabled();
 constexpr int kMaxDecodeProblems = 16;
 tlq_status launch_decode(const GemmArgs* a, int count, cudaStream_t stream);
 tlq_status launch_prefill(const GemmArgs& a, cudaStream_t stream);
-tlq_status loop_block_forward_no_alloc(float* x, const tl_block* b, int L, int M, const char* who, void* stream);
+// Workspace bytes the prefill kernel's planner would use for this problem with
+// an unlimited workspace (0: it would not split K).
+size_t prefill_workspace_bytes(const GemmArgs& a);
+tlq_status loop_block_forward_named(float* x, const tl_block* b, int L, int M, const char* who, void* stream);
 tlq_status launch_pack(const uint8_t* codes, uint32_t* W, int N, int K, int bits, cudaStream_t stream);
 tlq_status launch_unpack(const uint32_t* W, uint8_t* codes, int N, int K, int bits, cudaStream_t stream);
 // INT4 -> INT2 re-quantization of up to kMaxRequantProblems weights sharing
@@ -295,12 +302,14 @@ struct RequantArgs {
   const uint32_t* W4;
   const uint16_t* s4;
   const uint16_t* z4;
-  uint32_t* W2;
+  uint32_t* W2;  // == W4: in place (INT2 rows keep the INT4 row stride of K/8 words)
   uint16_t* s2;
   uint16_t* z2;
   int N, K;
 };
 tlq_status launch_requant(const RequantArgs* a, int count, int group, cudaStream_t stream);
+// The in-place conversions of a batch (every problem has W2 == W4), one launch.
+tlq_status launch_requant_in_place(const RequantArgs* a, int count, int group, cudaStream_t stream);
 tlq_status launch_body(const uint32_t* W, const uint16_t* s, const uint16_t* z, uint16_t* out, int N, int K, int bits,
                        int group, cudaStream_t stream);
 tlq_status launch_rmsnorm(const float* x, __half* h, int M, int D, int normalize, cudaStream_t stream);

@@ -807,7 +807,7 @@ bool build_unit_lists(DecodeLaunch& L, int grid) {
 bool same_args(const GemmArgs& x, const GemmArgs& y) {
   return x.A == y.A && x.lda == y.lda && x.W == y.W && x.S == y.S && x.Z == y.Z && x.C == y.C && x.ldc == y.ldc &&
          x.X == y.X && x.ldx == y.ldx && x.M == y.M && x.N == y.N && x.K == y.K && x.bits == y.bits &&
-         x.group == y.group && x.epi == y.epi && x.l2_keep == y.l2_keep && x.no_alloc == y.no_alloc;
+         x.group == y.group && x.epi == y.epi && x.l2_keep == y.l2_keep && x.ldw == y.ldw;
 }
 
 // The launch description of a call: tensor maps, problem table, unit lists,
@@ -855,7 +855,8 @@ tlq_status build_launch(const GemmArgs* a, int count, DecodeLaunch& L, size_t& s
     gmax = std::max(gmax, pr.G);
     const uint64_t wpr = (uint64_t)g.K / F::CPW;
     const bool contig = BITS == 4 && pr.spanq == 4;  // see WordMap
-    tlq_status st = encode_tiled_2d(&L.wmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT32, g.W, wpr, (uint64_t)g.N, wpr * 4,
+    const uint64_t ldw = g.ldw > 0 ? (uint64_t)g.ldw : wpr;  // row stride in words
+    tlq_status st = encode_tiled_2d(&L.wmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT32, g.W, wpr, (uint64_t)g.N, ldw * 4,
                                     kWordsPerKBlock, ROWS,
                                     contig ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);

@@ -13,7 +13,7 @@
 // dequantization work per MMA.  Warp roles (DQW = 16 dequantizing warps with
 // one token tile, 8 with two):
 //   warps 0 .. DQW-1  dequantize: the packed words of a stage (TMA ring) become
-//              exact FP16 weights (q - z) * s in the UMMA K-major SWIZZLE_128B
+//              FP16 weights (q - z) * s (see GroupDq) in the UMMA K-major SWIZZLE_128B
 //              layout of the B ring (two threads per weight row with one
 //              token tile, one with two); after the main loop warps 0-7 drain
 //              the accumulator (tcgen05.ld) in the epilogue.
@@ -24,7 +24,9 @@
 //              accumulator-ready barriers.
 // Short-M problems split K over the CTAs of a thread-block cluster; partial
 // tiles are reduced in a fixed rank order through an FP32 workspace in L2
-// (deterministic, no atomics).  Every mbarrier wait is bounded.
+// (deterministic, no atomics).  The workspace is the caller's: the library
+// allocates nothing, and without a workspace large enough for a split the
+// planner keeps K whole.  Every mbarrier wait is bounded.
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -151,6 +153,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t hadd2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -173,25 +181,58 @@ __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
-// FP16 weights of one packed word in k order, w = q * s + (-(z * s)): byte j
-// of the word is copied into both halves (one PRMT), the codes it holds are
-// masked into the mantissas of (base + q) halves (one LOP3 per pair), the
-// bases are removed exactly (one HSUB2) and one FMA applies scale and zero
-// point.  INT4: out[j] = (w_2j, w_2j+1); INT2: out[2j], out[2j+1] =
-// (w_4j, w_4j+1), (w_4j+2, w_4j+3).
+// The per-group constants of the dequantization: the zero point splits into
+// an integer part zi = round(z) (clamped to +-1024) and the rest zf = z - zi
+// (exact in FP16).  sub = (base + zi) for each code position's base (exact:
+// integers of magnitude <= 2048), so the HSUB2 below yields the exact integer
+// q - zi; nzf = -fp16(zf * s).  Then w = fp16((q - zi) * s - fp16(zf * s))
+// with one FMA: one rounding of the exact (q - zi) * s plus the rounding of a
+// bias of at most s / 2, instead of a bias of up to |z| * s.
+struct GroupDq {
+  uint32_t s2;     // (s, s)
+  uint32_t nzf2;   // (-fp16(zf * s), same)
+  uint32_t sub_a;  // INT4: (1024 + zi, 64 + zi); INT2: (1024 + zi, 256 + zi)
+  uint32_t sub_b;  // INT2: (64 + zi, 16 + zi)
+};
+
 template <int BITS>
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t nzs2, uint32_t (&out)[BITS == 4 ? 4 : 8]) {
+__device__ __forceinline__ GroupDq group_dq(uint32_t s_bits, uint32_t z_bits) {
+  // zi = round(z) clamped to [-1024, 1024]: zf = z - zi is exact (|zf| <= 1/2
+  // inside the clamp; beyond it z is an integer multiple of ulp(z) >= 1 and so
+  // is z -+ 1024), and base + zi and q - zi stay integers of magnitude <= 2048
+  const __half z = __ushort_as_half((unsigned short)z_bits);
+  const __half lim = __ushort_as_half((unsigned short)0x6400u);  // 1024
+  const __half zi = __hmax(__hneg(lim), __hmin(lim, hrint(z)));
+  const __half zf = __hsub(z, zi);
+  GroupDq g;
+  g.s2 = (uint32_t)(s_bits & 0xFFFFu) * 0x00010001u;
+  const uint32_t zf2 = (uint32_t)__half_as_ushort(zf) * 0x00010001u;
+  g.nzf2 = hmul2u(zf2, g.s2) ^ 0x80008000u;
+  const uint32_t zi2 = (uint32_t)__half_as_ushort(zi) * 0x00010001u;
+  g.sub_a = hadd2u(BITS == 4 ? 0x54006400u : 0x5C006400u, zi2);
+  g.sub_b = hadd2u(0x4C005400u, zi2);
+  return g;
+}
+
+// FP16 weights of one packed word in k order: byte j of the word is copied
+// into both halves (one PRMT), the codes it holds are masked into the
+// mantissas of (base + q) halves (one LOP3 per pair), (base + zi) is removed
+// exactly (one HSUB2) and one FMA applies scale and the fractional zero
+// point (see GroupDq).  INT4: out[j] = (w_2j, w_2j+1); INT2: out[2j],
+// out[2j+1] = (w_4j, w_4j+1), (w_4j+2, w_4j+3).
+template <int BITS>
+__device__ __forceinline__ void dequant_word(uint32_t w, const GroupDq& g, uint32_t (&out)[BITS == 4 ? 4 : 8]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t x = prmt(w, 0u, (uint32_t)(j | (j << 8)));  // byte j in bytes 0 and 2
     if constexpr (BITS == 4) {
       const uint32_t h = and_or(x, 0x00F0000Fu, 0x54006400u);  // (1024 + q_2j, 64 + q_2j+1)
-      out[j] = hfma2u(hsub2u(h, 0x54006400u), s2, nzs2);
+      out[j] = hfma2u(hsub2u(h, g.sub_a), g.s2, g.nzf2);
     } else {
       const uint32_t ha = and_or(x, 0x000C0003u, 0x5C006400u);  // (1024 + q_4j, 256 + q_4j+1)
       const uint32_t hb = and_or(x, 0x00C00030u, 0x4C005400u);  // (64 + q_4j+2, 16 + q_4j+3)
-      out[2 * j] = hfma2u(hsub2u(ha, 0x5C006400u), s2, nzs2);
-      out[2 * j + 1] = hfma2u(hsub2u(hb, 0x4C005400u), s2, nzs2);
+      out[2 * j] = hfma2u(hsub2u(ha, g.sub_a), g.s2, g.nzf2);
+      out[2 * j + 1] = hfma2u(hsub2u(hb, g.sub_b), g.s2, g.nzf2);
     }
   }
 }
@@ -381,11 +422,7 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
     // One stage: dequantize this thread's row of the packed tile into the B
     // ring (s_lo.. are raw FP16 bits of the scale / zero of the stage's first
     // and, for two groups per stage, second group).
-    auto do_stage = [&](int kb, uint32_t s_lo, uint32_t s_hi, uint32_t z_lo, uint32_t z_hi) -> bool {
-      s_lo = bcast16((unsigned short)s_lo);
-      s_hi = bcast16((unsigned short)s_hi);
-      const uint32_t nzs_lo = hmul2u(bcast16((unsigned short)z_lo), s_lo) ^ 0x80008000u;  // -(z * s)
-      const uint32_t nzs_hi = hmul2u(bcast16((unsigned short)z_hi), s_hi) ^ 0x80008000u;
+    auto do_stage = [&](int kb, const GroupDq& g_lo, const GroupDq& g_hi) -> bool {
       // this stage's packed words: row r of the TMA tile (INT4: two 16-byte
       // chunks, swapped in rows with bit 2 set by SWIZZLE_32B; INT2: one)
       const int ws = kb % SW;
@@ -427,7 +464,7 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
           const int wj = w0 + lj;
           const bool hi = two_groups && (wj >= WPS / 2);
           uint32_t o[OUTW];
-          dequant_word<BITS>(wv[lj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
+          dequant_word<BITS>(wv[lj], hi ? g_hi : g_lo, o);
           if constexpr (BITS == 4) {
             sts128(brow + (((uint32_t)wj ^ (uint32_t)(r & 7)) << 4), o[0], o[1], o[2], o[3]);
           } else {
@@ -441,7 +478,7 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
         const int wj = w0 + lj;
         const bool hi = two_groups && (wj >= WPS / 2);
         uint32_t o[OUTW];
-        dequant_word<BITS>(wv[lj], hi ? s_hi : s_lo, hi ? nzs_hi : nzs_lo, o);
+        dequant_word<BITS>(wv[lj], hi ? g_hi : g_lo, o);
         const bool valid = row_ok && (ks + wj * CPW < p.K);
         if constexpr (BITS == 4) {
           const uint32_t c = (uint32_t)wj;
@@ -473,20 +510,27 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
 
     bool ok = true;
     if (szvec) {
-      // plain stage loop (no unrolled copies: the kernel's code stays small)
+      // plain stage loop (no unrolled copies: the kernel's code stays small);
+      // the group constants are formed once per group (a group of 128 codes
+      // spans two stages), on a branch every thread takes together
+      GroupDq g_lo = {}, g_hi = {};
+      int gcur = -1;
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int kpos = k0 + kb * BK;
         const int g0 = p.gshift >= 0 ? (kpos >> p.gshift) : kpos / p.group;
-        if ((g0 >> 3) > win) {  // a stage spans at most two groups: the window moves by one
-          sv = svn;
-          zv = zvn;
-          ++win;
-          load_win(win + 1, svn, zvn);
+        if (g0 != gcur) {
+          if ((g0 >> 3) > win) {  // a stage spans at most two groups: the window moves by one
+            sv = svn;
+            zv = zvn;
+            ++win;
+            load_win(win + 1, svn, zvn);
+          }
+          // with two groups per stage g0 is even, so g0 + 1 stays in the window
+          g_lo = group_dq<BITS>(pick16(sv, g0 & 7), pick16(zv, g0 & 7));
+          g_hi = two_groups ? group_dq<BITS>(pick16(sv, (g0 + 1) & 7), pick16(zv, (g0 + 1) & 7)) : g_lo;
+          gcur = g0;
         }
-        // with two groups per stage g0 is even, so g0 + 1 stays in the window
-        const uint32_t s_lo = pick16(sv, g0 & 7), z_lo = pick16(zv, g0 & 7);
-        ok = do_stage(kb, s_lo, two_groups ? pick16(sv, (g0 + 1) & 7) : s_lo, z_lo,
-                      two_groups ? pick16(zv, (g0 + 1) & 7) : z_lo);
+        ok = do_stage(kb, g_lo, g_hi);
       }
     } else {
       for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
@@ -494,9 +538,10 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
         for (int j = 0; j < kPrefetch; ++j) {
           const int kb = kb0 + j;
           if (kb < nkb && ok) {
-            const uint32_t s_lo = sring[j][0], s_hi = sring[j][1], z_lo = zring[j][0], z_hi = zring[j][1];
+            const GroupDq g_lo = group_dq<BITS>(sring[j][0], zring[j][0]);
+            const GroupDq g_hi = two_groups ? group_dq<BITS>(sring[j][1], zring[j][1]) : g_lo;
             if (kb + kPrefetch < nkb) issue(kb + kPrefetch, sring[j], zring[j]);
-            ok = do_stage(kb, s_lo, s_hi, z_lo, z_hi);
+            ok = do_stage(kb, g_lo, g_hi);
           }
         }
       }
@@ -719,26 +764,13 @@ __global__ void __launch_bounds__(PCfg<NMT>::THREADS, 1)
   }
 }
 
-// The split-K workspaces come from the device's default stream-ordered memory
-// pool.  Freed blocks stay in the pool (release threshold raised once per
-// device, outside stream capture) instead of going back to the driver at
-// every synchronization, so a launch after a synchronize does not map new
-// memory.
-void keep_pool_memory(cudaStream_t stream) {
-  static std::mutex mu;
-  static bool done[64] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
-  std::lock_guard<std::mutex> lk(mu);
-  if (done[dev]) return;
-  cudaMemPool_t pool;
-  if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
-    uint64_t keep = uint64_t(1) << 30;
-    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-  }
-  done[dev] = true;
+// FP32 workspace of a launch with NMT token tiles per CTA and a k split of
+// ks: every cluster's ks partial tiles (NMT * ks^2 slices of BM x BN/ks).
+size_t split_ws_bytes(int M, int N, int nmt, int ks) {
+  if (ks <= 1) return 0;
+  const size_t ntile = (size_t)(N + BN - 1) / BN;
+  const size_t mtile = (size_t)(M + BM * nmt - 1) / (BM * nmt);
+  return ntile * mtile * (size_t)nmt * (size_t)ks * BM * BN * sizeof(float);
 }
 
 template <int BITS, int EPI, int NMT>
@@ -787,7 +819,8 @@ tlq_status launch_impl(const GemmArgs& a, int ks, cudaStream_t stream) {
 
   CUtensorMap wmap;
   const uint64_t wpr = (uint64_t)a.K * BITS / 32;  // words per row
-  st = encode_tiled_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, wpr, (uint64_t)a.N, wpr * 4, BK * BITS / 32, BN,
+  const uint64_t ldw = a.ldw > 0 ? (uint64_t)a.ldw : wpr;  // row stride in words
+  st = encode_tiled_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.W, wpr, (uint64_t)a.N, ldw * 4, BK * BITS / 32, BN,
                        BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (st != TLQ_OK) return st;
@@ -831,21 +864,18 @@ tlq_status launch_impl(const GemmArgs& a, int ks, cudaStream_t stream) {
   }
   lc.attrs = attrs;
   lc.numAttrs = na;
-  // k split: the partial slices go through a stream-ordered FP32 workspace of
-  // this launch (NMT * ksplit^2 slices of BM x BN/ksplit floats per cluster,
-  // i.e. ksplit partial tiles), freed in stream order after it
+  // k split: the partial slices go through the caller's FP32 workspace
+  // (NMT * ksplit^2 slices of BM x BN/ksplit floats per cluster, i.e.
+  // ksplit partial tiles); the planner only splits when it is large enough
   p.ws = nullptr;
   if (p.ksplit > 1) {
-    const size_t wsb = (size_t)ntile * mtile * NMT * p.ksplit * BM * BN * sizeof(float);
-    keep_pool_memory(stream);
-    cudaError_t ea = cudaMallocAsync(reinterpret_cast<void**>(&p.ws), wsb, stream);
-    if (ea != cudaSuccess) return cuda_error(ea, "prefill: split-K workspace");
+    const size_t wsb = split_ws_bytes(a.M, a.N, NMT, p.ksplit);
+    if (!a.ws || a.ws_bytes < wsb)
+      return set_error(TLQ_EINVAL, "prefill: a k split of %d needs a workspace of %zu bytes (%zu given)", p.ksplit,
+                       wsb, a.ws ? a.ws_bytes : (size_t)0);
+    p.ws = static_cast<float*>(a.ws);
   }
   cudaError_t e = cudaLaunchKernelEx(&lc, kern, amap, wmap, cmap, p);
-  if (p.ws) {
-    const cudaError_t ef = cudaFreeAsync(p.ws, stream);
-    if (e == cudaSuccess) e = ef;
-  }
   if (e != cudaSuccess) return cuda_error(e, "prefill: launch");
   if (log_enabled())
     fprintf(stderr,
@@ -910,42 +940,65 @@ double prefill_estimate_us(int nmt, int ks, int tiles, int nkb, int clusters) {
 // Token tiles per CTA (two share one dequantized weight tile) and k split:
 // the candidate with the smallest estimate among NMT in {1, 2} (2 only when
 // M has two token tiles) and ks in {1, 2, 4, 8} with slices of at least 4
-// stages; ties keep the first (fewer tiles, smaller split).
-// TLQ_PREFILL_NMT=1|2 and TLQ_PREFILL_KSPLIT=1|2|4|8 force either choice;
-// callers that may not allocate get no k split.
+// stages whose workspace fits in ws_bytes; ties keep the first (fewer tiles,
+// smaller split).  TLQ_PREFILL_NMT=1|2 and TLQ_PREFILL_KSPLIT=1|2|4|8 force
+// either choice.  Returns false when no candidate is left (a forced split
+// without the workspace it needs).
+struct PrefillPlan {
+  int nmt, ks;
+  double est_us;
+};
+
 template <int BITS, int EPI>
-tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
+bool plan_prefill(const GemmArgs& a, size_t ws_bytes, PrefillPlan& out) {
   int force_nmt = 0, force_ks = 0;
   if (const char* e = getenv("TLQ_PREFILL_NMT")) force_nmt = atoi(e);
   if (const char* e = getenv("TLQ_PREFILL_KSPLIT")) force_ks = atoi(e);
   if (force_nmt != 1 && force_nmt != 2) force_nmt = 0;
-  if (a.no_alloc) force_ks = 1;  // a k split needs a workspace
   const int ntile = (a.N + BN - 1) / BN;
   const int nkb = (a.K + BK - 1) / BK;
-  int best_nmt = 1, best_ks = 1;
-  double best = 1e30;
+  out = PrefillPlan{1, 1, 1e30};
   for (int nmt = 1; nmt <= 2; ++nmt) {
     if (force_nmt && nmt != force_nmt) continue;
     if (nmt == 2 && a.M <= BM && !force_nmt) continue;
     const int tiles = ntile * ((a.M + BM * nmt - 1) / (BM * nmt));
     for (int ks = 1; ks <= 8; ks *= 2) {
       if (force_ks ? ks != force_ks : (ks > 1 && nkb / ks < 4)) continue;
+      if (split_ws_bytes(a.M, a.N, nmt, ks) > ws_bytes) continue;
       const int clusters = nmt == 1 ? max_clusters<BITS, EPI, 1>(ks) : max_clusters<BITS, EPI, 2>(ks);
       const double t = prefill_estimate_us(nmt, ks, tiles, nkb, clusters);
-      if (t < best) {
-        best = t;
-        best_nmt = nmt;
-        best_ks = ks;
-      }
+      if (t < out.est_us) out = PrefillPlan{nmt, ks, t};
     }
   }
-  if (best > 1e29) return set_error(TLQ_EINVAL, "prefill: k split %d", force_ks);
+  return out.est_us < 1e29;
+}
+
+template <int BITS, int EPI>
+tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
+  PrefillPlan pl;
+  if (!plan_prefill<BITS, EPI>(a, a.ws ? a.ws_bytes : 0, pl))
+    return set_error(TLQ_EINVAL, "prefill: no k split allowed by TLQ_PREFILL_KSPLIT fits the workspace (%zu bytes)",
+                     a.ws ? a.ws_bytes : (size_t)0);
   if (log_enabled()) {
-    const int c1 = best_nmt == 1 ? max_clusters<BITS, EPI, 1>(best_ks) : max_clusters<BITS, EPI, 2>(best_ks);
+    const int c1 = pl.nmt == 1 ? max_clusters<BITS, EPI, 1>(pl.ks) : max_clusters<BITS, EPI, 2>(pl.ks);
     fprintf(stderr, "[tlq] prefill M=%d N=%d K=%d: %d token tile(s), k split %d (%d clusters fit), est %.1f us\n",
-            a.M, a.N, a.K, best_nmt, best_ks, c1, best);
+            a.M, a.N, a.K, pl.nmt, pl.ks, c1, pl.est_us);
   }
-  return best_nmt == 2 ? launch_impl<BITS, EPI, 2>(a, best_ks, s) : launch_impl<BITS, EPI, 1>(a, best_ks, s);
+  return pl.nmt == 2 ? launch_impl<BITS, EPI, 2>(a, pl.ks, s) : launch_impl<BITS, EPI, 1>(a, pl.ks, s);
+}
+
+template <int BITS>
+size_t workspace_bits(const GemmArgs& a) {
+  PrefillPlan pl;
+  const size_t unlimited = ~(size_t)0;
+  bool ok;
+  switch (a.epi) {
+    case kEpiStore: ok = plan_prefill<BITS, kEpiStore>(a, unlimited, pl); break;
+    case kEpiRelu: ok = plan_prefill<BITS, kEpiRelu>(a, unlimited, pl); break;
+    case kEpiSwiglu: ok = plan_prefill<BITS, kEpiSwiglu>(a, unlimited, pl); break;
+    default: ok = plan_prefill<BITS, kEpiResidual>(a, unlimited, pl); break;
+  }
+  return ok ? split_ws_bytes(a.M, a.N, pl.nmt, pl.ks) : 0;
 }
 
 template <int BITS>
@@ -959,6 +1012,11 @@ tlq_status dispatch_epi(const GemmArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+size_t prefill_workspace_bytes(const GemmArgs& a) {
+  if (a.M <= 16) return 0;
+  return a.bits == 4 ? workspace_bits<4>(a) : workspace_bits<2>(a);
+}
 
 tlq_status launch_prefill(const GemmArgs& a, cudaStream_t stream) {
   if (a.lda % 8) return set_error(TLQ_EINVAL, "prefill: lda=%d must be a multiple of 8", a.lda);

@@ -145,9 +145,18 @@ __device__ __forceinline__ int rq_advance(const RqLaunch& L, int p, long long g)
   return p;
 }
 
+// A chunk of 32 codes from src: through the read-only path from global
+// memory, or (GENERIC) a plain load through a generic address (the in-place
+// kernel's shared-memory staging).
+template <bool GENERIC>
+__device__ __forceinline__ uint4 rq_load(const uint4* src) {
+  if constexpr (GENERIC) return *src;
+  else return __ldg(src);
+}
+
 // Converts one group held in v[0..TC) (TC > 0) or re-read from src (TC == 0,
 // T chunks).  sz = s4 | z4 << 16.
-template <int TC>
+template <int TC, bool GENERIC = false>
 __device__ __forceinline__ void rq_group(const uint4* v, const uint4* __restrict__ src, int T, uint32_t sz,
                                          uint2* __restrict__ dst, uint16_t* s2, uint16_t* z2) {
   const int nch = TC > 0 ? TC : T;
@@ -162,11 +171,11 @@ __device__ __forceinline__ void rq_group(const uint4* v, const uint4* __restrict
     }
     first = v[0].x & 15u;
   } else {
-    first = __ldg(reinterpret_cast<const uint32_t*>(src)) & 15u;
+    first = rq_load<GENERIC>(src).x & 15u;
 #pragma unroll 1
     for (int i = 0; i < nch; ++i) {
       uint32_t a, b;
-      rq_chunk_minmax(__ldg(src + i), a, b);
+      rq_chunk_minmax(rq_load<GENERIC>(src + i), a, b);
       mn = rq_min(mn, a);
       mx = rq_max(mx, b);
     }
@@ -216,7 +225,7 @@ __device__ __forceinline__ void rq_group(const uint4* v, const uint4* __restrict
   } else {
 #pragma unroll 1
     for (int i = 0; i < nch; ++i) {
-      const uint4 u = __ldg(src + i);
+      const uint4 u = rq_load<GENERIC>(src + i);
       dst[i] = make_uint2(rq_pack16(u.x, u.y, t), rq_pack16(u.z, u.w, t));
     }
   }
@@ -272,7 +281,77 @@ __global__ void __launch_bounds__(kRqThreads, 3) requant_kernel(const __grid_con
   }
 }
 
+// In place ("beta-Informed Deployment Features", CTX-TIER, "Details of the
+// shipped kernel", storage reuse): W2 is W4 and the INT2 rows keep the INT4
+// row stride (K/2 bytes), the second half of every row left as it was.  The
+// INT2 bytes of group g land on bytes [g*group/4, (g+1)*group/4) of the row,
+// which hold INT4 codes of groups below g only.  So one CTA per row converts
+// the row's groups in chunks, in increasing order, staging each chunk's INT4
+// words in shared memory before writing any of its INT2 words: every INT4
+// byte is read before it can be overwritten.  The staging loads are plain
+// L2 loads (the same kernel writes this memory).
+constexpr int kIpThreads = 128;
+constexpr int kIpStageBytes = 32768;
+
+struct RqInPlaceLaunch {
+  RqProblem p[kMaxRequantProblems];  // W2 and W4 address the same words
+  long long rstart[kMaxRequantProblems];  // first row of each problem in the launch
+  int G[kMaxRequantProblems];             // groups per row
+  int count;
+  int T;      // chunks of 32 codes per group
+  int chunk;  // groups per staged pass
+};
+
+__global__ void __launch_bounds__(kIpThreads) requant_in_place_kernel(const __grid_constant__ RqInPlaceLaunch L) {
+  extern __shared__ uint4 stage[];  // [chunk][T]
+  const long long row = blockIdx.x;
+  int p = 0;
+#pragma unroll 1
+  while (p + 1 < L.count && row >= L.rstart[p + 1]) ++p;
+  const RqProblem& pr = L.p[p];
+  const long long n = row - L.rstart[p];
+  const int G = L.G[p], T = L.T;
+  const uint4* src = pr.W4 + n * G * T;                       // the row's INT4 words, T chunks per group
+  uint2* dst = pr.W2 + n * (long long)G * T * 2;              // the same row start (INT4 stride)
+#pragma unroll 1
+  for (int g0 = 0; g0 < G; g0 += L.chunk) {
+    const int ng = min(L.chunk, G - g0);
+    for (int i = threadIdx.x; i < ng * T; i += kIpThreads) stage[i] = __ldcg(src + (long long)g0 * T + i);
+    __syncthreads();  // the chunk's INT4 words are staged before any of its INT2 words are written
+    for (int j = threadIdx.x; j < ng; j += kIpThreads) {
+      const long long gi = n * G + g0 + j;
+      const uint32_t sz = static_cast<uint32_t>(pr.s4[gi]) | (static_cast<uint32_t>(pr.z4[gi]) << 16);
+      rq_group<0, true>(nullptr, stage + j * T, T, sz, dst + (long long)(g0 + j) * T, pr.s2 + gi, pr.z2 + gi);
+    }
+    __syncthreads();  // the stage is read before the next chunk replaces it
+  }
+}
+
 }  // namespace
+
+tlq_status launch_requant_in_place(const RequantArgs* a, int count, int group, cudaStream_t stream) {
+  RqInPlaceLaunch L = {};
+  long long rows = 0;
+  for (int i = 0; i < count; ++i) {
+    L.p[i] = RqProblem{reinterpret_cast<const uint4*>(a[i].W4), a[i].s4, a[i].z4, reinterpret_cast<uint2*>(a[i].W2),
+                       a[i].s2, a[i].z2, 0};
+    L.rstart[i] = rows;
+    L.G[i] = a[i].K / group;
+    rows += a[i].N;
+  }
+  L.count = count;
+  L.T = group / 32;
+  L.chunk = kIpStageBytes / (L.T * 16);
+  if (L.chunk < 1) L.chunk = 1;
+  if (rows == 0) return TLQ_OK;
+  if (rows > 0x7FFFFFFFll) return set_error(TLQ_EUNSUPPORTED, "requant in place: %lld rows in one launch", rows);
+  if (L.T * 16 > 48 * 1024) return set_error(TLQ_EUNSUPPORTED, "requant in place: group %d is too large", group);
+  int gmax = 1;
+  for (int i = 0; i < count; ++i) gmax = L.G[i] > gmax ? L.G[i] : gmax;
+  const size_t smem = (size_t)(L.chunk < gmax ? L.chunk : gmax) * L.T * 16;
+  requant_in_place_kernel<<<(unsigned)rows, kIpThreads, smem, stream>>>(L);
+  return cuda_error(cudaGetLastError(), "requant in place: launch");
+}
 
 tlq_status launch_requant(const RequantArgs* a, int count, int group, cudaStream_t stream) {
   RqLaunch L = {};

@@ -31,6 +31,7 @@ size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 extern "C" tlq_status tl_loop_block_forward_static_scratch(float* x, const tl_block* block, int L, int M,
                                                            void* stream) {
   using tlq::set_error;
+  tlq::clear_error();
   if (!x || !block) return set_error(TLQ_EINVAL, "tl_loop_block_forward_static_scratch: null x or block");
   if (M < 1) return set_error(TLQ_EINVAL, "tl_loop_block_forward_static_scratch: M=%d (must be >= 1)", M);
   const int D = block->D, F = block->up.N;
@@ -67,5 +68,7 @@ extern "C" tlq_status tl_loop_block_forward_static_scratch(float* x, const tl_bl
   b.qkv_out = reinterpret_cast<uint16_t*>(base + hb);
   b.o_out = reinterpret_cast<uint16_t*>(base + hb + qb);
   b.up_out = reinterpret_cast<uint16_t*>(base + hb + qb + ob);
-  return tlq::loop_block_forward_no_alloc(x, &b, L, M, "tl_loop_block_forward_static_scratch", stream);
+  b.workspace = nullptr;  // no k split: that would need a workspace
+  b.workspace_bytes = 0;
+  return tlq::loop_block_forward_named(x, &b, L, M, "tl_loop_block_forward_static_scratch", stream);
 }
