@@ -490,6 +490,7 @@ __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const Sched* tab
       load_acts<BITS, NT>(nu, warp, nx, ny);
     const int slot = warp * kSPW + (consumed % kSPW);
     if (ok) ok = mbar_wait(&full[slot], (consumed / kSPW) & 1, 0x112);
+    __syncwarp();  // the lanes leave the wait separately; the MMAs below are warp-collective
     if (kb < ur.nkb_full)
       kblock<BITS, RGW, NTP, SPANQ, true>(ur, kb, ring_base + (uint32_t)slot * STAGE_BYTES, woff, g, ax, ay, tot);
     else
