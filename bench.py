@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 DECODE_MS = (1, 4, 16)
+TRIALS = 7  # timed trials of the headline step (each exactly --steps steps); the median is reported
 PREFILL_MS = (128, 512, 2048)
 PROJ = synth.PROJ_ORDER
 
@@ -116,6 +117,56 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# peaks measured in the same run: dense FP16 tensor-core throughput (cuBLAS)
+# for the tensor-core kernel, L2 read bandwidth for the loop block
+# ---------------------------------------------------------------------------
+def measure_fp16_peak(torch, n=8192, reps=10):
+    """Dense FP16 GEMM n^3 through torch.matmul (cuBLAS, FP32 accumulation):
+    best of `reps` timed launches, TFLOP/s."""
+    a = torch.randn((n, n), device="cuda").half()
+    b = torch.randn((n, n), device="cuda").half()
+    c = torch.empty((n, n), device="cuda", dtype=torch.float16)
+    for _ in range(3):
+        torch.matmul(a, b, out=c)
+    torch.cuda.synchronize()
+    best = 1e30
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b, out=c)
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del a, b, c
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+
+
+def measure_l2_read(tlq, torch, l2_bytes, reps=20, trials=10):
+    """L2 read bandwidth: tl_probe_read_bandwidth over a buffer of a third of
+    the L2 (it stays resident), `reps` passes per launch; best of `trials`
+    launches, GB/s."""
+    nbytes = (l2_bytes // 3) // 4096 * 4096
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device="cuda")
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sink = torch.empty(2 * sms * 512, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        tlq.tl_probe_read_bandwidth(buf, reps, sink)
+    torch.cuda.synchronize()
+    best = 1e30
+    for _ in range(trials):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        tlq.tl_probe_read_bandwidth(buf, reps, sink)
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del buf, sink
+    return nbytes * reps / (best * 1e-3) / 1e9, nbytes
 
 
 # ---------------------------------------------------------------------------
@@ -371,6 +422,8 @@ def run_tlq(args, rank, world, dist):
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     l2 = getattr(props, "L2_cache_size", 128 << 20)
     peaks = measured_peaks()
+    peaks["fp16"] = measure_fp16_peak(torch)
+    peaks["l2_read"], l2_probe_bytes = measure_l2_read(tlq, torch, l2)
     result = {}
 
     # ---- headline: INT4 decode, D = 2048 projections, M in {1, 4, 16} ----
@@ -379,9 +432,13 @@ def run_tlq(args, rank, world, dist):
     wl4 = Workload(tlq, torch, 4, DECODE_MS, synth.SHAPES, ncopy)
     phases = ncopy // len(DECODE_MS)
     graphs = capture_steps(torch, wl4, phases)
+    # TRIALS trials of exactly `steps` timed steps each (every one bracketed by
+    # barrier + synchronize); the line reports the median trial
     with ClockSampler(torch.cuda.current_device()) as clk:
-        ms = time_graphs(torch, graphs, args.steps, args.warmup, dist)
+        trial_ms = [time_graphs(torch, graphs, args.steps, args.warmup if t == 0 else 3, dist)
+                    for t in range(TRIALS)]
     clocks = clk.summary()
+    ms = statistics.median(trial_ms)
     ms_max = ms
     if dist is not None:
         t = torch.tensor([ms], dtype=torch.float64, device="cuda")
@@ -440,7 +497,7 @@ def run_tlq(args, rank, world, dist):
     result["prefill"] = run_prefill(tlq, torch, peaks)
 
     # ---- secondary: loop block ----
-    result["loop_block"] = run_loop_block(tlq, torch)
+    result["loop_block"] = run_loop_block(tlq, torch, peaks)
 
     # ---- secondary: chunked prefill of the loop block ----
     result["chunked_prefill"] = run_chunked_prefill(tlq, torch)
@@ -485,6 +542,10 @@ def run_tlq(args, rank, world, dist):
                      "frac": round(achieved / peaks["hbm"], 3), "traffic": traffic,
                      "peak_source": peaks["src"],
                      "kernel": "decode_kernel (%d launch(es) per step; traffic per step)" % wl4.batched_launches},
+        "trials_ms_per_step": [round(t / args.steps, 6) for t in trial_ms],
+        "measured_in_run": {"fp16_dense_tflops": round(peaks["fp16"], 1), "l2_read_gbs": round(peaks["l2_read"], 1),
+                            "how": "torch.matmul fp16 8192^3 best of 10; tl_probe_read_bandwidth over %d MB "
+                                   "(L2-only loads, 20 passes) best of 10" % (l2_probe_bytes >> 20)},
         "per_gemm": per_gemm,
         "separate_launches": separate,
         "clocks": clocks,
@@ -492,8 +553,25 @@ def run_tlq(args, rank, world, dist):
         "gpu_launches": args.steps * wl4.batched_launches,
     }
     line.update(result)
+    # the other two rooflines of the metric: the tensor-core kernel (prefill
+    # step at M = 2048, four projections) against the dense FP16 peak measured
+    # above, and the loop block (INT4, M = 1, L = 16: weights re-read from L2)
+    # against the L2 read bandwidth measured above
+    pf = result.get("prefill", {}).get("M2048")
+    if pf:
+        line["roofline"]["prefill"] = {
+            "bound": "tensor", "achieved": pf["TFLOPs"], "peak": round(peaks["fp16"], 1), "unit": "TFLOP/s",
+            "frac": round(pf["TFLOPs"] / peaks["fp16"], 3), "traffic": None, "peak_source": "measured in this run",
+            "kernel": "prefill_kernel (INT4, M = 2048, QKV/O/UP/DOWN in one batched call)",
+            "frac_by_M": {k: v["frac_of_fp16_peak"] for k, v in result["prefill"].items()}}
+    lb = result.get("loop_block", {}).get("int4_M1_L16")
+    if lb:
+        line["roofline"]["loop_block"] = {
+            "bound": "l2", "achieved": lb["eff_GBps"], "peak": round(peaks["l2_read"], 1), "unit": "GB/s",
+            "frac": lb["frac_of_l2_read"], "traffic": None, "peak_source": "measured in this run",
+            "kernel": "loop block, INT4, M = 1, L = 16 (decode_kernel + rmsnorm_kernel, 5 launches per iteration)"}
     if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl4)
+        line["cpu_baseline"], line["cpu_baseline_1thread"] = cpu_baseline(wl4)
     return line
 
 
@@ -540,14 +618,15 @@ def run_prefill(tlq, torch, peaks):
             t = time_graphs(torch, gs, steps, 5)
             tf = wl.step_flops * steps / (t * 1e-3) / 1e12
             out["M%d" % M] = {"TFLOPs": round(tf, 1), "ms_per_step": round(t / steps, 4),
-                              "frac_of_bf16_peak": round(tf / peaks["bf16"], 3)}
+                              "frac_of_fp16_peak": round(tf / peaks["fp16"], 3),
+                              "launches_per_step": wl.batched_launches}
             del wl, gs
     except tlq.TLQError as e:
         return {"unavailable": str(e)}
     return out
 
 
-def run_loop_block(tlq, torch):
+def run_loop_block(tlq, torch, peaks):
     """The shared-weight block applied L times from one CUDA graph: the ReLU
     block (four weights) and the pages' five-weight SwiGLU block."""
     out = {}
@@ -593,10 +672,12 @@ def run_loop_block(tlq, torch):
                         e1.synchronize()
                         ms = e0.elapsed_time(e1) / reps
                         key = ("" if kind == "relu" else "swiglu_") + "int%d_M%d_L%d" % (bits, M, L)
+                        eff = L * wbytes / (ms * 1e-3) / 1e9
                         out[key] = {
                             "ms": round(ms, 4), "us_per_iter": round(ms * 1e3 / L, 2),
-                            "eff_GBps": round(L * wbytes / (ms * 1e-3) / 1e9, 1),
-                            "TFLOPs": round(L * 2 * M * macs / (ms * 1e-3) / 1e12, 2)}
+                            "eff_GBps": round(eff, 1), "frac_of_l2_read": round(eff / peaks["l2_read"], 3),
+                            "TFLOPs": round(L * 2 * M * macs / (ms * 1e-3) / 1e12, 2),
+                            "frac_of_fp16_peak": round(L * 2 * M * macs / (ms * 1e-3) / 1e12 / peaks["fp16"], 4)}
                         del g
                     del blk, proj
     except tlq.TLQError as e:
@@ -759,9 +840,11 @@ def run_requant(tlq, torch, peaks, l2):
         return {"unavailable": str(e)}
 
 
-def cpu_baseline(wl):
-    """The CPU oracle as it stands (single thread) on one full headline step,
-    on the same inputs (weights of rotation copy 0)."""
+def cpu_baseline(wl, min_s=3.0):
+    """The CPU oracle as it stands on one full headline step (12 GEMMs, the
+    weights of rotation copy 0): on every host core (its output rows shared
+    out by OpenMP; steps repeated until at least min_s seconds), and on one
+    thread (one step)."""
     import oracle
 
     cp = wl.copies[0]
@@ -770,14 +853,28 @@ def cpu_baseline(wl):
         W, s, z = cp[name]
         host[name] = (W.cpu().numpy().view(np.uint32), s.cpu().numpy(), z.cpu().numpy())
     As = {k: v.cpu().numpy() for k, v in wl.A.items()}
-    t0 = time.perf_counter()
-    for M in wl.Ms:
-        for name in wl.shapes:
-            W, s, z = host[name]
-            oracle.quant_gemm(As[M, name], W, s, z, wl.bits, wl.group)
-    dt = time.perf_counter() - t0
-    return {"value": round(wl.step_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "one full step (12 GEMMs: 4 projections x M = 1, 4, 16), %.1f s" % dt}
+
+    def step():
+        for M in wl.Ms:
+            for name in wl.shapes:
+                W, s, z = host[name]
+                oracle.quant_gemm(As[M, name], W, s, z, wl.bits, wl.group)
+
+    out = []
+    for threads in (os.cpu_count() or 1, 1):
+        cores = oracle.set_threads(threads)
+        n, t0 = 0, time.perf_counter()
+        while True:
+            step()
+            n += 1
+            dt = time.perf_counter() - t0
+            if threads == 1 or dt >= min_s:
+                break
+        out.append({"value": round(wl.step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                    "sample": "%d full step(s) (12 GEMMs: 4 projections x M = 1, 4, 16), %.1f s on %d thread(s)"
+                              % (n, dt, cores)})
+    oracle.set_threads(os.cpu_count() or 1)
+    return out[0], out[1]
 
 
 # ---------------------------------------------------------------------------
@@ -786,9 +883,11 @@ def cpu_baseline(wl):
 def run_reference(args, budget_s=60.0):
     """Each reference step is the M = 1 slice of the headline step (4 GEMMs),
     restricted to the first rows of every projection so that the whole run
-    takes about ``budget_s`` seconds of single-thread CPU time."""
+    takes about ``budget_s`` seconds on the host's cores (the oracle shares
+    its output rows out over all of them)."""
     import oracle
 
+    cores = oracle.set_threads(os.cpu_count() or 1)
     rng = synth.rng_for(0)
     host = {}
     for name, (N, K) in synth.SHAPES.items():
@@ -827,7 +926,7 @@ def run_reference(args, budget_s=60.0):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same distributions)",
         "config": {"workload": "INT4 decode, group 128, QKV 2048->6144 / O 2048->2048 / UP 2048->8192 / DOWN "
                                "8192->2048; reference steps are bounded samples (M = 1 rows)"},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -505,6 +505,18 @@ tlq_status tl_swiglu_block_to_int2(tl_swiglu_block* block, const tl_qproj* dst, 
 tlq_status tl_loop_block_forward_static_scratch(float* x, const tl_block* block, int L, int M, void* stream);
 
 /*
+ * tl_probe_read_bandwidth -- a measurement helper, no operation of the pages:
+ * `reps` passes of 16-byte L2-only loads (ld.global.cg) over buf, folded into
+ * one word per thread of sink (2 x SMs x 512 words, caller-owned).  With buf
+ * small enough to stay in L2 it measures the L2 read bandwidth that bounds
+ * the loop block (its packed weights fit in L2 and are re-read every
+ * iteration); the benchmark times it with CUDA events.
+ *   buf    device buffer, 16-byte aligned; bytes a positive multiple of 16.
+ * Returns TLQ_OK, TLQ_EINVAL or TLQ_ECUDA.
+ */
+tlq_status tl_probe_read_bandwidth(const void* buf, size_t bytes, int reps, uint32_t* sink, void* stream);
+
+/*
  * Synchronize `stream` and report the device status word: TLQ_OK, or
  * TLQ_ETIMEOUT if a kernel gave up on a bounded wait since the last
  * tl_reset_status().  Also returns TLQ_ECUDA on an asynchronous CUDA error.

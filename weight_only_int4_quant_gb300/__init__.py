@@ -24,7 +24,7 @@ __all__ = [
     "interleave_rows", "SwiGLUBlock", "tl_dequant_fp16", "dequant_fp16",
     "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked", "tl_quant_gemm_batched_host",
     "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws", "tl_loop_block_to_int2",
-    "tl_swiglu_block_to_int2", "gemm_workspace", "requant_descs",
+    "tl_swiglu_block_to_int2", "gemm_workspace", "requant_descs", "tl_probe_read_bandwidth",
 ]
 
 # every symbol include/tlq.h declares
@@ -35,7 +35,7 @@ EXPORTED = (
     "tl_requant_int4_to_int2_batched", "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward",
     "tl_dequant_fp16", "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
     "tl_quant_gemm_batched_host", "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws",
-    "tl_loop_block_to_int2", "tl_swiglu_block_to_int2",
+    "tl_loop_block_to_int2", "tl_swiglu_block_to_int2", "tl_probe_read_bandwidth",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -132,6 +132,7 @@ def load():
             "tl_quant_gemm_swiglu_ws": ([P, P, P, P, P, I, I, I, I, I, P, ctypes.c_size_t, P], I),
             "tl_loop_block_to_int2": ([ctypes.POINTER(_Block), ctypes.POINTER(_QProj), P], I),
             "tl_swiglu_block_to_int2": ([ctypes.POINTER(_SwigluBlock), ctypes.POINTER(_QProj), P], I),
+            "tl_probe_read_bandwidth": ([P, ctypes.c_size_t, I, P, P], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -409,6 +410,13 @@ def tl_loop_block_forward_static_scratch(x, block: "LoopBlock", L: int, stream=N
 
     _raise_if(load().tl_loop_block_forward_static_scratch(_dev(x, (torch.float32,), "x"), ctypes.byref(block._c), L,
                                                           x.shape[0], _stream(stream)))
+
+
+def tl_probe_read_bandwidth(buf, reps: int, sink, stream=None) -> None:
+    """reps passes of L2-only 16-byte loads over buf (a CUDA tensor); sink is
+    an int32 CUDA tensor of at least 2 * SMs * 512 elements."""
+    _raise_if(load().tl_probe_read_bandwidth(buf.data_ptr(), buf.numel() * buf.element_size(), reps,
+                                             sink.data_ptr(), _stream(stream)))
 
 
 def tl_check_status(stream=None) -> None:
