@@ -416,10 +416,29 @@ typedef struct {
  *   x      FP32 [M][D] device array, updated in place.
  *   block  HOST pointer to a tl_block describing device buffers.
  *   L >= 0 (L = 0 is a no-op); M >= 1.
- * With TLQ_LOG=1 in the environment the first call on a device prints
- * whether the block's packed weights fit in L2 and the kernel choice.
+ * L2 residency (see tl_loop_block_l2_plan): the projections the plan keeps
+ * resident are streamed with an evict-last policy, the others evict-first.
+ * With TLQ_LOG=1 in the environment the first call prints the plan.
  */
 tlq_status tl_loop_block_forward(float* x, const tl_block* block, int L, int M, void* stream);
+
+/*
+ * tl_loop_block_l2_plan -- the loop block's L2 residency plan ("Model",
+ * "Returns", item 4: auto tile sizing reports loop-block vs L2 cache
+ * residency).  The block's weights (packed words plus FP16 scales and zeros)
+ * are re-read every iteration; the plan keeps projections resident, in
+ * iteration order (qkv, o, up, down), while their running total fits a
+ * budget of half the device's L2, and only when L > 1.
+ *   block          HOST pointer; only the projections' N and K, bits and
+ *                  group are read (no device memory is touched).
+ *   resident_mask  out: bit i set when projection i is kept resident.
+ *   weight_bytes, budget_bytes  out (may be NULL): the block's weight bytes
+ *                  and the budget.
+ * The SwiGLU block uses the same plan over (qkv, o, gate_up, down).
+ * Returns TLQ_OK or TLQ_EINVAL.
+ */
+tlq_status tl_loop_block_l2_plan(const tl_block* block, int L, int* resident_mask, size_t* weight_bytes,
+                                 size_t* budget_bytes);
 
 /*
  * tl_swiglu_block_forward -- the five-weight SwiGLU loop block applied L times

@@ -259,6 +259,47 @@ def test_tier_switch_rejects_bad_blocks(clib):
     assert blk.bits == 4
 
 
+def test_loop_block_l2_plan(clib):
+    """The residency plan keeps the block's projections resident in
+    iteration order while their running byte total fits the budget, and
+    none when the block runs once; a block too large for the budget keeps
+    only the prefix that fits.  Host-only: the query reads shapes, not
+    device memory."""
+    import weight_only_int4_quant_gb300 as tlq
+
+    def plan(D, F, bits, group, L):
+        blk = tlq._Block()
+        for name, (N, K) in (("qkv", (3 * D, D)), ("o", (D, D)), ("up", (F, D)), ("down", (D, F))):
+            setattr(blk, name, tlq._QProj(1 << 20, 2 << 20, 3 << 20, N, K, 0))
+        blk.bits, blk.group, blk.D = bits, group, D
+        m, wb, bb = ctypes.c_int(), ctypes.c_size_t(), ctypes.c_size_t()
+        assert clib.tl_loop_block_l2_plan(ctypes.byref(blk), L, ctypes.byref(m), ctypes.byref(wb),
+                                          ctypes.byref(bb)) == tlq.TLQ_OK
+        sizes = [N * K * bits // 8 + 4 * N * (K // group) for (N, K) in ((3 * D, D), (D, D), (F, D), (D, F))]
+        return m.value, wb.value, bb.value, sizes
+
+    # the D = 2048 block: 26.7 MB (INT4 g128) / 15.7 MB (INT2 g64)
+    for bits, group, total in ((4, 128, 26738688), (2, 64, 15728640)):
+        m, wb, bb, sizes = plan(2048, 8192, bits, group, 8)
+        assert wb == total == sum(sizes)
+        expect = 0
+        for i in range(4):
+            if sum(sizes[:i + 1]) <= bb:
+                expect |= 1 << i
+            else:
+                break
+        assert m == expect
+        assert plan(2048, 8192, bits, group, 1)[0] == 0  # one iteration: nothing to keep
+    # a block four times wider: only a prefix fits (or none), never a gap
+    m, wb, bb, sizes = plan(8192, 32768, 4, 128, 8)
+    assert wb > bb and m in (0, 1, 3, 7)
+    k = bin(m).count("1")
+    assert sum(sizes[:k]) <= bb and (k == 4 or sum(sizes[:k + 1]) > bb)
+    blk = tlq._Block()
+    blk.bits = 3
+    assert clib.tl_loop_block_l2_plan(ctypes.byref(blk), 2, ctypes.byref(ctypes.c_int()), None, None) == tlq.TLQ_EINVAL
+
+
 def test_library_sources_allocate_nothing():
     """The library makes no device or host-pinned allocation anywhere: every
     buffer is the caller's (the allocation-free entry point's static array is

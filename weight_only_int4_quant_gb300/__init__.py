@@ -25,6 +25,7 @@ __all__ = [
     "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked", "tl_quant_gemm_batched_host",
     "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws", "tl_loop_block_to_int2",
     "tl_swiglu_block_to_int2", "gemm_workspace", "requant_descs", "tl_probe_read_bandwidth",
+    "tl_loop_block_l2_plan",
 ]
 
 # every symbol include/tlq.h declares
@@ -35,7 +36,7 @@ EXPORTED = (
     "tl_requant_int4_to_int2_batched", "tl_quant_gemm_swiglu", "tl_interleave_rows", "tl_swiglu_block_forward",
     "tl_dequant_fp16", "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
     "tl_quant_gemm_batched_host", "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws",
-    "tl_loop_block_to_int2", "tl_swiglu_block_to_int2", "tl_probe_read_bandwidth",
+    "tl_loop_block_to_int2", "tl_swiglu_block_to_int2", "tl_probe_read_bandwidth", "tl_loop_block_l2_plan",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -133,6 +134,8 @@ def load():
             "tl_loop_block_to_int2": ([ctypes.POINTER(_Block), ctypes.POINTER(_QProj), P], I),
             "tl_swiglu_block_to_int2": ([ctypes.POINTER(_SwigluBlock), ctypes.POINTER(_QProj), P], I),
             "tl_probe_read_bandwidth": ([P, ctypes.c_size_t, I, P, P], I),
+            "tl_loop_block_l2_plan": ([ctypes.POINTER(_Block), I, ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], I),
         }
         for name, (args, res) in sigs.items():
             f = getattr(lib, name)
@@ -417,6 +420,20 @@ def tl_probe_read_bandwidth(buf, reps: int, sink, stream=None) -> None:
     an int32 CUDA tensor of at least 2 * SMs * 512 elements."""
     _raise_if(load().tl_probe_read_bandwidth(buf.data_ptr(), buf.numel() * buf.element_size(), reps,
                                              sink.data_ptr(), _stream(stream)))
+
+
+def tl_loop_block_l2_plan(block, L: int):
+    """The block's L2 residency plan: (resident projection mask, weight
+    bytes, budget bytes); bit i = projection i of (qkv, o, up / gate_up,
+    down) streamed evict-last."""
+    c = block._c
+    if isinstance(c, _SwigluBlock):  # same plan over (qkv, o, gate_up, down)
+        b = _Block()
+        b.qkv, b.o, b.up, b.down, b.bits, b.group, b.D = c.qkv, c.o, c.gate_up, c.down, c.bits, c.group, c.D
+        c = b
+    mask, wb, bb = ctypes.c_int(), ctypes.c_size_t(), ctypes.c_size_t()
+    _raise_if(load().tl_loop_block_l2_plan(ctypes.byref(c), L, ctypes.byref(mask), ctypes.byref(wb), ctypes.byref(bb)))
+    return mask.value, wb.value, bb.value
 
 
 def tl_check_status(stream=None) -> None:

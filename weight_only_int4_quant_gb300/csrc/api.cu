@@ -581,6 +581,32 @@ struct BlockSpec {
   size_t ws_bytes;
 };
 
+// The loop block's L2 residency plan: bytes of packed weights and scales /
+// zeros per projection, a budget of half the L2 (GB300 measured: re-reads of
+// up to ~80 MB of the 126 MB L2 run at full L2 bandwidth; the other half
+// leaves room for activations and other streams), and the projections kept
+// resident: the longest run from the first, in iteration order, that fits.
+struct L2Plan {
+  int mask;  // bit i: projection i (qkv, o, ff, down) streamed evict-last
+  size_t weight_bytes, budget_bytes;
+};
+
+L2Plan plan_l2(const tl_qproj* const* proj, int bits, int group, int L) {
+  L2Plan pl{0, 0, (size_t)device_info().l2_bytes / 2};
+  const int cpw = 32 / bits;
+  size_t cum = 0;
+  bool fits = true;
+  for (int i = 0; i < 4; ++i) {
+    const size_t bytes =
+        (size_t)proj[i]->N * (proj[i]->K / cpw) * 4 + (size_t)proj[i]->N * (proj[i]->K / group) * 4;
+    pl.weight_bytes += bytes;
+    cum += bytes;
+    fits = fits && cum <= pl.budget_bytes;
+    if (fits && L > 1) pl.mask |= 1 << i;
+  }
+  return pl;
+}
+
 tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_t stream) {
   const char* who = b.who;
   if (L < 0) return set_error(TLQ_EINVAL, "%s: L=%d (must be >= 0)", who, L);
@@ -612,21 +638,27 @@ tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_
   if (!aligned16(b.h) || !aligned16(b.qkv_out) || !aligned16(b.o_out) || !aligned16(b.act_out))
     return set_error(TLQ_EINVAL, "%s: scratch buffers must be 16-byte aligned", who);
 
-  // The block's weights are re-read every iteration: when they fit in half
-  // the L2 they are streamed with an evict-last policy so that iterations
-  // after the first read them from L2 ("Model", "Returns", item 4: auto tile
-  // sizing reports loop-block vs L2 residency).
-  const int cpw = 32 / b.bits;
-  size_t wb = 0;
-  for (int i = 0; i < 4; ++i)
-    wb += (size_t)b.proj[i]->N * (b.proj[i]->K / cpw) * 4 + (size_t)b.proj[i]->N * (b.proj[i]->K / b.group) * 4;
-  const bool keep = L > 1 && wb <= (size_t)device_info().l2_bytes / 2;
+  // The block's weights are re-read every iteration ("Model", "Returns",
+  // item 4: auto tile sizing reports loop-block vs L2 residency): the plan
+  // keeps the projections resident with an L2 evict-last policy in iteration
+  // order while they fit the L2 budget, and streams the rest evict-first so
+  // they do not push the resident ones out.
+  const L2Plan plan = plan_l2(b.proj, b.bits, b.group, L);
   static std::once_flag logged;
   if (log_enabled()) {
     std::call_once(logged, [&] {
-      fprintf(stderr, "[tlq] loop block: INT%d group %d, packed weights + scales/zeros %.1f MB, L2 %.1f MB -> %s\n",
-              b.bits, b.group, wb / 1e6, device_info().l2_bytes / 1e6,
-              keep ? "kept in L2 (evict-last) after the first iteration" : "streamed from HBM every iteration");
+      static const char* nm[4] = {"qkv", "o", "ff", "down"};
+      char kept[64] = "", streamed[64] = "";
+      for (int i = 0; i < 4; ++i) {
+        char* dst = ((plan.mask >> i) & 1) ? kept : streamed;
+        strncat(dst, nm[i], sizeof(kept) - strlen(dst) - 2);
+        strncat(dst, " ", sizeof(kept) - strlen(dst) - 1);
+      }
+      fprintf(stderr,
+              "[tlq] loop block: INT%d group %d, packed weights + scales/zeros %.1f MB, L2 %.1f MB, budget %.1f MB: "
+              "resident (evict-last) [ %s], streamed [ %s]\n",
+              b.bits, b.group, plan.weight_bytes / 1e6, device_info().l2_bytes / 1e6, plan.budget_bytes / 1e6, kept,
+              streamed);
     });
   }
 
@@ -635,7 +667,7 @@ tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_
     a.bits = b.bits;
     a.group = b.group;
     a.M = M;
-    a.l2_keep = keep ? 1 : 0;
+    a.l2_keep = (plan.mask >> (p == b.proj[0] ? 0 : p == b.proj[1] ? 1 : p == b.proj[2] ? 2 : 3)) & 1;
     a.ldw = p->ldw;
     a.ws = b.ws;
     a.ws_bytes = b.ws ? b.ws_bytes : 0;
@@ -665,6 +697,20 @@ tlq_status block_forward(float* x, const BlockSpec& b, int L, int M, cudaStream_
   return TLQ_OK;
 }
 }  // namespace
+
+tlq_status tl_loop_block_l2_plan(const tl_block* b, int L, int* resident_mask, size_t* weight_bytes,
+                                 size_t* budget_bytes) {
+  g_msg[0] = 0;
+  if (!b || !resident_mask) return set_error(TLQ_EINVAL, "tl_loop_block_l2_plan: null pointer");
+  if (b->bits != 4 && b->bits != 2) return set_error(TLQ_EINVAL, "tl_loop_block_l2_plan: bits=%d", b->bits);
+  if (b->group < 32 || b->group % 32) return set_error(TLQ_EINVAL, "tl_loop_block_l2_plan: group=%d", b->group);
+  const tl_qproj* proj[4] = {&b->qkv, &b->o, &b->up, &b->down};
+  const L2Plan pl = plan_l2(proj, b->bits, b->group, L);
+  *resident_mask = pl.mask;
+  if (weight_bytes) *weight_bytes = pl.weight_bytes;
+  if (budget_bytes) *budget_bytes = pl.budget_bytes;
+  return TLQ_OK;
+}
 
 tlq_status tl_loop_block_forward(float* x, const tl_block* b, int L, int M, void* stream) {
   g_msg[0] = 0;
