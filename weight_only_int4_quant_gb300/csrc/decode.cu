@@ -965,9 +965,8 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
 // (N = 2048, K = 2048) is fastest with 32-row units (2.64 against 3.26 us at
 // M = 1), DOWN (N = 2048, K = 8192) with 16-row units (6.56 against 9.45 us);
 // QKV, UP and the batched decode step keep 64.  Launches whose weights are
-// kept in L2 (the loop block) also keep 64: they are short, and the next
-// kernel's early start on the SMs they leave idle matters more (the loop
-// block at M = 1 measured 5 % slower, INT2 14 %, with the smaller units).
+// kept in L2 (the loop block) also keep 64 (the next kernel's early start on
+// the SMs they leave idle matters more), except the INT4 DOWN projection.
 // The unit height does not change any result: every row's sums are formed
 // the same way.  TLQ_DECODE_ROWS=16|32|64 forces it.
 template <int BITS>
@@ -976,8 +975,12 @@ int decode_rgw(const GemmArgs* a, int count) {
     const int r = atoi(e);
     if (r == 16 || r == 32 || r == 64) return r / 16;
   }
+  // launches whose weights stay in L2 (the loop block): 64-row units, except
+  // a single INT4 problem with long rows (the block's DOWN projection), which
+  // would leave most SMs idle: 16-row units (INT4 M = 1 blocks 8-10 % faster
+  // per iteration, measured; INT2 unchanged, so it keeps 64)
   for (int i = 0; i < count; ++i)
-    if (a[i].l2_keep) return 4;
+    if (a[i].l2_keep) return (count == 1 && BITS == 4 && a[i].K >= 4096) ? 1 : 4;
   const int sms = device_info().sms;
   bool long_rows = true;
   for (int i = 0; i < count; ++i) long_rows &= (a[i].K + Fmt<BITS>::KBLK - 1) / Fmt<BITS>::KBLK >= 32;
