@@ -163,7 +163,13 @@ typedef struct {
  * on up to three library-owned streams per caller stream, forked from
  * `stream` and joined back with events (so the call's work still completes in
  * `stream` order, and a graph capture of `stream` records the fork and join).
- * Results equal `count` separate tl_quant_gemm calls.  Same source passages as tl_quant_gemm; batching is a
+ * When two to four such launches run at once, their token tiles per CTA and
+ * k splits are planned together for the shared GPU (within the workspace
+ * each descriptor gives); otherwise each is planned as a single call would
+ * plan it.  Results equal `count` separate tl_quant_gemm_ws calls within the
+ * layer's tolerance, and M <= 16 problems bit for bit (a tensor-core
+ * problem's k split, and so its FP32 summation order, may differ from the
+ * one a single call picks); repeated calls give the same bits.  Same source passages as tl_quant_gemm; batching is a
  * launch-overhead measure of this library (the layers of one decode step that
  * do not depend on each other, or several requests at once).
  *   descs  HOST array of `count` descriptors (count >= 0; 0 is a no-op).

@@ -397,6 +397,35 @@ def test_batched_prefill_side_streams_in_a_graph(lib):
         assert_close(p["C"].cpu().numpy()[rows], ref, "side streams M%d N%d K%d" % (M, N, K))
 
 
+@pytest.mark.parametrize("M", [128, 512])
+def test_batched_prefill_step_full_size(lib, M):
+    """The four D = 2048 projections at M = 128 / 512 in one batched call, each
+    with the workspace its own plan asks for: the launches run side by side
+    with token tiles and k splits planned for the shared GPU (at M = 128 the
+    DOWN projection alone keeps a k split).  16 whole rows per problem against
+    the oracle; a second call gives the same bits."""
+    specs = [(M, N, K, 4, 128) for (N, K) in synth.SHAPES.values()]
+    probs = _problems(specs, seed=50)
+    for p, (M_, N, K, bits, group) in zip(probs, specs):
+        p["ws"] = lib.gemm_workspace(M_, N, K, bits, group)
+    descs = lib.gemm_descs([(p["A"], p["W"], p["s"], p["z"], p["C"], 4, 128, p["ws"]) for p in probs])
+    lib.tl_quant_gemm_batched(descs)
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+    first = [p["C"].clone() for p in probs]
+    lib.tl_quant_gemm_batched(descs)
+    torch.cuda.synchronize()
+    for p, f in zip(probs, first):
+        assert torch.equal(p["C"].view(torch.int16), f.view(torch.int16))
+    rng = np.random.default_rng(M)
+    for p, (M_, N, K, bits, group) in zip(probs, specs):
+        rows = sample_rows(M, 16, rng)
+        c = p["case"]
+        ref = oracle.quant_gemm(c["A"][rows], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
+                                group)
+        assert_close(p["C"].cpu().numpy()[rows], ref, "batched step M%d N%d K%d" % (M, N, K))
+
+
 def test_batched_mixed_bits_and_paths(lib):
     specs = [(1, 256, 1024, 4, 128), (9, 136, 448, 2, 64), (40, 264, 512, 4, 128), (3, 512, 2048, 2, 128),
              (16, 64, 4096, 4, 4096), (130, 256, 1024, 2, 64)]

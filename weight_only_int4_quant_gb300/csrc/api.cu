@@ -437,14 +437,29 @@ tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_
     for (int k = 0; k < used && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(ss->s[k], ss->fork, 0);
     if (e != cudaSuccess) return cuda_error(e, "tl_quant_gemm_batched: fork");
   }
+  // up to four problems all run at once (one per stream): their token tiles
+  // and k splits are chosen together for the shared GPU
+  GemmArgs joint[kSideStreams + 1];
+  const bool together = ss && np >= 2 && np <= kSideStreams + 1;
+  if (together) {
+    for (int i = 0, j = 0; i < count; ++i)
+      if (d[i].M > 16)
+        joint[j++] = plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
+                                d[i].bits, d[i].group, d[i].ldw, d[i].workspace, d[i].workspace_bytes);
+    plan_prefill_joint(joint, np);
+  }
   tlq_status st = TLQ_OK;
   for (int i = 0, j = 0; i < count && st == TLQ_OK; ++i) {
     if (d[i].M <= 16) continue;
     const int lane = used ? j % (used + 1) : 0;  // 0: the caller's stream
+    const cudaStream_t ls = lane ? ss->s[lane - 1] : stream;
+    if (together)
+      st = launch_prefill(joint[j], ls);
+    else
+      st = launch_prefill(plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
+                                     d[i].bits, d[i].group, d[i].ldw, d[i].workspace, d[i].workspace_bytes),
+                          ls);
     ++j;
-    st = launch_prefill(plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
-                                   d[i].bits, d[i].group, d[i].ldw, d[i].workspace, d[i].workspace_bytes),
-                        lane ? ss->s[lane - 1] : stream);
   }
   for (int k = 0; k < used; ++k) {  // join even after a failed launch
     cudaError_t e = cudaEventRecord(ss->join[k], ss->s[k]);

@@ -258,6 +258,8 @@ struct GemmArgs {
   int ldw = 0;           // packed-weight row stride in 32-bit words (0: compact rows of K*bits/32 words)
   void* ws = nullptr;    // caller-owned workspace for the prefill kernel's k split (nullptr: no k split)
   size_t ws_bytes = 0;
+  int plan_nmt = 0;      // prefill: token tiles per CTA and k split chosen for a batch (0: the launch's own plan)
+  int plan_ks = 0;
 };
 
 // Error reporting (thread-local message)
@@ -292,6 +294,10 @@ tlq_status launch_prefill(const GemmArgs& a, cudaStream_t stream);
 // Workspace bytes the prefill kernel's planner would use for this problem with
 // an unlimited workspace (0: it would not split K).
 size_t prefill_workspace_bytes(const GemmArgs& a);
+// Plans of n prefill problems that will run side by side (the batched call's
+// side streams): sets every a[i].plan_nmt / plan_ks.  Returns false (and
+// leaves the plans unset) when it does not plan jointly.
+bool plan_prefill_joint(GemmArgs* a, int n);
 tlq_status loop_block_forward_named(float* x, const tl_block* b, int L, int M, const char* who, void* stream);
 tlq_status launch_pack(const uint8_t* codes, uint32_t* W, int N, int K, int bits, cudaStream_t stream);
 tlq_status launch_unpack(const uint32_t* W, uint8_t* codes, int N, int K, int bits, cudaStream_t stream);

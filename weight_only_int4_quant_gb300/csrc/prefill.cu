@@ -27,6 +27,7 @@
 // (deterministic, no atomics).  The workspace is the caller's: the library
 // allocates nothing, and without a workspace large enough for a split the
 // planner keeps K whole.  Every mbarrier wait is bounded.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -844,16 +845,127 @@ bool plan_prefill(const GemmArgs& a, size_t ws_bytes, PrefillPlan& out) {
 template <int BITS, int EPI>
 tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
   PrefillPlan pl;
-  if (!plan_prefill<BITS, EPI>(a, a.ws ? a.ws_bytes : 0, pl))
+  if (a.plan_nmt) {
+    pl = PrefillPlan{a.plan_nmt, a.plan_ks, 0.0};  // a batch's joint plan (checked when it was made)
+  } else if (!plan_prefill<BITS, EPI>(a, a.ws ? a.ws_bytes : 0, pl)) {
     return set_error(TLQ_EINVAL, "prefill: no k split allowed by TLQ_PREFILL_KSPLIT fits the workspace (%zu bytes)",
                      a.ws ? a.ws_bytes : (size_t)0);
-  if (log_enabled()) {
+  }
+  if (log_enabled() && !a.plan_nmt) {
     const int c1 = pl.nmt == 1 ? max_clusters<BITS, EPI, 1>(pl.ks) : max_clusters<BITS, EPI, 2>(pl.ks);
     fprintf(stderr, "[tlq] prefill M=%d N=%d K=%d: %d token tile(s), k split %d (%d clusters fit), est %.1f us\n",
             a.M, a.N, a.K, pl.nmt, pl.ks, c1, pl.est_us);
   }
   return pl.nmt == 2 ? launch_impl<BITS, EPI, 2>(a, pl.ks, s) : launch_impl<BITS, EPI, 1>(a, pl.ks, s);
 }
+
+// Joint plan of problems that share the GPU.  Each problem's launch, planned
+// alone, assumes it has every SM: at short M the four projections of a step
+// then ask for 350-480 CTAs, most of them in k-split clusters, and together
+// run 1.3-1.4x slower than the best joint choice (GB300, INT4, the D = 2048
+// projections side by side, measured over every combination of token tiles
+// per CTA and k split: M = 128 46.1 us planned alone, 31.0 us best; M = 512
+// 85.2 and 61.2 us; M = 2048 173.2 us either way).  The estimate of a
+// combination keeps each launch's own cost model (prefill_estimate_us) and
+// combines the launches as
+//     E = max(a, b) + 0.5 * min(a, b),
+//     a = the longest launch alone (its waves x per-CTA time),
+//     b = the CTA-time of all launches / SMs (the GPU's share of the work);
+// the half weight on the smaller term stands for the imperfect packing of
+// CTAs of different lengths (fitted to the measured combinations: within 7 %
+// on average, and the best estimate is within 3 % of the best measured).
+// Splits of 8 are left out: a cluster of 8 CTAs needs 8 free SMs of one GPC
+// at once, which the other launches' CTAs rarely leave, and the estimate
+// cannot see that (with splits of 8 allowed, its favourite at M = 128
+// measured 37.9 us against the best 31.0).
+constexpr int kJointMax = 4;
+constexpr double kJointMix = 0.5;
+
+struct JointCand {
+  int nmt, ks;
+  double t_cta;  // per-CTA time estimate (us)
+  double waves;  // waves of this launch alone
+  double ctas;
+};
+
+// Cluster capacity of the prefill kernel for a token-tile count (the same
+// for every bit width and epilogue: shared memory and threads depend on NMT
+// only).
+int joint_clusters(int nmt, int ks) {
+  return nmt == 1 ? max_clusters<4, kEpiStore, 1>(ks) : max_clusters<4, kEpiStore, 2>(ks);
+}
+
+int joint_candidates(const GemmArgs& a, JointCand* out) {
+  const int ntile = (a.N + BN - 1) / BN;
+  const int nkb = (a.K + BK - 1) / BK;
+  const size_t ws = a.ws ? a.ws_bytes : 0;
+  int n = 0;
+  for (int nmt = 1; nmt <= 2; ++nmt) {
+    if (nmt == 2 && a.M <= BM) continue;
+    const int tiles = ntile * ((a.M + BM * nmt - 1) / (BM * nmt));
+    for (int ks = 1; ks <= 4; ks *= 2) {
+      if (ks > 1 && nkb / ks < 4) continue;
+      if (split_ws_bytes(a.M, a.N, nmt, ks) > ws) continue;
+      const int cl = joint_clusters(nmt, ks);
+      JointCand c;
+      c.nmt = nmt;
+      c.ks = ks;
+      c.t_cta = prefill_estimate_us(nmt, ks, 1, nkb, 1);
+      c.waves = (double)((tiles + cl - 1) / cl);
+      c.ctas = (double)tiles * ks;
+      out[n++] = c;
+    }
+  }
+  return n;
+}
+
+}  // namespace
+
+bool plan_prefill_joint(GemmArgs* a, int n) {
+  if (n < 2 || n > kJointMax) return false;
+  if (getenv("TLQ_PREFILL_NMT") || getenv("TLQ_PREFILL_KSPLIT")) return false;  // forced plans stay per launch
+  const double sms = (double)device_info().sms;
+  JointCand cand[kJointMax][6];
+  int nc[kJointMax];
+  for (int i = 0; i < n; ++i) {
+    if (a[i].M <= 16) return false;
+    nc[i] = joint_candidates(a[i], cand[i]);
+    if (nc[i] == 0) return false;
+  }
+  // every combination (at most 6^4); ties keep fewer CTAs, then the earlier one
+  int idx[kJointMax] = {0, 0, 0, 0};
+  int best[kJointMax] = {0, 0, 0, 0};
+  double best_e = 1e30, best_ctas = 1e30;
+  for (;;) {
+    double mx = 0.0, work = 0.0, ctas = 0.0;
+    for (int i = 0; i < n; ++i) {
+      const JointCand& c = cand[i][idx[i]];
+      mx = std::max(mx, c.waves * c.t_cta);
+      work += c.ctas * c.t_cta;
+      ctas += c.ctas;
+    }
+    const double share = work / sms;
+    const double e = std::max(mx, share) + kJointMix * std::min(mx, share);
+    if (e < best_e * (1.0 - 1e-9) || (e <= best_e * (1.0 + 1e-9) && ctas < best_ctas)) {
+      best_e = e;
+      best_ctas = ctas;
+      for (int i = 0; i < n; ++i) best[i] = idx[i];
+    }
+    int i = 0;
+    while (i < n && ++idx[i] == nc[i]) idx[i++] = 0;
+    if (i == n) break;
+  }
+  for (int i = 0; i < n; ++i) {
+    a[i].plan_nmt = cand[i][best[i]].nmt;
+    a[i].plan_ks = cand[i][best[i]].ks;
+    if (log_enabled())
+      fprintf(stderr, "[tlq] prefill (joint, %d side by side, est %.1f us) M=%d N=%d K=%d: %d token tile(s), k split %d\n",
+              n, best_e, a[i].M, a[i].N, a[i].K, a[i].plan_nmt, a[i].plan_ks);
+  }
+  return true;
+}
+
+namespace {
 
 template <int BITS>
 size_t workspace_bits(const GemmArgs& a) {
