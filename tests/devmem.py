@@ -1,6 +1,7 @@
-"""Device-memory observations for the GPU tests: the high watermark of the
+"""Device-memory helpers for the GPU tests: the high watermark of the
 device's default stream-ordered memory pool (what cudaMallocAsync draws
-from), read through the CUDA runtime the library itself loaded."""
+from), read through the CUDA runtime the library itself loaded, and an L2
+flush."""
 import ctypes
 
 _POOL_USED_MEM_HIGH = 8  # cudaMemPoolAttrUsedMemHigh
@@ -28,3 +29,15 @@ def default_pool_high_watermark(reset=False):
         assert rt.cudaMemPoolSetAttribute(pool, _POOL_USED_MEM_HIGH, ctypes.byref(v)) == 0
     assert rt.cudaMemPoolGetAttribute(pool, _POOL_USED_MEM_HIGH, ctypes.byref(v)) == 0
     return v.value
+
+
+def flush_l2(nbytes=256 << 20):
+    """Write a buffer twice the size of GB300's L2, so that whatever a kernel
+    reads next comes from HBM unless that kernel's own earlier reads put it in
+    L2."""
+    import torch
+
+    junk = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda")
+    junk.fill_(1)
+    torch.cuda.synchronize()
+    del junk

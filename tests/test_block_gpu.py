@@ -4,6 +4,7 @@ import pytest
 
 import oracle
 import synth
+from devmem import flush_l2
 from parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -64,9 +65,11 @@ def test_block_without_norm_one_iteration(lib, bits):
 
 @pytest.mark.parametrize("bits", [4, 2])
 def test_block_full_width_decode(lib, bits):
-    """D = 2048, FFN 8192, M = 1, L = 4 against the oracle."""
+    """D = 2048, FFN 8192, M = 1, L = 4 against the oracle.  The L2 is flushed
+    first: iteration 1 reads the weights from HBM, the later ones from L2."""
     case = synth.block_case(1, bits, seed=0)
     blk, host = make_block(lib, case)
+    flush_l2()
     got = run_gpu(lib, blk, case["x0"], 4)
     ref = oracle.loop_block(case["x0"], host, bits, case["group"], 4, normalize=True)
     assert_close(got, ref, "block D2048 int%d" % bits)

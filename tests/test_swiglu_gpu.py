@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 import synth
+from devmem import flush_l2
 from parity import assert_close, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -159,9 +160,12 @@ def test_swiglu_block_small_matches_oracle(lib, bits, M, L):
 
 @pytest.mark.parametrize("bits", [4, 2])
 def test_swiglu_block_full_width_decode(lib, bits):
-    """D = 2048, F = 8192 (32 MiB of INT4 weights, the pages' loop block), M = 1, L = 4."""
+    """D = 2048, F = 8192 (32 MiB of INT4 weights, the pages' loop block), M = 1, L = 4.
+    The L2 is flushed first: iteration 1 reads the weights from HBM, the later
+    ones from L2."""
     case = synth.swiglu_block_case(1, bits, seed=5)
     blk, host = make_block(lib, case)
+    flush_l2()
     got = run(lib, blk, case["x0"], 4)
     assert_close(got, oracle.loop_block_swiglu(case["x0"], host, bits, case["group"], 4), "int%d" % bits)
 
