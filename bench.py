@@ -398,18 +398,25 @@ def copies_for(weight_set_bytes, per_step_sets, l2_bytes):
     return n
 
 
-def kernel_hash():
+def kernel_hash(files=("decode.cu", "common.cuh")):
     h = hashlib.sha256()
-    for f in ("decode.cu", "common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "weight_only_int4_quant_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+PREFILL_SOURCES = ("prefill.cu", "tc_common.cuh", "common.cuh")
 
 
 # dram bytes (read + write) per launch of the decode kernel for the headline
 # step, from one ncu capture of that launch; used only while the kernel source
 # hashes to the captured one.
 NCU_TRAFFIC = {"kernel_hash": "6c2833ff948ff39e", "bytes_per_step": 81979648}
+# the same for the prefill step at M = 2048 (four launches of the tensor-core
+# kernel; their C tiles stay in L2 while the step runs, so the bytes are the
+# reads of A and of the weights, each once)
+NCU_PREFILL_TRAFFIC = {"kernel_hash": "fae538e853fdc27e", "bytes_per_step": 85815296}
 
 
 def run_tlq(args, rank, world, dist):
@@ -561,7 +568,10 @@ def run_tlq(args, rank, world, dist):
     if pf:
         line["roofline"]["prefill"] = {
             "bound": "tensor", "achieved": pf["TFLOPs"], "peak": round(peaks["fp16"], 1), "unit": "TFLOP/s",
-            "frac": round(pf["TFLOPs"] / peaks["fp16"], 3), "traffic": None, "peak_source": "measured in this run",
+            "frac": round(pf["TFLOPs"] / peaks["fp16"], 3),
+            "traffic": NCU_PREFILL_TRAFFIC["bytes_per_step"]
+            if NCU_PREFILL_TRAFFIC["kernel_hash"] == kernel_hash(PREFILL_SOURCES) else None,
+            "peak_source": "measured in this run",
             "kernel": "prefill_kernel (INT4, M = 2048, QKV/O/UP/DOWN in one batched call)",
             "frac_by_M": {k: v["frac_of_fp16_peak"] for k, v in result["prefill"].items()}}
     lb = result.get("loop_block", {}).get("int4_M1_L16")

@@ -397,9 +397,9 @@ def test_batched_prefill_side_streams_in_a_graph(lib):
         assert_close(p["C"].cpu().numpy()[rows], ref, "side streams M%d N%d K%d" % (M, N, K))
 
 
-@pytest.mark.parametrize("M", [128, 512])
+@pytest.mark.parametrize("M", [128, 512, 2048])
 def test_batched_prefill_step_full_size(lib, M):
-    """The four D = 2048 projections at M = 128 / 512 in one batched call, each
+    """The four D = 2048 projections at M = 128 / 512 / 2048 in one batched call, each
     with the workspace its own plan asks for: the launches run side by side
     with token tiles and k splits planned for the shared GPU (at M = 128 the
     DOWN projection alone keeps a k split).  16 whole rows per problem against
