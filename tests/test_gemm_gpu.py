@@ -74,6 +74,30 @@ def test_decode_matches_oracle(lib, bits, group, N, K, M):
     assert_close(C, ref, "int%d g%d M%d N%d K%d" % (bits, group, M, N, K))
 
 
+@pytest.mark.parametrize("bits,group,G_ok,G_bad", [(4, 32, 168, 176), (2, 64, 168, 176)])
+def test_decode_largest_groups_per_row(lib, monkeypatch, bits, group, G_ok, G_bad):
+    """The decode kernel stages a unit's scales and zeros in shared memory, so
+    K/group has a ceiling (64-row units, two token tiles: 168 groups per row).
+    At the ceiling the result matches the oracle; one step above it the call
+    is refused on the host with TLQ_EUNSUPPORTED before anything is launched."""
+    monkeypatch.setenv("TLQ_DECODE_ROWS", "64")
+    M, N = 16, 128
+    case = synth.gemm_case(M, N, group * G_ok, bits, group, seed=G_ok + bits)
+    _, C = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(C, ref, "int%d g%d K%d" % (bits, group, group * G_ok))
+    K = group * G_bad
+    A = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    W = torch.zeros((N, K * bits // 32), dtype=torch.int32, device="cuda")
+    s = torch.ones((N, G_bad), dtype=torch.float16, device="cuda")
+    z = torch.zeros((N, G_bad), dtype=torch.float16, device="cuda")
+    with pytest.raises(lib.TLQError) as e:
+        lib.quant_gemm(A, W, s, z, bits, group)
+    assert e.value.status == lib.TLQ_EUNSUPPORTED
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+
+
 @pytest.mark.parametrize("M", [2, 5, 7, 12, 15])
 def test_decode_other_token_counts(lib, M):
     case = synth.gemm_case(M, 512, 2048, 4, 128, seed=M)
@@ -397,18 +421,20 @@ def test_batched_prefill_side_streams_in_a_graph(lib):
         assert_close(p["C"].cpu().numpy()[rows], ref, "side streams M%d N%d K%d" % (M, N, K))
 
 
-@pytest.mark.parametrize("M", [128, 512, 2048])
-def test_batched_prefill_step_full_size(lib, M):
-    """The four D = 2048 projections at M = 128 / 512 / 2048 in one batched call, each
+@pytest.mark.parametrize("M,bits", [(128, 4), (512, 4), (2048, 4), (128, 2), (512, 2)])
+def test_batched_prefill_step_full_size(lib, M, bits):
+    """The four D = 2048 projections at M = 128 / 512 / 2048 (INT4) and 128 / 512
+    (INT2) in one batched call, each
     with the workspace its own plan asks for: the launches run side by side
     with token tiles and k splits planned for the shared GPU (at M = 128 the
     DOWN projection alone keeps a k split).  16 whole rows per problem against
     the oracle; a second call gives the same bits."""
-    specs = [(M, N, K, 4, 128) for (N, K) in synth.SHAPES.values()]
+    group = synth.DIST[bits]["group"]
+    specs = [(M, N, K, bits, group) for (N, K) in synth.SHAPES.values()]
     probs = _problems(specs, seed=50)
-    for p, (M_, N, K, bits, group) in zip(probs, specs):
-        p["ws"] = lib.gemm_workspace(M_, N, K, bits, group)
-    descs = lib.gemm_descs([(p["A"], p["W"], p["s"], p["z"], p["C"], 4, 128, p["ws"]) for p in probs])
+    for p, (M_, N, K, bits_, group_) in zip(probs, specs):
+        p["ws"] = lib.gemm_workspace(M_, N, K, bits_, group_)
+    descs = lib.gemm_descs([(p["A"], p["W"], p["s"], p["z"], p["C"], bits, group, p["ws"]) for p in probs])
     lib.tl_quant_gemm_batched(descs)
     torch.cuda.synchronize()
     lib.tl_check_status()
@@ -417,13 +443,13 @@ def test_batched_prefill_step_full_size(lib, M):
     torch.cuda.synchronize()
     for p, f in zip(probs, first):
         assert torch.equal(p["C"].view(torch.int16), f.view(torch.int16))
-    rng = np.random.default_rng(M)
-    for p, (M_, N, K, bits, group) in zip(probs, specs):
+    rng = np.random.default_rng(M + bits)
+    for p, (M_, N, K, bits_, group_) in zip(probs, specs):
         rows = sample_rows(M, 16, rng)
         c = p["case"]
         ref = oracle.quant_gemm(c["A"][rows], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
                                 group)
-        assert_close(p["C"].cpu().numpy()[rows], ref, "batched step M%d N%d K%d" % (M, N, K))
+        assert_close(p["C"].cpu().numpy()[rows], ref, "batched step int%d M%d N%d K%d" % (bits, M, N, K))
 
 
 def test_batched_mixed_bits_and_paths(lib):
