@@ -119,6 +119,31 @@ tlq_status tl_quant_gemm(const uint16_t* A, const uint32_t* Wpacked, const uint1
 size_t tl_quant_gemm_workspace_size(int M, int N, int K, int bits, int group);
 
 /*
+ * tl_prefill_plan -- the launch plan the library would use for `count`
+ * problems: per problem the token tiles per CTA of the tensor-core kernel
+ * (1 or 2) and its k split (1, 2, 4 or 8), or 0 and 0 when M <= 16 (the
+ * decode kernel).  count = 1 plans a single call (tl_quant_gemm_ws with the
+ * given workspace); count = 2..4 with every M > 16 gives the joint plan of a
+ * batched call whose launches run side by side; otherwise each problem is
+ * planned alone.
+ *   M, N, K, ws_bytes  HOST arrays of `count` entries (ws_bytes: the bytes of
+ *                      workspace each problem is given, 0 = none).
+ *   device             NULL: the current device.  Else a HOST int[9]: the SM
+ *                      count, then how many clusters of 1, 2, 4 and 8 CTAs
+ *                      fit at once with one token tile per CTA, then the same
+ *                      with two.  With a device description no CUDA call is
+ *                      made (the planners are host code).
+ *   nmt_out, ks_out    HOST arrays of `count` entries, written.
+ * TLQ_PREFILL_NMT / TLQ_PREFILL_KSPLIT force the choice as they do for the
+ * launches.  A library choice (launch shape), not an operation of the pages.
+ * Returns TLQ_OK or TLQ_EINVAL (count outside 1..16, null arrays, a size
+ * below 1, a device entry below 1, or a forced split without the workspace
+ * it needs).
+ */
+tlq_status tl_prefill_plan(const int* M, const int* N, const int* K, const size_t* ws_bytes, int count,
+                           const int* device, int* nmt_out, int* ks_out);
+
+/*
  * tl_quant_gemm_ws -- tl_quant_gemm with a caller-owned workspace for the
  * tensor-core kernel's k split (same operation, layouts and errors).
  *   workspace        device buffer, 16-byte aligned, or NULL; must not

@@ -321,3 +321,85 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tlq, "_LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         tlq.load()
+
+
+# GB300 as the prefill planners see it: 152 SMs; clusters of 1 / 2 / 4 / 8
+# CTAs that fit at once (one CTA per SM) with one and with two token tiles
+GB300 = (152, (152, 76, 36, 15), (152, 76, 36, 15))
+PROJ = [(6144, 2048), (2048, 2048), (8192, 2048), (2048, 8192)]  # QKV, O, UP, DOWN (N, K)
+UNLIMITED = 1 << 40
+
+
+def test_prefill_plan_single_calls(clib, monkeypatch):
+    """Plans of single calls on the GB300 description (host only: no CUDA
+    call with a device description).  At M = 128 each projection alone asks
+    for a k split (the weight tiles alone leave SMs idle); without a
+    workspace it keeps K whole; M <= 16 is the decode kernel; the
+    environment's forced choices win."""
+    import weight_only_int4_quant_gb300 as tlq
+
+    monkeypatch.delenv("TLQ_PREFILL_NMT", raising=False)
+    monkeypatch.delenv("TLQ_PREFILL_KSPLIT", raising=False)
+    for (N, K), want in zip(PROJ, [(1, 4), (1, 8), (1, 4), (1, 8)]):
+        assert tlq.tl_prefill_plan([(128, N, K)], [UNLIMITED], GB300) == [want]
+        assert tlq.tl_prefill_plan([(128, N, K)], [0], GB300) == [(1, 1)]
+        assert tlq.tl_prefill_plan([(16, N, K)], [UNLIMITED], GB300) == [(0, 0)]
+    # two token tiles per CTA only when M has two token tiles
+    assert tlq.tl_prefill_plan([(2048, 8192, 2048)], [UNLIMITED], GB300) == [(2, 1)]
+    assert all(p[0] == 1 for p in tlq.tl_prefill_plan([(128, N, K) for N, K in PROJ][:1], [UNLIMITED], GB300))
+    monkeypatch.setenv("TLQ_PREFILL_KSPLIT", "2")
+    assert tlq.tl_prefill_plan([(128, 2048, 8192)], [UNLIMITED], GB300) == [(1, 2)]
+    with pytest.raises(tlq.TLQError):  # a forced split without its workspace
+        tlq.tl_prefill_plan([(128, 2048, 8192)], [0], GB300)
+
+
+def test_prefill_plan_joint(clib, monkeypatch):
+    """Four projections side by side (a batched call): the joint plan is the
+    combination measured fastest on GB300 at M = 128 (31.0 us against 46.1 us
+    for the single-call plans; every combination swept), keeps splits of 8
+    out, and uses far fewer CTAs than the single-call plans; at M = 512 and
+    2048 every launch takes two token tiles per CTA and only DOWN splits K.
+    Forcing a choice through the environment turns joint planning off."""
+    import weight_only_int4_quant_gb300 as tlq
+
+    monkeypatch.delenv("TLQ_PREFILL_NMT", raising=False)
+    monkeypatch.delenv("TLQ_PREFILL_KSPLIT", raising=False)
+
+    def ctas(M, plans):
+        return sum(((N + 255) // 256) * ((M + 128 * nmt - 1) // (128 * nmt)) * ks
+                   for (N, K), (nmt, ks) in zip(PROJ, plans))
+
+    probs = [(128, N, K) for N, K in PROJ]
+    joint = tlq.tl_prefill_plan(probs, [UNLIMITED] * 4, GB300)
+    assert joint == [(1, 1), (1, 1), (1, 1), (1, 4)]
+    solo = [tlq.tl_prefill_plan([p], [UNLIMITED], GB300)[0] for p in probs]
+    assert ctas(128, joint) == 96 < ctas(128, solo) == 352
+    assert tlq.tl_prefill_plan([(512, N, K) for N, K in PROJ], [UNLIMITED] * 4, GB300) == \
+        [(2, 1), (2, 1), (2, 1), (2, 4)]
+    assert tlq.tl_prefill_plan([(2048, N, K) for N, K in PROJ], [UNLIMITED] * 4, GB300) == \
+        [(2, 1), (2, 1), (2, 1), (2, 2)]
+    # each launch stays within its own workspace: none for QKV keeps it unsplit
+    j = tlq.tl_prefill_plan(probs, [0, UNLIMITED, UNLIMITED, 0], GB300)
+    assert j[0][1] == 1 and j[3][1] == 1
+    # a decode-sized problem in the batch: no joint plan, each planned alone
+    mixed = tlq.tl_prefill_plan([(1, 6144, 2048)] + probs[1:], [UNLIMITED] * 4, GB300)
+    assert mixed == [(0, 0)] + solo[1:]
+    monkeypatch.setenv("TLQ_PREFILL_NMT", "1")
+    assert tlq.tl_prefill_plan(probs, [UNLIMITED] * 4, GB300) == solo
+
+
+def test_prefill_plan_rejects_bad_arguments(clib):
+    import weight_only_int4_quant_gb300 as tlq
+
+    n = (ctypes.c_int * 1)(128)
+    ws = (ctypes.c_size_t * 1)(0)
+    out1, out2 = (ctypes.c_int * 1)(), (ctypes.c_int * 1)()
+    dev = (ctypes.c_int * 9)(152, 152, 76, 36, 15, 152, 76, 36, 15)
+    assert clib.tl_prefill_plan(n, n, n, ws, 0, dev, out1, out2) == tlq.TLQ_EINVAL
+    assert clib.tl_prefill_plan(n, n, n, ws, 17, dev, out1, out2) == tlq.TLQ_EINVAL
+    assert clib.tl_prefill_plan(n, None, n, ws, 1, dev, out1, out2) == tlq.TLQ_EINVAL
+    zero = (ctypes.c_int * 1)(0)
+    assert clib.tl_prefill_plan(n, zero, n, ws, 1, dev, out1, out2) == tlq.TLQ_EINVAL
+    bad = (ctypes.c_int * 9)(152, 152, 76, 0, 15, 152, 76, 36, 15)
+    assert clib.tl_prefill_plan(n, n, n, ws, 1, bad, out1, out2) == tlq.TLQ_EINVAL
+    assert b"device[3]" in clib.tl_last_error()

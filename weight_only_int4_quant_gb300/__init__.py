@@ -25,7 +25,7 @@ __all__ = [
     "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked", "tl_quant_gemm_batched_host",
     "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws", "tl_loop_block_to_int2",
     "tl_swiglu_block_to_int2", "gemm_workspace", "requant_descs", "tl_probe_read_bandwidth",
-    "tl_loop_block_l2_plan",
+    "tl_loop_block_l2_plan", "tl_prefill_plan",
 ]
 
 # every symbol include/tlq.h declares
@@ -37,6 +37,7 @@ EXPORTED = (
     "tl_dequant_fp16", "tl_loop_block_forward_chunked", "tl_swiglu_block_forward_chunked",
     "tl_quant_gemm_batched_host", "tl_quant_gemm_ws", "tl_quant_gemm_workspace_size", "tl_quant_gemm_swiglu_ws",
     "tl_loop_block_to_int2", "tl_swiglu_block_to_int2", "tl_probe_read_bandwidth", "tl_loop_block_l2_plan",
+    "tl_prefill_plan",
 )
 
 TLQ_OK, TLQ_EINVAL, TLQ_EUNSUPPORTED, TLQ_ECUDA, TLQ_ETIMEOUT = 0, 1, 2, 3, 4
@@ -129,6 +130,7 @@ def load():
             "tl_swiglu_block_forward_chunked": ([P, ctypes.POINTER(_SwigluBlock), I, I, I, P], I),
             "tl_swiglu_block_forward": ([P, ctypes.POINTER(_SwigluBlock), I, I, P], I),
             "tl_quant_gemm_workspace_size": ([I, I, I, I, I], ctypes.c_size_t),
+            "tl_prefill_plan": ([P, P, P, P, I, P, P, P], I),
             "tl_quant_gemm_ws": ([P, P, P, P, P, I, I, I, I, I, P, ctypes.c_size_t, P], I),
             "tl_quant_gemm_swiglu_ws": ([P, P, P, P, P, I, I, I, I, I, P, ctypes.c_size_t, P], I),
             "tl_loop_block_to_int2": ([ctypes.POINTER(_Block), ctypes.POINTER(_QProj), P], I),
@@ -195,6 +197,29 @@ def tl_quant_gemm(A, W, scales, zeros, C, bits: int, group: int, stream=None) ->
 def tl_quant_gemm_workspace_size(M: int, N: int, K: int, bits: int, group: int) -> int:
     """Bytes of k-split workspace the tensor-core kernel would use (0: none)."""
     return int(load().tl_quant_gemm_workspace_size(M, N, K, bits, group))
+
+
+def tl_prefill_plan(shapes, ws_bytes=None, device=None):
+    """[(token tiles per CTA, k split)] the library would launch for the
+    (M, N, K) problems in ``shapes`` ((0, 0): the decode kernel); several
+    problems with M > 16 (up to four) are planned jointly, as a batched call
+    runs them.  ``ws_bytes``: the workspace bytes each is given (default 0);
+    ``device``: None for the current device, or (sms, clusters with one token
+    tile for k splits 1/2/4/8, the same with two) -- then no CUDA call is made."""
+    n = len(shapes)
+    arr = lambda t, vals: (t * n)(*vals)  # noqa: E731
+    Ms = arr(ctypes.c_int, [s[0] for s in shapes])
+    Ns = arr(ctypes.c_int, [s[1] for s in shapes])
+    Ks = arr(ctypes.c_int, [s[2] for s in shapes])
+    ws = arr(ctypes.c_size_t, list(ws_bytes) if ws_bytes is not None else [0] * n)
+    dev = None
+    if device is not None:
+        sms, one, two = device
+        dev = (ctypes.c_int * 9)(sms, *one, *two)
+    nmt = (ctypes.c_int * n)()
+    ks = (ctypes.c_int * n)()
+    _raise_if(load().tl_prefill_plan(Ms, Ns, Ks, ws, n, dev, nmt, ks))
+    return [(nmt[i], ks[i]) for i in range(n)]
 
 
 def gemm_workspace(M: int, N: int, K: int, bits: int, group: int, device="cuda"):

@@ -201,6 +201,27 @@ size_t tl_quant_gemm_workspace_size(int M, int N, int K, int bits, int group) {
   return prefill_workspace_bytes(a);
 }
 
+tlq_status tl_prefill_plan(const int* M, const int* N, const int* K, const size_t* ws_bytes, int count,
+                           const int* device, int* nmt_out, int* ks_out) {
+  g_msg[0] = 0;
+  if (count < 1 || count > 16) return set_error(TLQ_EINVAL, "tl_prefill_plan: count=%d (1..16)", count);
+  if (!M || !N || !K || !ws_bytes || !nmt_out || !ks_out) return set_error(TLQ_EINVAL, "tl_prefill_plan: null array");
+  for (int i = 0; i < count; ++i)
+    if (M[i] < 1 || N[i] < 1 || K[i] < 1)
+      return set_error(TLQ_EINVAL, "tl_prefill_plan[%d]: M=%d N=%d K=%d (must be >= 1)", i, M[i], N[i], K[i]);
+  PlanDevice d;
+  if (device) {
+    for (int i = 0; i < 9; ++i)
+      if (device[i] < 1) return set_error(TLQ_EINVAL, "tl_prefill_plan: device[%d]=%d (must be >= 1)", i, device[i]);
+    d.sms = device[0];
+    for (int i = 0; i < 4; ++i) {
+      d.clusters[0][i] = device[1 + i];
+      d.clusters[1][i] = device[5 + i];
+    }
+  }
+  return prefill_plan(M, N, K, ws_bytes, count, device ? &d : nullptr, nmt_out, ks_out);
+}
+
 tlq_status tl_quant_gemm_ws(const uint16_t* A, const uint32_t* Wpacked, const uint16_t* scales,
                             const uint16_t* zeros, uint16_t* C, int M, int N, int K, int bits, int group,
                             void* workspace, size_t workspace_bytes, void* stream) {

@@ -298,6 +298,17 @@ size_t prefill_workspace_bytes(const GemmArgs& a);
 // side streams): sets every a[i].plan_nmt / plan_ks.  Returns false (and
 // leaves the plans unset) when it does not plan jointly.
 bool plan_prefill_joint(GemmArgs* a, int n);
+// The device as the prefill planners see it: SMs, and for one and two token
+// tiles per CTA the clusters of 1, 2, 4 and 8 CTAs that fit at once.
+struct PlanDevice {
+  int sms;
+  int clusters[2][4];
+};
+// The plans of n problems (token tiles per CTA and k split; 0 and 0 for
+// M <= 16, the decode kernel): joint when all n (2..4) run side by side as in
+// a batched call, else each planned alone.  dev NULL: the current device.
+tlq_status prefill_plan(const int* M, const int* N, const int* K, const size_t* ws, int n, const PlanDevice* dev,
+                        int* nmt, int* ks);
 tlq_status loop_block_forward_named(float* x, const tl_block* b, int L, int M, const char* who, void* stream);
 tlq_status launch_pack(const uint8_t* codes, uint32_t* W, int N, int K, int bits, cudaStream_t stream);
 tlq_status launch_unpack(const uint32_t* W, uint8_t* codes, int N, int K, int bits, cudaStream_t stream);

@@ -818,28 +818,50 @@ struct PrefillPlan {
   double est_us;
 };
 
-template <int BITS, int EPI>
-bool plan_prefill(const GemmArgs& a, size_t ws_bytes, PrefillPlan& out) {
+int ks_index(int ks) { return ks == 1 ? 0 : ks == 2 ? 1 : ks == 4 ? 2 : 3; }
+
+// The device as the planners see it: SMs, and the clusters of ks CTAs of the
+// kernel with one or two token tiles that fit at once.  Queried once (the
+// kernel's shared memory and threads depend on the token tiles only, so one
+// bit width and epilogue stands for all).
+const PlanDevice& plan_device() {
+  static std::once_flag once;
+  static PlanDevice d;
+  std::call_once(once, [] {
+    d.sms = device_info().sms;
+    for (int i = 0; i < 4; ++i) {
+      d.clusters[0][i] = max_clusters<4, kEpiStore, 1>(1 << i);
+      d.clusters[1][i] = max_clusters<4, kEpiStore, 2>(1 << i);
+    }
+  });
+  return d;
+}
+
+bool plan_solo(int M, int N, int K, size_t ws_bytes, const PlanDevice& dev, PrefillPlan& out) {
   int force_nmt = 0, force_ks = 0;
   if (const char* e = getenv("TLQ_PREFILL_NMT")) force_nmt = atoi(e);
   if (const char* e = getenv("TLQ_PREFILL_KSPLIT")) force_ks = atoi(e);
   if (force_nmt != 1 && force_nmt != 2) force_nmt = 0;
-  const int ntile = (a.N + BN - 1) / BN;
-  const int nkb = (a.K + BK - 1) / BK;
+  const int ntile = (N + BN - 1) / BN;
+  const int nkb = (K + BK - 1) / BK;
   out = PrefillPlan{1, 1, 1e30};
   for (int nmt = 1; nmt <= 2; ++nmt) {
     if (force_nmt && nmt != force_nmt) continue;
-    if (nmt == 2 && a.M <= BM && !force_nmt) continue;
-    const int tiles = ntile * ((a.M + BM * nmt - 1) / (BM * nmt));
+    if (nmt == 2 && M <= BM && !force_nmt) continue;
+    const int tiles = ntile * ((M + BM * nmt - 1) / (BM * nmt));
     for (int ks = 1; ks <= 8; ks *= 2) {
       if (force_ks ? ks != force_ks : (ks > 1 && nkb / ks < 4)) continue;
-      if (split_ws_bytes(a.M, a.N, nmt, ks) > ws_bytes) continue;
-      const int clusters = nmt == 1 ? max_clusters<BITS, EPI, 1>(ks) : max_clusters<BITS, EPI, 2>(ks);
-      const double t = prefill_estimate_us(nmt, ks, tiles, nkb, clusters);
+      if (split_ws_bytes(M, N, nmt, ks) > ws_bytes) continue;
+      const double t = prefill_estimate_us(nmt, ks, tiles, nkb, dev.clusters[nmt - 1][ks_index(ks)]);
       if (t < out.est_us) out = PrefillPlan{nmt, ks, t};
     }
   }
   return out.est_us < 1e29;
+}
+
+template <int BITS, int EPI>
+bool plan_prefill(const GemmArgs& a, size_t ws_bytes, PrefillPlan& out) {
+  return plan_solo(a.M, a.N, a.K, ws_bytes, plan_device(), out);
 }
 
 template <int BITS, int EPI>
@@ -852,7 +874,7 @@ tlq_status launch_pick(const GemmArgs& a, cudaStream_t s) {
                      a.ws ? a.ws_bytes : (size_t)0);
   }
   if (log_enabled() && !a.plan_nmt) {
-    const int c1 = pl.nmt == 1 ? max_clusters<BITS, EPI, 1>(pl.ks) : max_clusters<BITS, EPI, 2>(pl.ks);
+    const int c1 = plan_device().clusters[pl.nmt - 1][ks_index(pl.ks)];
     fprintf(stderr, "[tlq] prefill M=%d N=%d K=%d: %d token tile(s), k split %d (%d clusters fit), est %.1f us\n",
             a.M, a.N, a.K, pl.nmt, pl.ks, c1, pl.est_us);
   }
@@ -888,25 +910,17 @@ struct JointCand {
   double ctas;
 };
 
-// Cluster capacity of the prefill kernel for a token-tile count (the same
-// for every bit width and epilogue: shared memory and threads depend on NMT
-// only).
-int joint_clusters(int nmt, int ks) {
-  return nmt == 1 ? max_clusters<4, kEpiStore, 1>(ks) : max_clusters<4, kEpiStore, 2>(ks);
-}
-
-int joint_candidates(const GemmArgs& a, JointCand* out) {
-  const int ntile = (a.N + BN - 1) / BN;
-  const int nkb = (a.K + BK - 1) / BK;
-  const size_t ws = a.ws ? a.ws_bytes : 0;
+int joint_candidates(int M, int N, int K, size_t ws, const PlanDevice& dev, JointCand* out) {
+  const int ntile = (N + BN - 1) / BN;
+  const int nkb = (K + BK - 1) / BK;
   int n = 0;
   for (int nmt = 1; nmt <= 2; ++nmt) {
-    if (nmt == 2 && a.M <= BM) continue;
-    const int tiles = ntile * ((a.M + BM * nmt - 1) / (BM * nmt));
+    if (nmt == 2 && M <= BM) continue;
+    const int tiles = ntile * ((M + BM * nmt - 1) / (BM * nmt));
     for (int ks = 1; ks <= 4; ks *= 2) {
       if (ks > 1 && nkb / ks < 4) continue;
-      if (split_ws_bytes(a.M, a.N, nmt, ks) > ws) continue;
-      const int cl = joint_clusters(nmt, ks);
+      if (split_ws_bytes(M, N, nmt, ks) > ws) continue;
+      const int cl = dev.clusters[nmt - 1][ks_index(ks)];
       JointCand c;
       c.nmt = nmt;
       c.ks = ks;
@@ -921,15 +935,16 @@ int joint_candidates(const GemmArgs& a, JointCand* out) {
 
 }  // namespace
 
-bool plan_prefill_joint(GemmArgs* a, int n) {
+static bool plan_joint(const int* M, const int* N, const int* K, const size_t* ws, int n, const PlanDevice& dev, int* nmt,
+                int* ks, double* est_us) {
   if (n < 2 || n > kJointMax) return false;
   if (getenv("TLQ_PREFILL_NMT") || getenv("TLQ_PREFILL_KSPLIT")) return false;  // forced plans stay per launch
-  const double sms = (double)device_info().sms;
+  const double sms = (double)dev.sms;
   JointCand cand[kJointMax][6];
   int nc[kJointMax];
   for (int i = 0; i < n; ++i) {
-    if (a[i].M <= 16) return false;
-    nc[i] = joint_candidates(a[i], cand[i]);
+    if (M[i] <= 16) return false;
+    nc[i] = joint_candidates(M[i], N[i], K[i], ws[i], dev, cand[i]);
     if (nc[i] == 0) return false;
   }
   // every combination (at most 6^4); ties keep fewer CTAs, then the earlier one
@@ -956,13 +971,52 @@ bool plan_prefill_joint(GemmArgs* a, int n) {
     if (i == n) break;
   }
   for (int i = 0; i < n; ++i) {
-    a[i].plan_nmt = cand[i][best[i]].nmt;
-    a[i].plan_ks = cand[i][best[i]].ks;
+    nmt[i] = cand[i][best[i]].nmt;
+    ks[i] = cand[i][best[i]].ks;
+  }
+  if (est_us) *est_us = best_e;
+  return true;
+}
+
+bool plan_prefill_joint(GemmArgs* a, int n) {
+  if (n < 2 || n > kJointMax) return false;
+  int M[kJointMax], N[kJointMax], K[kJointMax], nmt[kJointMax], ks[kJointMax];
+  size_t ws[kJointMax];
+  for (int i = 0; i < n; ++i) {
+    M[i] = a[i].M;
+    N[i] = a[i].N;
+    K[i] = a[i].K;
+    ws[i] = a[i].ws ? a[i].ws_bytes : 0;
+  }
+  double est = 0.0;
+  if (!plan_joint(M, N, K, ws, n, plan_device(), nmt, ks, &est)) return false;
+  for (int i = 0; i < n; ++i) {
+    a[i].plan_nmt = nmt[i];
+    a[i].plan_ks = ks[i];
     if (log_enabled())
       fprintf(stderr, "[tlq] prefill (joint, %d side by side, est %.1f us) M=%d N=%d K=%d: %d token tile(s), k split %d\n",
-              n, best_e, a[i].M, a[i].N, a[i].K, a[i].plan_nmt, a[i].plan_ks);
+              n, est, a[i].M, a[i].N, a[i].K, a[i].plan_nmt, a[i].plan_ks);
   }
   return true;
+}
+
+tlq_status prefill_plan(const int* M, const int* N, const int* K, const size_t* ws, int n, const PlanDevice* dev_in,
+                        int* nmt, int* ks) {
+  const PlanDevice& dev = dev_in ? *dev_in : plan_device();
+  for (int i = 0; i < n; ++i) nmt[i] = ks[i] = 0;  // M <= 16: the decode kernel
+  int np = 0;
+  for (int i = 0; i < n; ++i) np += M[i] > 16;
+  if (np == n && plan_joint(M, N, K, ws, n, dev, nmt, ks, nullptr)) return TLQ_OK;
+  for (int i = 0; i < n; ++i) {
+    if (M[i] <= 16) continue;
+    PrefillPlan pl;
+    if (!plan_solo(M[i], N[i], K[i], ws[i], dev, pl))
+      return set_error(TLQ_EINVAL, "tl_prefill_plan[%d]: no k split allowed by TLQ_PREFILL_KSPLIT fits the workspace",
+                       i);
+    nmt[i] = pl.nmt;
+    ks[i] = pl.ks;
+  }
+  return TLQ_OK;
 }
 
 namespace {
