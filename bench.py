@@ -419,6 +419,23 @@ NCU_TRAFFIC = {"kernel_hash": "6a6efe2b71c75afc", "bytes_per_step": 82194432}
 NCU_PREFILL_TRAFFIC = {"kernel_hash": "87429b88a76b0ba5", "bytes_per_step": 85818880}
 
 
+def max_over_ranks(torch, value, dist, device="cuda"):
+    """The largest of every rank's value: the slowest rank sets the job's
+    time (the value itself when there is one rank)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, step_bytes, steps, ms_max):
+    """GB/s of the whole job: every rank runs the full step on its own GPU
+    (replicas, weak scaling), so the bytes all ranks processed over the
+    slowest rank's time."""
+    return world * step_bytes * steps / (ms_max * 1e-3) / 1e9
+
+
 def run_tlq(args, rank, world, dist):
     import torch
 
@@ -446,13 +463,9 @@ def run_tlq(args, rank, world, dist):
                     for t in range(TRIALS)]
     clocks = clk.summary()
     ms = statistics.median(trial_ms)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(torch, ms, dist)
     ms_step = ms_max / args.steps
-    value = world * wl4.step_bytes * args.steps / (ms_max * 1e-3) / 1e9
+    value = whole_job_gbs(world, wl4.step_bytes, args.steps, ms_max)
     per_rank_gbs = wl4.step_bytes / (ms_step * 1e-3) / 1e9
 
     # the same step as 12 separate tl_quant_gemm launches (one graph per phase)
