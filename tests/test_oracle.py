@@ -282,6 +282,22 @@ def test_gemm_against_torch_float64():
     assert np.mean(C.view(np.uint16) == ref16.view(np.uint16)) > 0.999
 
 
+def test_gemm_independent_of_host_threads():
+    """The oracle shares output rows over host threads; every output is the
+    same k-order sum, so the bits do not depend on the thread count."""
+    case = synth.gemm_case(7, 136, 1024, 4, 128, seed=11)
+    W = oracle.pack(case["codes"], 4)
+    before = oracle.set_threads(0)
+    try:
+        outs = []
+        for n in (1, 3, 8):
+            oracle.set_threads(n)
+            outs.append(oracle.quant_gemm(case["A"], W, case["scales"], case["zeros"], 4, 128))
+    finally:
+        oracle.set_threads(before)
+    assert all(np.array_equal(o.view(np.uint16), outs[0].view(np.uint16)) for o in outs[1:])
+
+
 def test_gemm_points_match_full():
     case = synth.gemm_case(9, 40, 256, 2, 64, seed=9)
     W = oracle.pack(case["codes"], 2)
