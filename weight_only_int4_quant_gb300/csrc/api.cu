@@ -461,26 +461,28 @@ tlq_status tl_quant_gemm_batched(const tl_gemm_desc* d, int count, void* stream_
   // up to four problems all run at once (one per stream): their token tiles
   // and k splits are chosen together for the shared GPU
   GemmArgs joint[kSideStreams + 1];
-  const bool together = ss && np >= 2 && np <= kSideStreams + 1;
+  int order[kSideStreams + 1];
+  bool together = ss && np >= 2 && np <= kSideStreams + 1;
   if (together) {
     for (int i = 0, j = 0; i < count; ++i)
       if (d[i].M > 16)
         joint[j++] = plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
                                 d[i].bits, d[i].group, d[i].ldw, d[i].workspace, d[i].workspace_bytes);
-    plan_prefill_joint(joint, np);
+    together = plan_prefill_joint(joint, np, order);
   }
   tlq_status st = TLQ_OK;
-  for (int i = 0, j = 0; i < count && st == TLQ_OK; ++i) {
-    if (d[i].M <= 16) continue;
-    const int lane = used ? j % (used + 1) : 0;  // 0: the caller's stream
-    const cudaStream_t ls = lane ? ss->s[lane - 1] : stream;
-    if (together)
-      st = launch_prefill(joint[j], ls);
-    else
+  if (together) {  // the jointly planned launches, the longest first
+    for (int j = 0; j < np && st == TLQ_OK; ++j)
+      st = launch_prefill(joint[order[j]], j % (used + 1) ? ss->s[j % (used + 1) - 1] : stream);
+  } else {
+    for (int i = 0, j = 0; i < count && st == TLQ_OK; ++i) {
+      if (d[i].M <= 16) continue;
+      const int lane = used ? j % (used + 1) : 0;  // 0: the caller's stream
       st = launch_prefill(plain_args(d[i].A, d[i].Wpacked, d[i].scales, d[i].zeros, d[i].C, d[i].M, d[i].N, d[i].K,
                                      d[i].bits, d[i].group, d[i].ldw, d[i].workspace, d[i].workspace_bytes),
-                          ls);
-    ++j;
+                          lane ? ss->s[lane - 1] : stream);
+      ++j;
+    }
   }
   for (int k = 0; k < used; ++k) {  // join even after a failed launch
     cudaError_t e = cudaEventRecord(ss->join[k], ss->s[k]);

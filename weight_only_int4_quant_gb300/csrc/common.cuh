@@ -295,9 +295,10 @@ tlq_status launch_prefill(const GemmArgs& a, cudaStream_t stream);
 // an unlimited workspace (0: it would not split K).
 size_t prefill_workspace_bytes(const GemmArgs& a);
 // Plans of n prefill problems that will run side by side (the batched call's
-// side streams): sets every a[i].plan_nmt / plan_ks.  Returns false (and
-// leaves the plans unset) when it does not plan jointly.
-bool plan_prefill_joint(GemmArgs* a, int n);
+// side streams): sets every a[i].plan_nmt / plan_ks, and order[] to the
+// order to launch them in (the longest first).  Returns false (and leaves
+// the plans unset) when it does not plan jointly.
+bool plan_prefill_joint(GemmArgs* a, int n, int* order);
 // The device as the prefill planners see it: SMs, and for one and two token
 // tiles per CTA the clusters of 1, 2, 4 and 8 CTAs that fit at once.
 struct PlanDevice {
