@@ -148,6 +148,50 @@ def test_decode_unit_heights_bitwise(lib, monkeypatch, bits, group, N, K, M):
         assert np.array_equal(outs[rows].view(np.uint16), outs["16"].view(np.uint16)), rows
 
 
+@pytest.mark.parametrize("bits,group,N,K", [(4, 128, 200, 2048), (4, 256, 96, 1024), (4, 512, 64, 8192),
+                                            (4, 128, 2048, 8192), (2, 64, 136, 2048), (2, 128, 72, 768),
+                                            (2, 64, 2048, 8192)])
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_decode_fixed_forms_bitwise(lib, monkeypatch, bits, group, N, K, M):
+    """INT4 launches whose groups are multiples of 128 codes run the decode
+    kernel built for whole four-set spans only, INT2 launches with whole
+    k-blocks (K a multiple of 256) the one without the ragged-k-block body;
+    TLQ_DECODE_GENERIC=1 forces the general kernel.  All give the same bits,
+    and the oracle agrees."""
+    case = synth.gemm_case(M, N, K, bits, group, seed=3 * M + N + K)
+    outs = {}
+    for generic in ("1", "0"):
+        monkeypatch.setenv("TLQ_DECODE_GENERIC", generic)
+        _, outs[generic] = run_case(lib, case)
+    ref = oracle.quant_gemm(case["A"], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits, group)
+    assert_close(outs["0"], ref, "fixed-form kernel int%d g%d M%d N%d K%d" % (bits, group, M, N, K))
+    assert np.array_equal(outs["0"].view(np.uint16), outs["1"].view(np.uint16))
+
+
+def test_decode_batch_mixing_group_classes_bitwise(lib):
+    """A batched INT4 decode call whose problems all have groups of 128 or 256
+    takes the whole-span kernel; adding one problem with groups of 64 sends
+    the whole batch to the general kernel.  Every problem's output is the same
+    bits either way, and the oracle agrees."""
+    specs = [(1, 256, 2048, 4, 128), (16, 192, 1024, 4, 256), (4, 320, 4096, 4, 128), (9, 160, 768, 4, 64)]
+    probs = _problems(specs, seed=11)
+    descs = lambda ps: [(p["A"], p["W"], p["s"], p["z"], p["C"], 4, p["case"]["group"]) for p in ps]
+    lib.tl_quant_gemm_batched(descs(probs[:3]))
+    torch.cuda.synchronize()
+    whole = [p["C"].clone() for p in probs[:3]]
+    for p in probs:
+        p["C"].zero_()
+    lib.tl_quant_gemm_batched(descs(probs))
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+    for i in range(3):
+        assert torch.equal(whole[i].view(torch.int16), probs[i]["C"].view(torch.int16)), i
+    for p in probs:
+        c = p["case"]
+        ref = oracle.quant_gemm(c["A"], oracle.pack(c["codes"], 4), c["scales"], c["zeros"], 4, c["group"])
+        assert_close(p["C"].cpu().numpy(), ref, "batch g%d" % c["group"])
+
+
 # ---------------------------------------------------------------------------
 # full-size decode configurations (the four D = 2048 projections): every
 # output against the oracle

@@ -332,6 +332,28 @@ __device__ __forceinline__ void load_acts(const UnitRegs& ur, int kb, uint4 (&ax
   }
 }
 
+// Packed FP32 pairs (sm_100 family): one instruction applies the same IEEE
+// operation, rounded to nearest, to both halves, so the results are those of
+// the scalar operations.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // One k-block (4 sets) of one warp: MMAs over the span(s), correction, and
 // the scaled accumulation into tot.  SPANQ: sets per span (4, 2, 1), or 0 when
 // the group size is not a multiple of the set width pattern (each set then
@@ -443,13 +465,33 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
                                       lds_half(za + (uint32_t)(16 * r * ur.gp) * 2));
         const float2 fh = make_float2(lds_half(sa + (uint32_t)((16 * r + 8) * ur.gp) * 2),
                                       lds_half(za + (uint32_t)((16 * r + 8) * ur.gp) * 2));
+        // acc + corr0 + z * corr2 = sum a (q - z); then * s.  The two tokens
+        // of a lane's pair share s and z, so they go through packed pairs
+        // (the same bits as the scalar form below).  The INT2 two-tile body
+        // keeps the scalar form: packed, it spilled registers (measured
+        // slower); elsewhere packed pairs were 1 % (INT4) and 2.5 % (INT2
+        // step) faster.
+        if constexpr (BITS == 4 || NTP == 1) {
+          const uint64_t SG = f2pack(fg.x, fg.x), ZG = f2pack(fg.y, fg.y);
+          const uint64_t SH = f2pack(fh.x, fh.x), ZH = f2pack(fh.y, fh.y);
 #pragma unroll
-        for (int t = 0; t < NTP; ++t) {
-          // acc + corr0 + z * corr2 = sum a (q - z); then * s
-          tot[r][t][0] = fmaf(fg.x, fmaf(fg.y, corr[t][2], acc[r][t][0] + corr[t][0]), tot[r][t][0]);
-          tot[r][t][1] = fmaf(fg.x, fmaf(fg.y, corr[t][3], acc[r][t][1] + corr[t][1]), tot[r][t][1]);
-          tot[r][t][2] = fmaf(fh.x, fmaf(fh.y, corr[t][2], acc[r][t][2] + corr[t][0]), tot[r][t][2]);
-          tot[r][t][3] = fmaf(fh.x, fmaf(fh.y, corr[t][3], acc[r][t][3] + corr[t][1]), tot[r][t][3]);
+          for (int t = 0; t < NTP; ++t) {
+            const uint64_t c01 = f2pack(corr[t][0], corr[t][1]), c23 = f2pack(corr[t][2], corr[t][3]);
+            const uint64_t t01 = f2fma(SG, f2fma(ZG, c23, f2add(f2pack(acc[r][t][0], acc[r][t][1]), c01)),
+                                       f2pack(tot[r][t][0], tot[r][t][1]));
+            const uint64_t t23 = f2fma(SH, f2fma(ZH, c23, f2add(f2pack(acc[r][t][2], acc[r][t][3]), c01)),
+                                       f2pack(tot[r][t][2], tot[r][t][3]));
+            f2unpack(t01, tot[r][t][0], tot[r][t][1]);
+            f2unpack(t23, tot[r][t][2], tot[r][t][3]);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < NTP; ++t) {
+            tot[r][t][0] = fmaf(fg.x, fmaf(fg.y, corr[t][2], acc[r][t][0] + corr[t][0]), tot[r][t][0]);
+            tot[r][t][1] = fmaf(fg.x, fmaf(fg.y, corr[t][3], acc[r][t][1] + corr[t][1]), tot[r][t][1]);
+            tot[r][t][2] = fmaf(fh.x, fmaf(fh.y, corr[t][2], acc[r][t][2] + corr[t][0]), tot[r][t][2]);
+            tot[r][t][3] = fmaf(fh.x, fmaf(fh.y, corr[t][3], acc[r][t][3] + corr[t][1]), tot[r][t][3]);
+          }
         }
       }
     }
@@ -460,7 +502,7 @@ __device__ __forceinline__ void kblock(const UnitRegs& ur, int kb, uint32_t wq0,
 // in nx/ny (NT tiles): on entry they hold this warp's first k-block of the
 // unit, on exit the first k-block of the next unit (nu), so no unit starts
 // on an exposed global load.
-template <int BITS, int RGW, int NTP, int SPANQ, int NT>
+template <int BITS, int RGW, int NTP, int SPANQ, int NT, bool ALLFULL>
 __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const Sched* tab, const UnitRegs& ur,
                                          const UnitRegs& nu, bool has_next, int warp, int lane,
                                          const uint32_t (&woff)[5], uint32_t ring_base, uint8_t* ring,
@@ -491,7 +533,7 @@ __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const Sched* tab
     const int slot = warp * kSPW + (consumed % kSPW);
     if (ok) ok = mbar_wait(&full[slot], (consumed / kSPW) & 1, 0x112);
     __syncwarp();  // the lanes leave the wait separately; the MMAs below are warp-collective
-    if (kb < ur.nkb_full)
+    if (ALLFULL || kb < ur.nkb_full)
       kblock<BITS, RGW, NTP, SPANQ, true>(ur, kb, ring_base + (uint32_t)slot * STAGE_BYTES, woff, g, ax, ay, tot);
     else
       kblock<BITS, RGW, NTP, SPANQ, false>(ur, kb, ring_base + (uint32_t)slot * STAGE_BYTES, woff, g, ax, ay, tot);
@@ -506,7 +548,14 @@ __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const Sched* tab
   if (warp >= ur.nkb && has_next && warp < nu.nkb) load_acts<BITS, NT>(nu, warp, nx, ny);
 }
 
-template <int BITS, int RGW, int NT>
+// SQ = 0: the group class (sets per span) is chosen per unit at run time;
+// SQ = 4: every problem of the launch has four sets per span (INT4, groups of
+// a multiple of 128 codes).  WHOLE: every problem's K is a whole number of
+// k-blocks, so the body for a ragged last k-block is left out.  The arithmetic
+// is the same in every form; leaving out the code that cannot run shrinks the
+// loop the SMs fetch instructions for (measured on the decode steps: INT4
+// 3028 -> 3176 GB/s with SQ = 4, INT2 1668 -> 1693 GB/s with WHOLE).
+template <int BITS, int RGW, int NT, int SQ, bool WHOLE>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeLaunch L) {
   constexpr int ROWS = 16 * RGW;
   constexpr int STAGE_BYTES = ROWS * kStageRowBytes;
@@ -653,21 +702,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if constexpr (NT == 2) {
       if (M > 8) {
         done = true;
-        switch (spanq) {
-          case 4: run_unit<BITS, RGW, 2, 4, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
-          case 2: run_unit<BITS, RGW, 2, 2, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
-          case 1: run_unit<BITS, RGW, 2, 1, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
-          default: run_unit<BITS, RGW, 2, 0, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+        if constexpr (SQ == 4) {
+          run_unit<BITS, RGW, 2, 4, NT, true>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot);
+        } else {
+          switch (spanq) {
+            case 4: run_unit<BITS, RGW, 2, 4, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+            case 2: run_unit<BITS, RGW, 2, 2, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+            case 1: run_unit<BITS, RGW, 2, 1, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+            default: run_unit<BITS, RGW, 2, 0, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot); break;
+          }
         }
       }
     }
     if (!done) {
       float t1[RGW][1][4];
-      switch (spanq) {
-        case 4: run_unit<BITS, RGW, 1, 4, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
-        case 2: run_unit<BITS, RGW, 1, 2, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
-        case 1: run_unit<BITS, RGW, 1, 1, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
-        default: run_unit<BITS, RGW, 1, 0, NT>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+      if constexpr (SQ == 4) {
+        run_unit<BITS, RGW, 1, 4, NT, true>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1);
+      } else {
+        switch (spanq) {
+          case 4: run_unit<BITS, RGW, 1, 4, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+          case 2: run_unit<BITS, RGW, 1, 2, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+          case 1: run_unit<BITS, RGW, 1, 1, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+          default: run_unit<BITS, RGW, 1, 0, NT, WHOLE>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1); break;
+        }
       }
 #pragma unroll
       for (int r = 0; r < RGW; ++r)
@@ -892,7 +949,7 @@ tlq_status build_launch(const GemmArgs* a, int count, DecodeLaunch& L, size_t& s
 // costs more host time than the launch itself.
 constexpr int kLaunchCache = 8;
 
-template <int BITS, int RGW, int NT>
+template <int BITS, int RGW, int NT, int SQ, bool WHOLE>
 tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   constexpr int ROWS = 16 * RGW;
   static_assert(sizeof(DecodeLaunch) < 30000, "kernel parameter space");
@@ -907,7 +964,7 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   static std::mutex mu;
   static Entry cache[kLaunchCache];
   static int next = 0;
-  auto kern = decode_kernel<BITS, RGW, NT>;
+  auto kern = decode_kernel<BITS, RGW, NT, SQ, WHOLE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -953,8 +1010,8 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   cudaError_t e = cudaLaunchKernelEx(&lc, kern, L);
   if (e != cudaSuccess) return cuda_error(e, "decode: launch");
   if (log_enabled())
-    fprintf(stderr, "[tlq] decode int%d: %d problem(s), %d units of %d rows, grid %d, smem %zu\n", BITS, count, units,
-            ROWS, grid, smem);
+    fprintf(stderr, "[tlq] decode int%d: %d problem(s), %d units of %d rows, grid %d, smem %zu%s\n", BITS, count,
+            units, ROWS, grid, smem, SQ ? ", whole k-blocks of 4-set spans" : WHOLE ? ", whole k-blocks" : "");
   return TLQ_OK;
 }
 
@@ -995,6 +1052,33 @@ int decode_rgw(const GemmArgs* a, int count) {
   return rgw;
 }
 
+// Kernel forms: INT4 launches whose groups are all multiples of 128 codes
+// (four sets per span, which also makes every k-block whole) take the form
+// with one k-block body per token-tile count; INT2 launches whose K are all
+// whole k-blocks (256 codes) take the form without the ragged-k-block body.
+// (An INT2 form with one group class spilled registers and measured 0.6 %
+// slower.)  Everything else takes the general form.  TLQ_DECODE_GENERIC=1
+// forces the general form.
+template <int BITS>
+bool decode_fixed_form(const GemmArgs* a, int count) {
+  if (const char* e = getenv("TLQ_DECODE_GENERIC"))
+    if (atoi(e) != 0) return false;
+  for (int i = 0; i < count; ++i) {
+    if (a[i].K % Fmt<BITS>::KBLK != 0) return false;
+    if (BITS == 4 && a[i].group % (4 * Fmt<BITS>::SETC) != 0) return false;
+  }
+  return true;
+}
+
+template <int BITS, int RGW, int NT>
+tlq_status launch_sq(const GemmArgs* a, int count, cudaStream_t s) {
+  if (decode_fixed_form<BITS>(a, count)) {
+    if constexpr (BITS == 4) return launch_impl<BITS, RGW, NT, 4, true>(a, count, s);
+    else return launch_impl<BITS, RGW, NT, 0, true>(a, count, s);
+  }
+  return launch_impl<BITS, RGW, NT, 0, false>(a, count, s);
+}
+
 // One launch per call: the two-token-tile kernel when any problem has M > 8
 // (its problems with M <= 8 take the one-tile path inside it).  Splitting the
 // call into a one-tile and a two-tile launch was measured slower for the INT4
@@ -1004,13 +1088,18 @@ tlq_status dispatch_bits(const GemmArgs* a, int count, cudaStream_t s) {
   bool two = false;
   for (int i = 0; i < count; ++i) two |= a[i].M > 8;
   switch (decode_rgw<BITS>(a, count)) {
-    case 1: return two ? launch_impl<BITS, 1, 2>(a, count, s) : launch_impl<BITS, 1, 1>(a, count, s);
-    case 2: return two ? launch_impl<BITS, 2, 2>(a, count, s) : launch_impl<BITS, 2, 1>(a, count, s);
-    default: return two ? launch_impl<BITS, 4, 2>(a, count, s) : launch_impl<BITS, 4, 1>(a, count, s);
+    case 1: return two ? launch_sq<BITS, 1, 2>(a, count, s) : launch_sq<BITS, 1, 1>(a, count, s);
+    case 2: return two ? launch_sq<BITS, 2, 2>(a, count, s) : launch_sq<BITS, 2, 1>(a, count, s);
+    default: return two ? launch_sq<BITS, 4, 2>(a, count, s) : launch_sq<BITS, 4, 1>(a, count, s);
   }
 }
 
 }  // namespace
+
+#ifndef TLQ_DECODE_INT2_UNIT
+// The INT2 forms are compiled in decode_int2.cu (this file again, with
+// TLQ_DECODE_INT2_UNIT defined), so that the two bit widths build in parallel.
+tlq_status launch_decode_int2(const GemmArgs* a, int count, cudaStream_t stream);
 
 tlq_status launch_decode(const GemmArgs* a, int count, cudaStream_t stream) {
   if (count < 1 || count > kMaxProblems)
@@ -1019,7 +1108,12 @@ tlq_status launch_decode(const GemmArgs* a, int count, cudaStream_t stream) {
     if (a[i].M < 1 || a[i].M > 16) return set_error(TLQ_EINVAL, "decode: M=%d outside 1..16", a[i].M);
     if (a[i].bits != a[0].bits) return set_error(TLQ_EINVAL, "decode: mixed bit widths in one launch");
   }
-  return a[0].bits == 4 ? dispatch_bits<4>(a, count, stream) : dispatch_bits<2>(a, count, stream);
+  return a[0].bits == 4 ? dispatch_bits<4>(a, count, stream) : launch_decode_int2(a, count, stream);
 }
+#else
+tlq_status launch_decode_int2(const GemmArgs* a, int count, cudaStream_t stream) {
+  return dispatch_bits<2>(a, count, stream);
+}
+#endif
 
 }  // namespace tlq
