@@ -49,7 +49,9 @@
  *    launch off; TLQ_PREFILL_NMT=1|2, TLQ_PREFILL_KSPLIT=1|2|4|8 and
  *    TLQ_DECODE_ROWS=16|32|64 force the kernels' tiling choices (for tests
  *    and measurements; the results of the decode kernel do not depend on
- *    TLQ_DECODE_ROWS).
+ *    TLQ_DECODE_ROWS); TLQ_DECODE_GENERIC=1 and TLQ_PREFILL_GENERIC=1 force
+ *    the kernels' general forms instead of the forms built for whole blocks
+ *    (the same results, bit for bit).
  */
 #ifndef TLQ_H_
 #define TLQ_H_

@@ -168,6 +168,35 @@ def test_decode_fixed_forms_bitwise(lib, monkeypatch, bits, group, N, K, M):
     assert np.array_equal(outs["0"].view(np.uint16), outs["1"].view(np.uint16))
 
 
+@pytest.mark.parametrize("bits,group,M,N,K,ks", [(4, 128, 128, 512, 2048, 1), (4, 128, 40, 256, 4096, 4),
+                                                 (4, 256, 300, 768, 4096, 2), (2, 64, 200, 512, 2048, 1),
+                                                 (2, 128, 129, 256, 8192, 8), (4, 128, 2048, 2048, 2048, 1)])
+def test_prefill_lean_form_bitwise(lib, monkeypatch, bits, group, M, N, K, ks):
+    """Prefill launches with whole stages and row tiles, vector scales/zeros
+    and a power-of-two group take the lean kernel form;
+    TLQ_PREFILL_GENERIC=1 forces the general one.  Both give the same bits,
+    with and without a k split, and the oracle agrees."""
+    case = synth.gemm_case(M, N, K, bits, group, seed=M + N + K + ks, a_scale=0.5)
+    monkeypatch.setenv("TLQ_PREFILL_KSPLIT", str(ks))
+    Wd = gpu_pack(lib, case["codes"], bits)
+    A, s, z = dev(case["A"]), dev(case["scales"]), dev(case["zeros"])
+    wsb = lib.tl_quant_gemm_workspace_size(M, N, K, bits, group)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    outs = {}
+    for generic in ("1", "0"):
+        monkeypatch.setenv("TLQ_PREFILL_GENERIC", generic)
+        C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        lib.tl_quant_gemm_ws(A, Wd, s, z, C, bits, group, ws)
+        torch.cuda.synchronize()
+        lib.tl_check_status()
+        outs[generic] = C.cpu().numpy()
+    assert np.array_equal(outs["0"].view(np.uint16), outs["1"].view(np.uint16))
+    rows = sample_rows(M, 24, np.random.default_rng(K))
+    ref = oracle.quant_gemm(case["A"][rows], oracle.pack(case["codes"], bits), case["scales"], case["zeros"], bits,
+                            group)
+    assert_close(outs["0"][rows], ref, "lean prefill int%d g%d M%d N%d K%d ks%d" % (bits, group, M, N, K, ks))
+
+
 def test_decode_batch_mixing_group_classes_bitwise(lib):
     """A batched INT4 decode call whose problems all have groups of 128 or 256
     takes the whole-span kernel; adding one problem with groups of 64 sends
