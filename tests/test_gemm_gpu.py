@@ -453,6 +453,27 @@ def test_batched_equals_separate_calls_bitwise(lib):
         assert_close(p["C"].cpu().numpy()[rows], ref, "batched M%d N%d K%d" % (M, N, K))
 
 
+def test_batched_int2_decode_step_bitwise(lib):
+    """The INT2 decode step (the four projections at M = 1, 4, 16, group 64)
+    as one batched launch: the same bits as one call per problem, and a
+    sample of rows against the oracle."""
+    specs = [(M, N, K, 2, 64) for M in (1, 4, 16) for (N, K) in synth.SHAPES.values()]
+    probs = _problems(specs, seed=70)
+    lib.tl_quant_gemm_batched([(p["A"], p["W"], p["s"], p["z"], p["C"], 2, 64) for p in probs])
+    torch.cuda.synchronize()
+    lib.tl_check_status()
+    for p, (M, N, K, bits, group) in zip(probs, specs):
+        single = lib.quant_gemm(p["A"], p["W"], p["s"], p["z"], bits, group)
+        assert torch.equal(single.view(torch.int16), p["C"].view(torch.int16)), (M, N, K)
+    rng = np.random.default_rng(7)
+    for p, (M, N, K, bits, group) in zip(probs, specs):
+        rows = sample_rows(M, 4, rng)
+        c = p["case"]
+        ref = oracle.quant_gemm(c["A"][rows], p["W"].cpu().numpy().view(np.uint32), c["scales"], c["zeros"], bits,
+                                group)
+        assert_close(p["C"].cpu().numpy()[rows], ref, "batched int2 M%d N%d K%d" % (M, N, K))
+
+
 def test_batched_prefill_side_streams_in_a_graph(lib):
     """The prefill problems of one batched call run side by side on side
     streams forked from the caller's stream.  A CUDA graph captured on that

@@ -550,7 +550,8 @@ __device__ __forceinline__ void run_unit(const DecodeLaunch& L, const Sched* tab
 
 // SQ = 0: the group class (sets per span) is chosen per unit at run time;
 // SQ = 4: every problem of the launch has four sets per span (INT4, groups of
-// a multiple of 128 codes).  WHOLE: every problem's K is a whole number of
+// a multiple of 128 codes); SQ = 1: one set per span (INT2, groups of 64
+// codes).  WHOLE: every problem's K is a whole number of
 // k-blocks, so the body for a ragged last k-block is left out.  The arithmetic
 // is the same in every form; leaving out the code that cannot run shrinks the
 // loop the SMs fetch instructions for (measured on the decode steps: INT4
@@ -702,7 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if constexpr (NT == 2) {
       if (M > 8) {
         done = true;
-        if constexpr (SQ == 4) {
+        if constexpr (SQ == 1) {
+          run_unit<BITS, RGW, 2, 1, NT, true>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot);
+        } else if constexpr (SQ == 4) {
           run_unit<BITS, RGW, 2, 4, NT, true>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, tot);
         } else {
           switch (spanq) {
@@ -716,7 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     if (!done) {
       float t1[RGW][1][4];
-      if constexpr (SQ == 4) {
+      if constexpr (SQ == 1) {
+        run_unit<BITS, RGW, 1, 1, NT, true>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1);
+      } else if constexpr (SQ == 4) {
         run_unit<BITS, RGW, 1, 4, NT, true>(L, tab, ur, nu, has_next, warp, lane, woff, ring_base, ring, full, pol, prod, consumed, ok, nx, ny, t1);
       } else {
         switch (spanq) {
@@ -1011,7 +1016,9 @@ tlq_status launch_impl(const GemmArgs* a, int count, cudaStream_t stream) {
   if (e != cudaSuccess) return cuda_error(e, "decode: launch");
   if (log_enabled())
     fprintf(stderr, "[tlq] decode int%d: %d problem(s), %d units of %d rows, grid %d, smem %zu%s\n", BITS, count,
-            units, ROWS, grid, smem, SQ ? ", whole k-blocks of 4-set spans" : WHOLE ? ", whole k-blocks" : "");
+            units, ROWS, grid, smem,
+            SQ == 4 ? ", whole k-blocks of 4-set spans" : SQ == 1 ? ", whole k-blocks of 1-set spans"
+                                                         : WHOLE ? ", whole k-blocks" : "");
   return TLQ_OK;
 }
 
@@ -1055,10 +1062,10 @@ int decode_rgw(const GemmArgs* a, int count) {
 // Kernel forms: INT4 launches whose groups are all multiples of 128 codes
 // (four sets per span, which also makes every k-block whole) take the form
 // with one k-block body per token-tile count; INT2 launches whose K are all
-// whole k-blocks (256 codes) take the form without the ragged-k-block body.
-// (An INT2 form with one group class spilled registers and measured 0.6 %
-// slower.)  Everything else takes the general form.  TLQ_DECODE_GENERIC=1
-// forces the general form.
+// whole k-blocks (256 codes) take the form without the ragged-k-block body,
+// and with one k-block body per token-tile count when every group is 64 codes
+// (one set per span).  Everything else takes the general form.
+// TLQ_DECODE_GENERIC=1 forces the general form.
 template <int BITS>
 bool decode_fixed_form(const GemmArgs* a, int count) {
   if (const char* e = getenv("TLQ_DECODE_GENERIC"))
@@ -1072,8 +1079,11 @@ bool decode_fixed_form(const GemmArgs* a, int count) {
 
 template <int BITS, int RGW, int NT>
 tlq_status launch_sq(const GemmArgs* a, int count, cudaStream_t s) {
+  bool one_set_spans = BITS == 2;
+  for (int i = 0; i < count; ++i) one_set_spans &= a[i].group == Fmt<BITS>::SETC;
   if (decode_fixed_form<BITS>(a, count)) {
     if constexpr (BITS == 4) return launch_impl<BITS, RGW, NT, 4, true>(a, count, s);
+    else if (one_set_spans) return launch_impl<BITS, RGW, NT, 1, true>(a, count, s);
     else return launch_impl<BITS, RGW, NT, 0, true>(a, count, s);
   }
   return launch_impl<BITS, RGW, NT, 0, false>(a, count, s);
